@@ -1,0 +1,50 @@
+// Internal declarations shared by the translation units of libpw.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include <cuda_runtime.h>
+
+#include "pw.h"
+
+namespace pw {
+
+// Device descriptor of one linear-block at its committed bitwidth (128 bytes).
+// Written by pw_page_table_sync, read by the fused kernels.
+struct alignas(16) BlockDesc {
+  int32_t q;        // committed bitwidth (0 = not committed)
+  int32_t rows;     // N
+  int32_t cols;     // K
+  int32_t parent;   // P
+  int32_t seed;     // S
+  int32_t layout;
+  int32_t pad0, pad1;
+  const uint32_t* planes[PW_MAX_BITS];  // planes 0..q-1 (MSB first); rest NULL
+  const uint16_t* lut;                  // LUT_q, fp16 [rows][2^q]
+  int64_t pad2[3];
+};
+static_assert(sizeof(BlockDesc) == 128, "descriptor must stay 128 bytes");
+
+constexpr int kTileRows = 16;
+constexpr int kTileCols = 256;
+constexpr int kTileBytes = 512;
+
+// Records a message for pw_last_error() and returns `code`.
+int set_error(int code, const char* fmt, ...);
+void clear_error();
+int cuda_error(cudaError_t e, const char* what);
+
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+// Host-side descriptor of `block` of a page table, at its committed bitwidth
+// (or at `bits_override` if > 0); fails unless the planes are attached.
+int table_block(const pw_page_table* t, int block, BlockDesc* out, int bits_override);
+
+}  // namespace pw
+
+#define PW_CUDA_TRY(expr)                                  \
+  do {                                                     \
+    cudaError_t pw_e_ = (expr);                            \
+    if (pw_e_ != cudaSuccess) return pw::cuda_error(pw_e_, #expr); \
+  } while (0)

@@ -1,0 +1,233 @@
+/*
+ * pw.h -- C ABI of libpw, the GB300 (sm_103a) library for the data-parallel hot
+ * path of PagedWeight's fused mixed-precision Any-Precision MoE expert layer.
+ *
+ * Source of every operation: "PagedWeight: Efficient MoE LLM Serving with
+ * Dynamic Quality-Aware Weight Quantization" (arXiv text).  Section, equation
+ * and figure are cited beside each call.
+ *
+ * Conventions
+ *  - Every call returns int: PW_OK (0) or a negative PW_ERR_* code; the
+ *    message of the last failure on the calling thread is pw_last_error().
+ *    No C++ exception crosses this boundary.
+ *  - Arguments are validated on the host before anything is enqueued.
+ *  - Device memory is always caller-owned.  libpw never allocates or frees
+ *    device memory; scratch space is a caller-provided workspace.
+ *  - "stream" is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream).  Device work is enqueued on it and the call returns without
+ *    synchronising.  Pointers named d_* are device pointers; h_* are host.
+ *  - fp16 data is IEEE binary16 passed as uint16_t.
+ *  - Failures that only the device can see (a wait that ran out, a block that
+ *    is routed to but not committed) are written to a caller-provided int32
+ *    status word in device memory (d_status) with the PW_ERR_* code; the
+ *    caller reads it after synchronising.  The kernels never trap.
+ *  - The page table is host state and is not thread-safe.
+ */
+#ifndef PW_H_
+#define PW_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define PW_OK 0
+#define PW_ERR_INVALID_ARG (-1)
+#define PW_ERR_UNSUPPORTED (-2)   /* bitwidth or shape this library does not handle */
+#define PW_ERR_NOT_RESIDENT (-3)  /* a page needed for the requested bitwidth is not attached */
+#define PW_ERR_CUDA (-4)          /* a CUDA runtime call failed; see pw_last_error() */
+#define PW_ERR_TIMEOUT (-5)       /* a bounded in-kernel wait ran out (device status only) */
+#define PW_ERR_WORKSPACE (-6)     /* workspace too small or misaligned */
+
+#define PW_MAX_BITS 8
+#define PW_LAYOUT_TILED 1
+
+/* Message describing the last failure on this thread ("" if none). */
+const char* pw_last_error(void);
+
+/* ------------------------------------------------------------------------ */
+/* Bit-plane packer (§1 and Figure 3: the overlaid bit-plane format)          */
+/* ------------------------------------------------------------------------ */
+
+/* Bytes of one bit-plane of a rows x cols block in `layout` (= rows*cols/8).
+ * Returns 0 if the shape is not supported: the tiled layout needs
+ * rows % 16 == 0 and cols % 256 == 0. */
+size_t pw_plane_bytes(int64_t rows, int64_t cols, int layout);
+
+/* Split parent-bit indices into bit-planes.
+ *  d_idx       device uint8 [rows][cols], row-major, every value < 2^parent_bits
+ *  parent_bits P in 1..8
+ *  h_planes    HOST array of P device pointers, each to pw_plane_bytes() bytes,
+ *              16-byte aligned; plane 0 receives the most significant bit, so
+ *              the top b planes hold the b-bit index idx >> (P - b)
+ *  layout      PW_LAYOUT_TILED (the only layout), defined element by element:
+ *                half = n / (rows/2), r = n % (rows/2), strip = r / 8, g = r % 8
+ *                tile = j / 256, jj = j % 256, step = jj / 16, t = jj % 16
+ *                c = (t % 8) / 2, odd = t % 2, upper = t / 8
+ *                lane = 4g + c, elem = 4*half + 2*upper + odd
+ *                bit (n, j) is bit 4*elem + step%4 of the little-endian uint32
+ *                at byte (strip*(cols/256) + tile)*512 + 16*lane + 4*(step/4)
+ *              i.e. 16-row x 256-column tiles of 512 bytes, strip-major; lane l
+ *              of a warp loads the 16 bytes at 16*l of a tile and holds exactly
+ *              the elements of its m16n8k16 A-fragments for 16 k-steps.
+ * Values >= 2^P are masked to their low P bits.  Asynchronous on `stream`. */
+int pw_pack_bitplanes(const uint8_t* d_idx, int64_t rows, int64_t cols, int parent_bits,
+                      uint32_t* const* h_planes, int layout, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Weight page table (§3 and §3.1; Eq. 3)                                      */
+/* ------------------------------------------------------------------------ */
+
+/* Shape and supported bitwidths B_i = {seed_bits .. parent_bits} of one
+ * per-expert linear-block i = (layer, expert, gate_up|down). */
+typedef struct pw_block_info {
+  int64_t rows;      /* output rows N (gate_up: 2I, down: H) */
+  int64_t cols;      /* input columns K (gate_up: H, down: I) */
+  int32_t parent_bits;
+  int32_t seed_bits;
+  int32_t layout;    /* PW_LAYOUT_TILED */
+  int32_t reserved;
+} pw_block_info;
+
+typedef struct pw_page_table pw_page_table;
+
+/* Bytes of the device descriptor array for n_blocks blocks (see _sync). */
+size_t pw_desc_bytes(int n_blocks);
+
+/* Create a table of n_blocks rows.  Block ids are chosen by the caller; the
+ * fused layer reads block (layer*E + e)*2 + u, u = 0 gate_up, 1 down.
+ * Every block starts uncommitted (q = 0, d = 0) with no pages attached. */
+int pw_page_table_create(pw_page_table** out, int n_blocks, const pw_block_info* h_info);
+int pw_page_table_destroy(pw_page_table* t);
+
+/* Attach (borrow) the device buffer of bit-plane `plane` (0 = MSB) of a block;
+ * marks that plane GPU-resident.  The buffer must stay valid while attached. */
+int pw_page_table_attach_plane(pw_page_table* t, int block, int plane, const uint32_t* d_plane);
+
+/* Attach the LUT of bitwidth `bits` (seed..parent): fp16 [rows][2^bits],
+ * 16-byte aligned, one row of centroids per output row (Figure 3 caption). */
+int pw_page_table_attach_lut(pw_page_table* t, int block, int bits, const uint16_t* d_lut);
+
+/* Record the planner's desired bitwidth d_i (bookkeeping; §3: q_i, not d_i,
+ * is what inference uses).  d must be in B_i. */
+int pw_page_table_set_desired(pw_page_table* t, int block, int d);
+
+/* Commit q_i = q (§3.1 and §3.3 ordering rules).
+ *  Lowering (q < q_i): commits q at once; planes q..P-1 and LUTs q+1..P become
+ *  unreferenced, are detached, and are reported in *released_mask (bit p for
+ *  plane p, bit 8+b for the LUT of bitwidth b) so the caller can free them
+ *  once the stream has passed every launch that used them.  The planes below
+ *  q are not touched.
+ *  Raising (q > q_i): only allowed once planes 0..q-1 and the LUTs seed..q are
+ *  attached (reload first, then raise); otherwise PW_ERR_NOT_RESIDENT and
+ *  nothing changes.  q must be in B_i.  released_mask may be NULL. */
+int pw_page_table_set_bits(pw_page_table* t, int block, int q, uint64_t* released_mask);
+
+/* Committed q_i, desired d_i and the attached-page mask (bit p plane p,
+ * bit 8+b LUT b) of a block; any out pointer may be NULL. */
+int pw_page_table_get(const pw_page_table* t, int block, int* q, int* d, uint64_t* resident_mask);
+
+/* M_i^b of Eq. 3: bytes block i holds on the GPU at bitwidth b -- b planes of
+ * rows*cols/8 bytes plus the fp16 LUTs of every bitwidth seed..b.  Returns -1
+ * for an invalid block or b outside B_i. */
+int64_t pw_page_table_bytes(const pw_page_table* t, int block, int b);
+
+/* Sum over blocks of M_i^{q_i} (uncommitted blocks count 0). */
+int64_t pw_page_table_resident_bytes(const pw_page_table* t);
+
+/* Upload the descriptors of all blocks (committed q, plane and LUT_q
+ * pointers, shape) to d_desc (pw_desc_bytes(n_blocks) bytes, 16-byte aligned)
+ * with an asynchronous copy on `stream`.  The fused kernels read only this
+ * array, so a commit becomes visible to launches enqueued after the sync. */
+int pw_page_table_sync(pw_page_table* t, void* d_desc, size_t desc_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Routing (§2.1: top-K experts per token; Eq. 1: routing mass)                */
+/* ------------------------------------------------------------------------ */
+
+/* Top-k routing of fp32 logits [T][E] (finite values), one launch:
+ *  d_ids     int32 [T][k]   chosen experts by decreasing logit, ties to the
+ *                           lower expert index
+ *  d_w       fp32  [T][k]   softmax probabilities renormalised over the k picks
+ *  d_offsets int32 [E+1]    offsets[e] = first position of expert e
+ *  d_perm    int32 [T*k]    perm[pos] = slot t*k+j, positions ordered by
+ *                           (expert, token, j)
+ *  d_inv_perm int32 [T*k]   inverse of perm
+ *  d_mass_accum fp32 [E] or NULL: adds sum_t sum_j w[t][j]*[ids[t][j] == e]
+ *                           (the numerator of Eq. 1; the denominator is T)
+ * Limits: 1 <= k <= E <= 256, k <= 8, 0 <= T <= 2^20.  T = 0 writes the
+ * offsets (all zero) and nothing else. */
+int pw_moe_route_topk(const float* d_logits, int T, int E, int k, int32_t* d_ids, float* d_w,
+                      int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm,
+                      float* d_mass_accum, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Fused mixed-precision MoE expert layer (§3.3, "Fused Mixed-Precision MoE Kernel") */
+/* ------------------------------------------------------------------------ */
+
+/* Workspace bytes pw_moe_apl_ffn needs for this problem size. */
+size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k);
+
+/* One launch computing, for every token t,
+ *   y[t] = sum_j w[t][j] * down_e( silu(gate_e x_t) * up_e x_t ),  e = ids[t][j]
+ * where each expert's gate_up (rows [0,I) gate, [I,2I) up) and down blocks
+ * are read at their own committed bitwidth q_i straight from the bit-planes:
+ * only the top q_i planes are loaded, the q_i-bit index is looked up in that
+ * block's LUT_{q_i} (fp16), products accumulate in fp32, the activation h is
+ * rounded to fp16, and y is rounded to fp16.  Experts with no tokens are not
+ * read.  Blocks of expert e in `layer` are descriptor entries
+ * (layer*E + e)*2 + {0: gate_up, 1: down} of d_desc (see _sync).
+ *  d_x  fp16 [T][H];  d_y fp16 [T][H] (written);  routing arrays as produced by
+ *  pw_moe_route_topk (d_ids may be NULL: it is not read);
+ *  d_ws workspace of pw_moe_apl_ffn_workspace() bytes, 256-byte aligned,
+ *  contents need not be initialised;
+ *  d_status int32, set to a PW_ERR_* code on a device-side failure (left
+ *  untouched on success, so the caller zeroes it beforehand).
+ * Shapes: H % 256 == 0, I % 256 == 0, committed bitwidths 2..8. */
+int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
+                   int E, int k, const int32_t* d_ids, const float* d_w,
+                   const int32_t* d_offsets, const int32_t* d_perm, const int32_t* d_inv_perm,
+                   void* d_ws, size_t ws_bytes, uint16_t* d_y, int32_t* d_status, void* stream);
+
+/* Options of pw_moe_apl_ffn_ex (zero-initialise, then set what you need). */
+#define PW_PATH_AUTO 0
+#define PW_PATH_DECODE 1   /* CUDA-core dequant + register-fragment tensor MMA */
+#define PW_PATH_PREFILL 2  /* tcgen05/TMEM tile path */
+#define PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL 1u  /* test hook: one gate_up unit never
+                                                 signals completion, so the waits
+                                                 that depend on it run out */
+typedef struct pw_ffn_options {
+  int32_t path;              /* PW_PATH_* */
+  uint32_t flags;            /* PW_FFN_FLAG_* */
+  uint32_t wait_timeout_us;  /* bound of each in-kernel wait; 0 = 2 s */
+  int32_t reserved[5];
+} pw_ffn_options;
+
+int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
+                      int E, int k, const int32_t* d_ids, const float* d_w,
+                      const int32_t* d_offsets, const int32_t* d_perm, const int32_t* d_inv_perm,
+                      void* d_ws, size_t ws_bytes, uint16_t* d_y, int32_t* d_status,
+                      const pw_ffn_options* opts, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Test exports: they run the same device dequant code as the fused layer.     */
+/* ------------------------------------------------------------------------ */
+
+/* b-bit overlay indices of `block` of the table, read from its top b
+ * attached planes: d_idx_out uint8 [rows][cols].  b must be 1..8 and planes
+ * 0..b-1 attached (else PW_ERR_NOT_RESIDENT). */
+int pw_unpack_indices(const pw_page_table* t, int block, int b, uint8_t* d_idx_out,
+                      void* stream);
+
+/* out[m][n] = sum_j W[n][j] * x[m][j], W = LUT_q[n][idx_q[n][j]] of `block`
+ * at its committed bitwidth q (2..8): d_x fp16 [M][cols], d_out fp32
+ * [M][rows], fp32 accumulation.  M >= 0. */
+int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,
+                  float* d_out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* PW_H_ */
