@@ -75,13 +75,12 @@ __device__ __forceinline__ void load_strip_lut(const uint16_t* __restrict__ lut,
 // q-bit indices of the 8 fragment elements of k-step s, packed as two nibble
 // words (elements e at bits 4e..4e+3): lo = index bits 3..0, hi = bits 7..4.
 template <int Q>
-__device__ __forceinline__ void step_indices(const uint4 (&pl)[Q], int w, int js, uint32_t& lo, uint32_t& hi) {
+__device__ __forceinline__ void step_indices(const uint32_t (&words)[Q], int js, uint32_t& lo, uint32_t& hi) {
   lo = 0u;
   hi = 0u;
 #pragma unroll
   for (int p = 0; p < Q; ++p) {
-    const uint32_t word = w == 0 ? pl[p].x : (w == 1 ? pl[p].y : (w == 2 ? pl[p].z : pl[p].w));
-    const uint32_t xb = (word >> js) & 0x11111111u;
+    const uint32_t xb = (words[p] >> js) & 0x11111111u;
     const int bitpos = Q - 1 - p;
     if (bitpos >= 4)
       hi |= xb << (bitpos - 4);
@@ -97,12 +96,12 @@ __device__ __forceinline__ uint32_t elem_index(uint32_t lo, uint32_t hi, int e) 
   return l | (((hi >> (4 * e)) & 0xFu) << 4);
 }
 
-// Dequantised A-fragment of k-step s from the tile's plane words.
+// Dequantised A-fragment of k-step 4w+js from word w of each plane.
 template <int Q>
-__device__ __forceinline__ void step_fragment(const uint4 (&pl)[Q], int s, const uint16_t* __restrict__ lut_g,
+__device__ __forceinline__ void step_fragment(const uint32_t (&words)[Q], int js, const uint16_t* __restrict__ lut_g,
                                               const uint16_t* __restrict__ lut_g8, uint32_t (&a)[4]) {
   uint32_t lo, hi;
-  step_indices<Q>(pl, s >> 2, s & 3, lo, hi);
+  step_indices<Q>(words, js, lo, hi);
   const uint32_t v0 = lut_g[elem_index<Q>(lo, hi, 0)];
   const uint32_t v1 = lut_g[elem_index<Q>(lo, hi, 1)];
   const uint32_t v2 = lut_g[elem_index<Q>(lo, hi, 2)];
@@ -117,15 +116,44 @@ __device__ __forceinline__ void step_fragment(const uint4 (&pl)[Q], int s, const
   a[3] = v6 | (v7 << 16);  // row g+8, cols 2c+8, 2c+9
 }
 
-// Main loop of one warp unit: strip `strip` of a block (planes, tiles
-// [t0, t1)), B operand = nt_count n-tiles whose row g (this lane's token) is
-// brow[nt] (element offset of column 0 of that token's row in `bbase`).
-// kFromH: B rows were written earlier in the same launch -> L2-only loads.
+// Per-warp shared-memory budget of the plane-staging ring.
+constexpr int kRingBytesPerWarp = 8192;
+
+// Pipeline depth (tiles) for bitwidth Q: as many 512-byte-per-plane tiles as
+// fit in the ring, at most 4.
+template <int Q>
+struct RingDepth {
+  static constexpr int value = (kRingBytesPerWarp / (Q * kTileBytes)) > 4 ? 4 : (kRingBytesPerWarp / (Q * kTileBytes));
+};
+
+__device__ __forceinline__ void cp_async_16(uint32_t smem_addr, const void* gmem) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ uint32_t lds_u32(uint32_t smem_addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(smem_addr));
+  return v;
+}
+
+// Main loop of one warp unit: strip `strip` of a block (tiles [t0, t1)),
+// B operand = nt_count n-tiles whose row g (this lane's token) starts at
+// element offset brow[nt] of `bbase`.  Each lane streams its own 16 bytes of
+// every plane of the next tiles into its private slots of the warp's ring
+// (cp.async, L2 only) while it works on the current tile, so no cross-lane
+// synchronisation is needed.  kFromH: the B rows were written earlier in the
+// same launch -> L2-only loads.
 template <int Q, bool kFromH>
 __device__ __forceinline__ void strip_mainloop(const BlockDesc& d, int strip, int t0, int t1,
-                                               const uint16_t* __restrict__ lut_s, const uint16_t* __restrict__ bbase,
-                                               const long long (&brow)[kNtMax], int nt_count,
-                                               float (&acc)[kNtMax][4]) {
+                                               const uint16_t* __restrict__ lut_s, uint32_t ring_s,
+                                               const uint16_t* __restrict__ bbase, const int (&brow)[kNtMax],
+                                               int nt_count, float (&acc)[kNtMax][4]) {
+  constexpr int D = RingDepth<Q>::value;
+  constexpr int kStageBytes = Q * kTileBytes;
   const int lane = static_cast<int>(lane_id());
   const int g = lane >> 2, c = lane & 3;
   const uint16_t* lut_g = lut_s + g * (1 << Q);
@@ -135,37 +163,49 @@ __device__ __forceinline__ void strip_mainloop(const BlockDesc& d, int strip, in
   const uint32_t* planes[Q];
 #pragma unroll
   for (int p = 0; p < Q; ++p) planes[p] = d.planes[p] + strip_word0;
+  const uint32_t my_slot = ring_s + lane * 16;
 
-  uint4 cur[Q];
+  auto issue = [&](int t, int stage) {
+    if (t < t1) {
 #pragma unroll
-  for (int p = 0; p < Q; ++p) cur[p] = ld_stream_v4(planes[p] + static_cast<long long>(t0) * (kTileBytes / 4));
-  for (int t = t0; t < t1; ++t) {
-    uint4 nxt[Q];
-    if (t + 1 < t1) {
-#pragma unroll
-      for (int p = 0; p < Q; ++p) nxt[p] = ld_stream_v4(planes[p] + static_cast<long long>(t + 1) * (kTileBytes / 4));
+      for (int p = 0; p < Q; ++p)
+        cp_async_16(my_slot + stage * kStageBytes + p * kTileBytes, planes[p] + static_cast<long long>(t) * (kTileBytes / 4));
     }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < D - 1; ++i) issue(t0 + i, i);
+
+  int stage = 0;
+  for (int t = t0; t < t1; ++t) {
+    issue(t + D - 1, (stage + D - 1) % D);
+    cp_async_wait<D - 1>();
+    const uint32_t base = my_slot + stage * kStageBytes;
     const int col_tile = t * kTileCols + 2 * c;
 #pragma unroll
-    for (int s = 0; s < 16; ++s) {
-      uint32_t a[4];
-      step_fragment<Q>(cur, s, lut_g, lut_g8, a);
-      const int col = col_tile + 16 * s;
+    for (int w = 0; w < 4; ++w) {
+      uint32_t words[Q];
 #pragma unroll
-      for (int nt = 0; nt < kNtMax; ++nt) {
-        if (nt < nt_count) {
-          const uint16_t* bp = bbase + brow[nt] + col;
-          const uint32_t b0 = kFromH ? ld_cg_u32(bp) : ld_nc_u32(bp);
-          const uint32_t b1 = kFromH ? ld_cg_u32(bp + 8) : ld_nc_u32(bp + 8);
-          mma_16816(acc[nt], a, b0, b1);
+      for (int p = 0; p < Q; ++p) words[p] = lds_u32(base + p * kTileBytes + 4 * w);
+#pragma unroll
+      for (int js = 0; js < 4; ++js) {
+        uint32_t a[4];
+        step_fragment<Q>(words, js, lut_g, lut_g8, a);
+        const int col = col_tile + 16 * (4 * w + js);
+#pragma unroll
+        for (int nt = 0; nt < kNtMax; ++nt) {
+          if (nt < nt_count) {
+            const uint16_t* bp = bbase + brow[nt] + col;
+            const uint32_t b0 = kFromH ? ld_cg_u32(bp) : ld_nc_u32(bp);
+            const uint32_t b1 = kFromH ? ld_cg_u32(bp + 8) : ld_nc_u32(bp + 8);
+            mma_16816(acc[nt], a, b0, b1);
+          }
         }
       }
     }
-    if (t + 1 < t1) {
-#pragma unroll
-      for (int p = 0; p < Q; ++p) cur[p] = nxt[p];
-    }
+    stage = (stage + 1 == D) ? 0 : stage + 1;
   }
+  cp_async_wait<0>();
 }
 
 }  // namespace pw

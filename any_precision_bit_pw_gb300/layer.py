@@ -1,0 +1,159 @@
+"""Device storage and call plumbing for Any-Precision MoE layers on one GPU.
+
+PyTorch is used here only for device memory and streams: every computation
+(packing, routing, the fused expert layer) is a libpw kernel called through
+the C ABI binding in ``pw.py``.
+
+``APLMoEStack`` owns, for L MoE layers of E experts, the bit-plane tensors and
+LUT tensors of every per-expert linear-block (layer, expert, gate_up|down),
+the libpw page table that borrows them, and the device descriptor array the
+fused kernel reads.  Lowering a block's committed bitwidth drops the plane and
+LUT tensors above it (the torch caching allocator reuses that memory for
+later allocations on the same stream, i.e. after the launches already
+enqueued -- the "release at a safe boundary" of §3.3 of the PagedWeight
+arXiv text).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+from typing import Dict, List, Optional
+
+import torch
+
+from . import pw
+
+GATE_UP, DOWN = 0, 1
+
+
+class APLMoEStack:
+    def __init__(self, hidden: int, intermediate: int, experts: int, top_k: int, layers: int = 1,
+                 parent_bits: int = 8, seed_bits: int = 3, device="cuda"):
+        self.H, self.I, self.E, self.k, self.L = hidden, intermediate, experts, top_k, layers
+        self.P, self.S = parent_bits, seed_bits
+        self.device = torch.device(device)
+        self.n_blocks = layers * experts * 2
+        infos = []
+        for b in range(self.n_blocks):
+            rows, cols = self.block_shape(b % 2)
+            infos.append(pw.pw_block_info(rows, cols, parent_bits, seed_bits, pw.PW_LAYOUT_TILED, 0))
+        self.table = pw.pw_page_table_create(infos)
+        self.planes: Dict[int, List[Optional[torch.Tensor]]] = {}
+        self.luts: Dict[int, Dict[int, torch.Tensor]] = {}
+        nbytes = pw.pw_desc_bytes(self.n_blocks)
+        self.desc = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+
+    def __del__(self):
+        t = getattr(self, "table", None)
+        if t is not None:
+            try:
+                pw.pw_page_table_destroy(t)
+            except Exception:
+                pass
+            self.table = None
+
+    # ------------------------------------------------------------------
+    def block_shape(self, u: int):
+        return (2 * self.I, self.H) if u == GATE_UP else (self.H, self.I)
+
+    def block_id(self, layer: int, expert: int, u: int) -> int:
+        return (layer * self.E + expert) * 2 + u
+
+    def load_block(self, block: int, idx: torch.Tensor, luts: Dict[int, torch.Tensor], q: int,
+                   keep_planes: Optional[int] = None, stream=None) -> None:
+        """Pack parent indices (uint8 [rows][cols] on the device) into P planes,
+        keep the top ``keep_planes`` (default q) and the LUTs seed..keep, attach
+        them to the page table and commit q."""
+        rows, cols = self.block_shape(block % 2)
+        assert tuple(idx.shape) == (rows, cols)
+        keep = q if keep_planes is None else keep_planes
+        nb = pw.pw_plane_bytes(rows, cols)
+        planes = [torch.empty(nb // 4, dtype=torch.int32, device=self.device) for _ in range(self.P)]
+        pw.pw_pack_bitplanes(idx.to(self.device).contiguous(), self.P, planes, stream=stream)
+        kept: List[Optional[torch.Tensor]] = [planes[p] if p < keep else None for p in range(self.P)]
+        del planes
+        self.planes[block] = kept
+        self.luts[block] = {}
+        for p in range(keep):
+            pw.pw_page_table_attach_plane(self.table, block, p, kept[p].data_ptr())
+        for b in range(self.S, keep + 1):
+            t = luts[b].to(self.device).contiguous()
+            assert t.dtype == torch.float16 and tuple(t.shape) == (rows, 1 << b)
+            self.luts[block][b] = t
+            pw.pw_page_table_attach_lut(self.table, block, b, t.data_ptr())
+        self.commit(block, q)
+
+    def commit(self, block: int, q: int) -> int:
+        """Commit q for a block; returns the bytes released (Eq. 3)."""
+        before = self.resident_bytes_of(block)
+        mask = pw.pw_page_table_set_bits(self.table, block, q)
+        for p in range(self.P):
+            if mask >> p & 1:
+                self.planes[block][p] = None
+        for b in range(self.S, self.P + 1):
+            if mask >> (8 + b) & 1:
+                self.luts[block].pop(b, None)
+        return before - self.resident_bytes_of(block)
+
+    def resident_bytes_of(self, block: int) -> int:
+        q, _, _ = pw.pw_page_table_get(self.table, block)
+        return pw.pw_page_table_bytes(self.table, block, q) if q > 0 else 0
+
+    def committed_bits(self, block: int) -> int:
+        return pw.pw_page_table_get(self.table, block)[0]
+
+    def resident_bytes(self) -> int:
+        return pw.pw_page_table_resident_bytes(self.table)
+
+    def sync(self, stream=None) -> None:
+        pw.pw_page_table_sync(self.table, self.desc, stream=stream)
+
+
+@dataclass
+class RouteBuffers:
+    ids: torch.Tensor
+    w: torch.Tensor
+    offsets: torch.Tensor
+    perm: torch.Tensor
+    inv_perm: torch.Tensor
+
+
+class MoECall:
+    """Preallocated buffers for one (T, shape) and the two-launch layer call:
+    pw_moe_route_topk then pw_moe_apl_ffn."""
+
+    def __init__(self, stack: APLMoEStack, tokens: int, device=None):
+        dev = stack.device if device is None else torch.device(device)
+        T, E, k = tokens, stack.E, stack.k
+        self.stack, self.T = stack, T
+        A = max(1, T * k)
+        self.route = RouteBuffers(
+            ids=torch.empty((max(T, 1), k), dtype=torch.int32, device=dev),
+            w=torch.empty((max(T, 1), k), dtype=torch.float32, device=dev),
+            offsets=torch.empty((E + 1,), dtype=torch.int32, device=dev),
+            perm=torch.empty((A,), dtype=torch.int32, device=dev),
+            inv_perm=torch.empty((A,), dtype=torch.int32, device=dev))
+        self.mass = torch.zeros((stack.L, E), dtype=torch.float32, device=dev)
+        ws = pw.pw_moe_apl_ffn_workspace(T, stack.H, stack.I, E, k)
+        self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev)
+        self.y = torch.empty((max(T, 1), stack.H), dtype=torch.float16, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    def __call__(self, layer: int, x: torch.Tensor, logits: torch.Tensor, options=None, stream=None,
+                 accumulate_mass: bool = True) -> torch.Tensor:
+        s, r = self.stack, self.route
+        pw.pw_moe_route_topk(logits, s.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm,
+                             self.mass[layer] if accumulate_mass else None, stream=stream)
+        pw.pw_moe_apl_ffn(s.desc, layer, x, s.I, s.E, s.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm,
+                          self.ws, self.y, self.status, options=options, stream=stream)
+        return self.y[: self.T]
+
+
+def load_layer(stack: APLMoEStack, layer: int, inputs, experts=None, stream=None) -> None:
+    """Load one layer's blocks from a synth.LayerInputs-like object (fields
+    ``idx[(e, u)]``, ``luts[(e, u)][b]``, ``bits[2e+u]``) at their committed
+    bitwidths, keeping only the planes and LUTs those bitwidths need."""
+    ex = range(stack.E) if experts is None else experts
+    for e in ex:
+        for u in (GATE_UP, DOWN):
+            stack.load_block(stack.block_id(layer, e, u), inputs.idx[(e, u)], inputs.luts[(e, u)],
+                             inputs.bits[2 * e + u], stream=stream)

@@ -1,0 +1,428 @@
+"""Benchmark of the fused mixed-precision Any-Precision MoE layer on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pw|reference]
+                    [--workload NAME] [--sweep PATH]
+
+One step = one pass of the hot path over one batch: top-k routing
+(pw_moe_route_topk) + the fused expert layer (pw_moe_apl_ffn: gather, gate_up
+at each block's committed bitwidth, SiLU*mul, down, top-k weighted combine).
+Weights are resident in HBM (bit-planes + LUTs, packed once before timing).
+The default workload is the Mixtral-8x7B-shaped decode layer (H 4096, I 14336,
+8 experts, top-2, 32 tokens, per-block bitwidths uniform on 3..8).
+
+Prints ONE JSON line on rank 0.  Under torchrun every rank runs an independent
+replica of the workload on its own GPU (the path has no exchange step);
+``value`` is the tokens of all ranks over the slowest rank's time.
+
+``--impl reference`` times the CPU oracle (numpy, float64) on the host cores
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+from any_precision_bit_pw_gb300 import synth  # noqa: E402
+
+METRIC = "MoE APL layer tokens/s; achieved HBM GB/s vs ~8 TB/s peak per bitwidth"
+UNIT = "tokens/s"
+DEFAULT_WORKLOAD = synth.MIXTRAL_8X7B_DECODE.name
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.send_signal(signal.SIGTERM)
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower().startswith("active")})
+        power = [num(r[3]) for r in rows if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------------------
+# the GPU arm
+# ---------------------------------------------------------------------------
+def algorithmic_bytes(wl, bits, offsets):
+    """Bytes one fused-layer launch must move: the committed planes and LUT_q
+    of every block of every active expert, x, y and the h write + read."""
+    sh = wl.shape
+    H, I, E, k = sh.hidden, sh.intermediate, sh.experts, sh.top_k
+    T = int(offsets[-1]) // k
+    planes = luts = 0
+    for e in range(E):
+        if offsets[e + 1] > offsets[e]:
+            for u, (N, K) in ((0, (2 * I, H)), (1, (H, I))):
+                q = bits[2 * e + u]
+                planes += q * N * K // 8
+                luts += N * (1 << q) * 2
+    other = 2 * T * H + 2 * T * H + 2 * 2 * T * k * I
+    return planes + luts + other, planes, luts
+
+
+def gpu_arm(args, rank, world, local_rank):
+    from any_precision_bit_pw_gb300 import pw
+    from any_precision_bit_pw_gb300.layer import APLMoEStack, MoECall, load_layer
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    pw.lib()
+    wl = synth.WORKLOADS[args.workload]
+    sh = wl.shape
+    li = synth.layer_inputs(wl, device=dev)
+    stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, wl.parent_bits, wl.seed_bits, dev)
+    load_layer(stack, 0, li)
+    stack.sync()
+    del li.idx
+    n_batches = 4
+    xs = [synth.activations(wl, 0, s, dev) for s in range(n_batches)]
+    lgs = [synth.router_logits(wl, 0, s, dev) for s in range(n_batches)]
+    call = MoECall(stack, wl.tokens)
+    stream = torch.cuda.current_stream()
+
+    # routing of each batch (for the algorithmic byte count)
+    bytes_per_batch = []
+    for s in range(n_batches):
+        call(0, xs[s], lgs[s])
+        torch.cuda.synchronize()
+        off = call.route.offsets.cpu().numpy()
+        bytes_per_batch.append(algorithmic_bytes(wl, li.bits, off))
+    assert int(call.status.item()) == 0, "device status after warm-up calls"
+
+    for i in range(args.warmup):
+        call(0, xs[i % n_batches], lgs[i % n_batches])
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    smi_index = vis.split(",")[local_rank] if vis and len(vis.split(",")) > local_rank else str(local_rank)
+    with ClockSampler(smi_index) as clk:
+        start.record(stream)
+        for i in range(K):
+            s = i % n_batches
+            pw.pw_moe_route_topk(lgs[s], sh.top_k, call.route.ids, call.route.w, call.route.offsets,
+                                 call.route.perm, call.route.inv_perm, call.mass[0])
+            ev[i][0].record(stream)
+            pw.pw_moe_apl_ffn(stack.desc, 0, xs[s], sh.intermediate, sh.experts, sh.top_k, call.route.ids,
+                              call.route.w, call.route.offsets, call.route.perm, call.route.inv_perm, call.ws,
+                              call.y, call.status)
+            ev[i][1].record(stream)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(stop)
+    ffn_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(K)]
+    status = int(call.status.item())
+
+    # end-to-end through the C ABI with pinned host buffers
+    T, H, E = wl.tokens, sh.hidden, sh.experts
+    hx = [x.cpu().pin_memory() for x in xs]
+    hl = [l.cpu().pin_memory() for l in lgs]
+    hy = torch.empty((T, H), dtype=torch.float16).pin_memory()
+    dx = torch.empty_like(xs[0])
+    dl = torch.empty_like(lgs[0])
+    K2 = max(1, min(K, 200))
+    for i in range(3):
+        dx.copy_(hx[i % n_batches], non_blocking=True)
+        dl.copy_(hl[i % n_batches], non_blocking=True)
+        y = call(0, dx, dl)
+        hy.copy_(y, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K2):
+        dx.copy_(hx[i % n_batches], non_blocking=True)
+        dl.copy_(hl[i % n_batches], non_blocking=True)
+        y = call(0, dx, dl)
+        hy.copy_(y, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K2
+
+    # max over ranks
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    total_ms = float(t.item())
+
+    mean_bytes = float(np.mean([b[0] for b in bytes_per_batch]))
+    mean_planes = float(np.mean([b[1] for b in bytes_per_batch]))
+    ffn_avg_ms = float(np.mean(ffn_ms))
+    achieved = mean_bytes / (ffn_avg_ms * 1e-3) / 1e9
+    peak, peak_kind = _peaks()
+    clocks = clk.summary()
+    value = wl.tokens * K * world / (total_ms * 1e-3)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic (seeded; bit-plane indices uniform, LUTs sorted N(0,0.02), x N(0,1))",
+        "config": {"workload": wl.name, "hidden": H, "intermediate": sh.intermediate, "experts": E,
+                   "top_k": sh.top_k, "tokens": T, "parent_bits": wl.parent_bits, "seed_bits": wl.seed_bits,
+                   "committed_bits": li.bits, "parallelism": f"replicas x{world}",
+                   "l2": "no flush: the planes read per step (%.0f MB) exceed the 129 MB L2" % (mean_planes / 1e6)},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": None,
+                     "kernel": "ffn_decode_kernel (pw_moe_apl_ffn)",
+                     "algorithmic_bytes_per_launch": mean_bytes, "plane_bytes_per_launch": mean_planes,
+                     "launch_ms": ffn_avg_ms, "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"},
+        "e2e": {"value": wl.tokens / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2},
+        "gpu_launches": 2 * K,
+        "clocks": clocks,
+        "status": status,
+    }
+    return line
+
+
+def sweep(args, dev, out_path):
+    """Uniform-bitwidth sweep (b x T) of the fused layer: tokens/s, GB/s and
+    fraction of the HBM roofline per point.  Writes JSON to ``out_path``."""
+    from any_precision_bit_pw_gb300 import pw
+    from any_precision_bit_pw_gb300.layer import APLMoEStack, MoECall, load_layer
+    base = synth.MIXTRAL_8X7B_SWEEP
+    sh = base.shape
+    peak, _ = _peaks()
+    li8 = synth.layer_inputs(base.with_(fixed_bits=8), device=dev)
+    results = []
+    for b in synth.SWEEP_BITS:
+        wl = base.with_(fixed_bits=b)
+        li8.bits = synth.committed_bits(wl)
+        stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, wl.parent_bits, wl.seed_bits, dev)
+        load_layer(stack, 0, li8)
+        stack.sync()
+        for T in synth.SWEEP_TOKENS:
+            call = MoECall(stack, T)
+            x = synth.activations(wl, 0, 0, dev, tokens=T)
+            lg = synth.router_logits(wl, 0, 0, dev, tokens=T)
+            for _ in range(5):
+                call(0, x, lg)
+            torch.cuda.synchronize()
+            off = call.route.offsets.cpu().numpy()
+            nbytes, planes, _ = algorithmic_bytes(wl.with_(tokens=T), li8.bits, off)
+            reps = 50
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(reps):
+                pw.pw_moe_apl_ffn(stack.desc, 0, x, sh.intermediate, sh.experts, sh.top_k, call.route.ids,
+                                  call.route.w, call.route.offsets, call.route.perm, call.route.inv_perm,
+                                  call.ws, call.y, call.status)
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / reps
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            results.append({"bits": b, "tokens": T, "ffn_ms": ms, "tokens_per_s": T / (ms * 1e-3),
+                            "algorithmic_GBps": gbs, "plane_GBps": planes / (ms * 1e-3) / 1e9,
+                            "frac_of_measured_hbm": gbs / peak, "status": int(call.status.item())})
+            print(json.dumps(results[-1]), file=sys.stderr)
+        del stack
+        torch.cuda.empty_cache()
+    with open(out_path, "w") as f:
+        json.dump(results, f, indent=1)
+
+
+# ---------------------------------------------------------------------------
+# the reference arm / CPU baseline: the oracle on the host cores
+# ---------------------------------------------------------------------------
+def oracle_sample(workload: str, experts_in_sample: int = 1) -> dict:
+    """Time the oracle on a bounded sample of the workload: the layer output
+    contribution of the first ``experts_in_sample`` active experts (their
+    gate_up and down blocks read from the packed bit-planes at the committed
+    bitwidths, for the tokens routed to them).  Scaled to the full layer by
+    the number of active experts (every expert's blocks have the same shape)."""
+    from oracle import apl
+    wl = synth.WORKLOADS[workload]
+    sh = wl.shape
+    x = synth.activations(wl).numpy()
+    logits = synth.router_logits(wl).numpy()
+    r = apl.route_topk(logits, sh.top_k)
+    active = [e for e in range(sh.experts) if r["offsets"][e + 1] > r["offsets"][e]]
+    sample = active[:experts_in_sample]
+    li = synth.layer_inputs(wl, experts=sample)
+    blocks = {}
+    for e in sample:
+        for u in (0, 1):
+            idx = li.idx[(e, u)].numpy()
+            N, K = idx.shape
+            blocks[(e, u)] = apl.Block(apl.pack_bitplanes(idx, wl.parent_bits),
+                                       {b: t.numpy() for b, t in li.luts[(e, u)].items()},
+                                       li.bits[2 * e + u], N, K)
+    ids = r["ids"]
+    mask = np.isin(ids, sample)
+    toks = sorted(set(np.nonzero(mask)[0].tolist()))
+    t0 = time.perf_counter()
+    ids_s = np.where(mask, ids, -1)
+    apl.moe_layer(x, ids_s, r["w"], sh.intermediate, lambda e, u: blocks[(e, u)], tokens=toks)
+    dt = time.perf_counter() - t0
+    est_layer_s = dt * len(active) / len(sample)
+    return {"sample_s": dt, "est_layer_s": est_layer_s, "tokens_per_s": wl.tokens / est_layer_s,
+            "sample": f"oracle layer contribution of {len(sample)} of {len(active)} active experts "
+                      f"({sh.intermediate * 2}x{sh.hidden} gate_up + {sh.hidden}x{sh.intermediate} down each, "
+                      f"read from packed bit-planes), scaled by {len(active)}/{len(sample)}"}
+
+
+def cpu_baseline(workload: str) -> dict:
+    """Run the oracle sample in a fresh single-threaded child process."""
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               CUDA_VISIBLE_DEVICES="")
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", workload]
+    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+    if r.returncode != 0:
+        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    return {"value": d["tokens_per_s"], "unit": UNIT, "cores": 1, "kind": "oracle", "sample": d["sample"],
+            "sample_s": d["sample_s"]}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    wl = synth.WORKLOADS[args.workload]
+    times = []
+    sample = ""
+    for _ in range(args.warmup):
+        pass  # the oracle has no warm-up state
+    for _ in range(max(1, args.steps)):
+        d = json.loads(subprocess.run(
+            [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", args.workload],
+            env=dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                     CUDA_VISIBLE_DEVICES=""), capture_output=True, text=True, timeout=600
+        ).stdout.strip().splitlines()[-1])
+        times.append(d["est_layer_s"])
+        sample = d["sample"]
+    ms = 1e3 * float(np.mean(times))
+    value = wl.tokens / (ms * 1e-3)
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": len(times),
+            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": wl.name, "tokens": wl.tokens},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="pw", choices=["pw", "reference"])
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--sweep", default=None, help="also run the uniform-bitwidth sweep, JSON to this path")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "pw":
+        args.warmup = 3
+
+    if args.cpu_baseline_child:
+        print(json.dumps(oracle_sample(args.workload)))
+        return
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        line = reference_arm(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    # the CPU baseline runs in a child process started before this process touches the GPU
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload)
+    if world > 1:
+        torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    line = gpu_arm(args, rank, world, local_rank)
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    if args.sweep and rank == 0:
+        sweep(args, torch.device(f"cuda:{local_rank}"), args.sweep)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

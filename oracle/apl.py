@@ -226,6 +226,27 @@ class Block:
         return apl_linear(self.planes, self.luts[self.q], self.q, self.N, self.K, x)
 
 
+class IndexBlock:
+    """A linear-block given by its parent indices instead of its planes: the
+    q-bit index is the definition idx >> (P - q) (the overlay rule, §1).  Equal
+    to Block on packed planes by the overlay pin; used where packing a large
+    block on the host would dominate the test time."""
+
+    def __init__(self, idx: np.ndarray, luts: Dict[int, np.ndarray], q: int, parent_bits: int):
+        self.idx, self.luts, self.q, self.P = idx, luts, int(q), int(parent_bits)
+        self.N, self.K = idx.shape
+
+    def linear(self, x: np.ndarray, row_chunk: int = 2048) -> np.ndarray:
+        xm = np.asarray(x).astype(np.float64)
+        out = np.zeros((xm.shape[0], self.N), dtype=np.float64)
+        for r0 in range(0, self.N, row_chunk):
+            r1 = min(self.N, r0 + row_chunk)
+            idx_b = self.idx[r0:r1].astype(np.int64) >> (self.P - self.q)
+            W = dequant(idx_b, self.luts[self.q], (r0, r1))
+            out[:, r0:r1] = xm @ W.T
+        return out
+
+
 def moe_layer(x: np.ndarray, ids: np.ndarray, w: np.ndarray, I: int,
               blocks: Callable[[int, int], Block], tokens: Optional[Sequence[int]] = None
               ) -> np.ndarray:
@@ -234,7 +255,8 @@ def moe_layer(x: np.ndarray, ids: np.ndarray, w: np.ndarray, I: int,
     gate_up rows [0, I) are the gate, rows [I, 2I) the up projection; the
     routing weight is applied after the down projection, in the output
     accumulation.  ``blocks(e, u)`` returns the Block of expert e.  ``tokens``
-    restricts the output to a subset of tokens (others stay zero).
+    restricts the output to a subset of tokens (others stay zero); a negative
+    expert id leaves that assignment out (used to time a subset of experts).
     Returns float64 [T][H].
     """
     xm = np.asarray(x).astype(np.float64)
@@ -243,7 +265,7 @@ def moe_layer(x: np.ndarray, ids: np.ndarray, w: np.ndarray, I: int,
     want = np.ones(T, dtype=bool) if tokens is None else np.isin(np.arange(T), tokens)
     H = xm.shape[1]
     y = np.zeros((T, H), dtype=np.float64)
-    experts = sorted(set(int(e) for e in ids[want].ravel()))
+    experts = sorted(set(int(e) for e in ids[want].ravel() if e >= 0))
     for e in experts:
         tt, jj = np.nonzero((ids == e) & want[:, None])
         if tt.size == 0:

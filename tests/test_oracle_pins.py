@@ -303,3 +303,18 @@ def test_compare_metrics():
     m = apl.compare(y, y + np.array([[0.0, 0.05]]))
     assert abs(m["rel_l2"] - 0.01) < 1e-12
     assert abs(m["max_abs"] - 0.05) < 1e-12
+
+
+def test_index_block_equals_plane_block():
+    """The definition path (idx >> (P - q)) and the packed-plane path agree
+    exactly, so either may serve as the oracle of a block."""
+    rng = np.random.default_rng(41)
+    N, K, P = 64, 512, 8
+    idx = _rand_idx(rng, N, K, P)
+    planes = apl.pack_bitplanes(idx, P)
+    luts = {b: np.sort(rng.standard_normal((N, 1 << b)).astype(np.float16), axis=1) for b in range(2, 9)}
+    x = rng.standard_normal((3, K)).astype(np.float16)
+    for q in (2, 3, 5, 8):
+        a = apl.Block(planes, luts, q, N, K).linear(x)
+        b = apl.IndexBlock(idx, luts, q, P).linear(x)
+        assert np.array_equal(a, b)
