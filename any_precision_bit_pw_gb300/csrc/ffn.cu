@@ -24,6 +24,8 @@
 //    in a fixed order (reproducible), rounds to fp16 and writes y.
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "apl_core.cuh"
 
 namespace {
@@ -486,3 +488,52 @@ int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory.  Its scratch is
+// this fixed array; host code must not hand the array's name to a kernel (on
+// the host it is only a stand-in symbol), so the device address is looked up
+// once per device with cudaGetSymbolAddress and cached.
+// ---------------------------------------------------------------------------
+namespace {
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[PW_NOALLOC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  PW_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= kMaxDevices) return pw::set_error(PW_ERR_UNSUPPORTED, "noalloc: device %d", dev);
+  std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+  if (!g_noalloc_ptr[dev]) {
+    void* p = nullptr;
+    PW_CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+    g_noalloc_ptr[dev] = p;
+  }
+  *out = g_noalloc_ptr[dev];
+  return PW_OK;
+}
+
+}  // namespace
+
+extern "C" int pw_moe_apl_ffn_noalloc(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I, int E,
+                                      int k, const int32_t* d_ids, const float* d_w, const int32_t* d_offsets,
+                                      const int32_t* d_perm, const int32_t* d_inv_perm, uint16_t* d_y,
+                                      int32_t* d_status, void* stream) {
+  if (int e = validate_shape(T, H, I, E, k)) return e;
+  const size_t need = ws_layout(T, H, I, E, k).total;
+  if (need > PW_NOALLOC_SCRATCH_BYTES)
+    return pw::set_error(PW_ERR_WORKSPACE,
+                         "noalloc: this call needs %zu bytes of scratch but the built-in array holds %u "
+                         "(use pw_moe_apl_ffn with a caller workspace)",
+                         need, PW_NOALLOC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  if (int e = noalloc_scratch(&scratch)) return e;
+  // The regular path zeroes the counters it needs and writes every h and
+  // partial value before reading it, so stale contents are harmless.
+  return pw_moe_apl_ffn(d_desc, layer, d_x, T, H, I, E, k, d_ids, d_w, d_offsets, d_perm, d_inv_perm, scratch,
+                        PW_NOALLOC_SCRATCH_BYTES, d_y, d_status, stream);
+}

@@ -36,7 +36,8 @@ EXPORTS = (
     "pw_page_table_destroy", "pw_page_table_attach_plane", "pw_page_table_attach_lut",
     "pw_page_table_set_desired", "pw_page_table_set_bits", "pw_page_table_get", "pw_page_table_bytes",
     "pw_page_table_resident_bytes", "pw_page_table_sync", "pw_moe_route_topk",
-    "pw_moe_apl_ffn_workspace", "pw_moe_apl_ffn", "pw_moe_apl_ffn_ex", "pw_unpack_indices",
+    "pw_moe_apl_ffn_workspace", "pw_moe_apl_ffn", "pw_moe_apl_ffn_ex", "pw_moe_apl_ffn_noalloc",
+    "pw_unpack_indices",
     "pw_apl_linear",
 )
 
@@ -87,6 +88,7 @@ def lib() -> ctypes.CDLL:
             "pw_moe_apl_ffn": (I32, [P, I32, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P, P, P]),
             "pw_moe_apl_ffn_ex": (I32, [P, I32, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P, P,
                                         ctypes.POINTER(pw_ffn_options), P]),
+            "pw_moe_apl_ffn_noalloc": (I32, [P, I32, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P]),
             "pw_unpack_indices": (I32, [P, I32, I32, P, P]),
             "pw_apl_linear": (I32, [P, I32, P, I32, P, P]),
         }
@@ -218,6 +220,23 @@ def pw_moe_apl_ffn(d_desc: torch.Tensor, layer: int, x: torch.Tensor, I: int, E:
         _check(lib().pw_moe_apl_ffn(*args, _stream(stream)))
     else:
         _check(lib().pw_moe_apl_ffn_ex(*args, ctypes.byref(options), _stream(stream)))
+
+
+PW_NOALLOC_SCRATCH_BYTES = 32 << 20
+
+
+def pw_moe_apl_ffn_noalloc(d_desc: torch.Tensor, layer: int, x: torch.Tensor, I: int, E: int, k: int,
+                           ids: Optional[torch.Tensor], w: torch.Tensor, offsets: torch.Tensor,
+                           perm: torch.Tensor, inv_perm: torch.Tensor, y: torch.Tensor, status: torch.Tensor,
+                           stream=None) -> None:
+    """pw_moe_apl_ffn without a caller workspace: libpw's built-in scratch
+    array is used instead (see include/pw.h for its size and sharing rules)."""
+    _dev(x, torch.float16, "x")
+    _dev(y, torch.float16, "y")
+    T, H = x.shape
+    _check(lib().pw_moe_apl_ffn_noalloc(_ptr(d_desc), layer, _ptr(x), T, H, I, E, k, _ptr(ids), _ptr(w),
+                                        _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(y), _ptr(status),
+                                        _stream(stream)))
 
 
 def pw_unpack_indices(t, block: int, b: int, out: torch.Tensor, stream=None) -> None:

@@ -191,6 +191,33 @@ int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, in
                    const int32_t* d_offsets, const int32_t* d_perm, const int32_t* d_inv_perm,
                    void* d_ws, size_t ws_bytes, uint16_t* d_y, int32_t* d_status, void* stream);
 
+/* Same computation as pw_moe_apl_ffn, for callers that cannot allocate
+ * device memory: code running while a CUDA graph is being captured, plugin
+ * hosts whose memory contract forbids allocation during inference, and
+ * real-time loops where an allocation's latency or failure is not acceptable.
+ * The paper has no counterpart; this is an interface convenience.
+ *
+ * The scratch space lives in a fixed array inside libpw of
+ * PW_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU that loads the library
+ * holds until the process exits.  Calls whose workspace
+ * (pw_moe_apl_ffn_workspace) exceeds it fail with PW_ERR_WORKSPACE before
+ * anything is enqueued; for the Mixtral-8x7B shape that allows up to 117
+ * tokens per call at top-2.  This entry point allocates nothing itself (no
+ * cudaMalloc/cudaFree, no allocating library routine).
+ *  - The first call on a device looks up the array's device address (a one-off
+ *    set-up, once per device, with that device current); make that first call
+ *    before any stream capture.
+ *  - All calls share the one array and it keeps the last call's contents:
+ *    calls that overlap on the GPU (different streams without ordering, or
+ *    concurrent host threads) race and give wrong results.  Serialise them.
+ * Arguments, layouts and errors are those of pw_moe_apl_ffn. */
+#define PW_NOALLOC_SCRATCH_BYTES (32u << 20)
+int pw_moe_apl_ffn_noalloc(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
+                           int E, int k, const int32_t* d_ids, const float* d_w,
+                           const int32_t* d_offsets, const int32_t* d_perm,
+                           const int32_t* d_inv_perm, uint16_t* d_y, int32_t* d_status,
+                           void* stream);
+
 /* Options of pw_moe_apl_ffn_ex (zero-initialise, then set what you need). */
 #define PW_PATH_AUTO 0
 #define PW_PATH_DECODE 1   /* CUDA-core dequant + register-fragment tensor MMA */

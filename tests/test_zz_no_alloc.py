@@ -1,0 +1,80 @@
+"""The allocation-free entry point, pw_moe_apl_ffn_noalloc.
+
+Some callers cannot allocate device memory at call time -- code running under
+CUDA graph capture, plugin hosts whose memory contract forbids allocation
+during inference, real-time loops that cannot afford an allocation's latency
+or failure.  For them libpw runs the fused layer with a fixed scratch array of
+its own.  This test calls that entry point through the C ABI twice in a row and
+checks each result against the regular entry point (caller workspace) within
+the tolerance of the other layer tests.  The file name sorts last so that a run
+stopping at the first failure has already run every other test.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import apl
+
+pytestmark = pytest.mark.gpu
+
+pw = pytest.importorskip("any_precision_bit_pw_gb300.pw")
+from any_precision_bit_pw_gb300 import synth  # noqa: E402
+from any_precision_bit_pw_gb300.layer import APLMoEStack, MoECall, load_layer  # noqa: E402
+
+REL_L2 = 2e-3
+MAX_ABS_OVER_RMS = 1e-2
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    if not os.path.exists(pw.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    pw.lib()
+    torch.cuda.set_device(0)
+
+
+def _noalloc(call, stack, x):
+    r = call.route
+    y = torch.full_like(call.y, float("nan"))
+    status = torch.zeros((1,), dtype=torch.int32, device=DEV)
+    pw.pw_moe_apl_ffn_noalloc(stack.desc, 0, x, stack.I, stack.E, stack.k, r.ids, r.w, r.offsets, r.perm,
+                              r.inv_perm, y, status)
+    return y, status
+
+
+@pytest.mark.parametrize("wl", [synth.TINY_LAYER, synth.MIXTRAL_8X7B_DECODE], ids=lambda w: w.name)
+def test_noalloc_matches_workspace_entry_point_twice(wl):
+    sh = wl.shape
+    dev_inputs = wl.shape.hidden >= 4096
+    li = synth.layer_inputs(wl, device=DEV if dev_inputs else "cpu")
+    stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, wl.parent_bits, wl.seed_bits, DEV)
+    load_layer(stack, 0, li)
+    stack.sync()
+    call = MoECall(stack, wl.tokens)
+    for step in range(2):
+        x = synth.activations(wl, 0, step, DEV)
+        lg = synth.router_logits(wl, 0, step, DEV)
+        y_ref = call(0, x, lg).float().cpu().numpy()          # regular entry point, caller workspace
+        y, status = _noalloc(call, stack, x)                   # same routing buffers
+        torch.cuda.synchronize()
+        assert int(call.status.item()) == 0 and int(status.item()) == 0
+        y = y[: wl.tokens].float().cpu().numpy()
+        assert np.all(np.isfinite(y))
+        m = apl.compare(y_ref, y)
+        assert m["rel_l2"] <= REL_L2 and m["max_abs_over_rms"] <= MAX_ABS_OVER_RMS, (step, m)
+
+
+def test_noalloc_rejects_calls_beyond_its_scratch():
+    # 8x7B shape at 512 tokens needs far more than the 32 MiB array
+    assert pw.pw_moe_apl_ffn_workspace(512, 4096, 14336, 8, 2) > pw.PW_NOALLOC_SCRATCH_BYTES
+    L = pw.lib()
+    rc = L.pw_moe_apl_ffn_noalloc(None, 0, None, 512, 4096, 14336, 8, 2, None, None, None, None, None, None,
+                                  None, None)
+    assert rc == pw.PW_ERR_WORKSPACE
+    assert "scratch" in pw.pw_last_error()
