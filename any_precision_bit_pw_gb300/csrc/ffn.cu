@@ -1,67 +1,129 @@
-// Fused mixed-precision MoE expert layer (decode path) and the any-precision
-// linear test export.
+// Fused mixed-precision MoE expert layer on the 5th-generation tensor cores,
+// and the any-precision linear test export.
 //
 // "PagedWeight" arXiv text, §3.3 (Fused Mixed-Precision MoE Kernel): one
 // kernel reads the weight pages directly, follows the committed bitwidth of
 // every gate_up and down linear-block, and does the expert activation, the down
 // projection and the output accumulation in one launch.
 //
-// Structure: a persistent launch (one wave of CTAs) whose warps take work
-// units from an atomic ticket counter.  Tickets are issued in order: every
-// gate_up unit of every active expert first, then every down unit.  A warp only
-// takes a new ticket after finishing its previous unit, so when a down unit
-// waits for the gate_up units it depends on, each of those is already held by
-// a running warp and will finish: the waits always end (and are also bounded
-// in time, after which the kernel reports PW_ERR_TIMEOUT and returns).
+// Structure: a persistent launch (one CTA per SM) whose CTAs take work units
+// from an atomic ticket counter.  Tickets are issued in order: every gate_up
+// unit of every active expert first, then every down unit.  A CTA only takes a
+// new ticket after finishing its previous unit, so when a down unit waits for
+// the gate_up units it depends on, each of those is held by a running CTA and
+// will finish; the wait is also bounded in time (PW_ERR_TIMEOUT).
 //
-//  gate_up unit (expert e, strip s): rows 8s..8s+7 of the gate and of the up
-//    projection over all H columns, for all of e's tokens; epilogue
-//    h = silu(gate) * up rounded to fp16 into the workspace, in expert order.
-//  down unit (expert e, split p, strip s): rows 8s..8s+7 and H/2+8s..+7 of down
-//    over one K-split of I; fp32 partial sums into the workspace.
-//  combine: the last down unit to finish a strip (over all experts and
-//    splits) forms y[t][rows] = sum_j w[t][j] * sum_p partial[p][pos(t,j)][row]
-//    in a fixed order (reproducible), rounds to fp16 and writes y.
+// A unit is one 128-row strip of one block, one group of at most NMAX of the
+// expert's tokens, and a K range:
+//   gate_up (expert e, strip s, group g): all H columns; rows 64s..64s+63 of
+//     the gate and of the up projection; epilogue h = silu(gate) * up,
+//     rounded to fp16, into the workspace (expert-ordered positions).
+//   down (expert e, split p, strip s, group g): one K-split of I; fp32
+//     partial sums into the workspace.
+//   combine: the last down unit of a strip (over experts, splits and groups)
+//     forms y[t][rows] = sum_j w[t][j] * sum_p partial[p][pos(t,j)][row] in a
+//     fixed order, rounds to fp16 and writes y.
+//
+// Inside a unit (warp roles):
+//   warps 0-3 (128 threads, thread = one row = one TMEM lane): stream their
+//     rows' committed bit-planes into shared memory with cp.async, dequantise
+//     64 columns per stage through the row's LUT (dequant.cuh) and write the
+//     fp16 operand A straight into a 4-stage TMEM ring with tcgen05.st;
+//   warp 4: gathers the B operand (the tokens' x rows, or h rows) for each
+//     stage into a 128-byte-swizzled shared ring with cp.async, and its lane 0
+//     issues tcgen05.mma (A from TMEM, B from shared memory, fp32 accumulator
+//     in TMEM), releasing ring slots with tcgen05.commit;
+//   epilogue: warps 0-3 read the accumulator rows from TMEM.
+// Every mbarrier wait is bounded; a thread whose wait runs out reports
+// PW_ERR_TIMEOUT, stops waiting for the rest of the unit (it still arrives
+// where it must, so the other roles reach the end of the unit) and the CTA
+// takes no further units.  TMEM is always released before the CTA exits.
 #include <cuda_fp16.h>
 
 #include <mutex>
 
-#include "apl_core.cuh"
+#include "dequant.cuh"
+#include "pw_internal.h"
 
 namespace {
 
 using pw::BlockDesc;
-using pw::kNtMax;
 
-constexpr int kThreads = 384;
-constexpr int kWarps = kThreads / 32;
-constexpr int kSplitTiles = 8;  // down K-split: 2048 columns of I
+constexpr int kDeqWarps = 4;
+constexpr int kDeqThreads = 128;
+constexpr int kThreads = kDeqThreads + 32;
+constexpr int kAStages = 4;
+constexpr int kACols = pw::kStageK / 2;     // 32 TMEM columns (fp16 pairs) per stage
+constexpr int kDCol = kAStages * kACols;    // accumulator columns start here
+constexpr int kRingBytesPerLane = 256;      // per-row plane staging ring
+constexpr int kDecodeSplitCols = 2048;      // down K-split of the decode path
 constexpr int kMaxE = 256;
-constexpr size_t kLutSmemPerWarp = pw::kLutRowsPerWarp * pw::kLutMaxEntries * sizeof(uint16_t);
-constexpr size_t kSmemPerWarp = kLutSmemPerWarp + pw::kRingBytesPerWarp;
-constexpr size_t kSmemBytes = kWarps * kSmemPerWarp;
 
-struct FfnParams {
-  const BlockDesc* desc;  // this layer's 2E descriptors
+enum UnitKind : int { kNone = -1, kGateUp = 0, kDown = 1, kLinear = 2 };
+
+template <int NMAX>
+struct Cfg {
+  static constexpr int kBStages = NMAX <= 64 ? 4 : 3;
+  static constexpr int kBLookahead = kBStages - 2;
+  static constexpr int kBStageBytes = NMAX * 128;
+  static constexpr int kTmemCols = (kDCol + NMAX) <= 256 ? 256 : 512;
+  static constexpr int kOffB = 0;
+  static constexpr int kOffRing = kOffB + kBStages * kBStageBytes;
+  static constexpr int kOffLut = kOffRing + kDeqThreads * kRingBytesPerLane;
+  static constexpr int kOffBar = kOffLut + kDeqWarps * pw::kLutBytesPerWarp;
+  static constexpr int kOffRows = kOffBar + 256;
+  static constexpr int kSmemUsed = kOffRows + NMAX * 4;
+  static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
+  static_assert(kBStageBytes % 1024 == 0, "B stages must keep 1024-byte alignment");
+};
+
+struct Params {
+  const BlockDesc* desc;   // this layer's 2E descriptors (fused mode)
+  BlockDesc lin;           // the block (linear mode)
   const uint16_t* x;
   uint16_t* y;
+  float* out;              // linear mode output [M][rows]
   const float* w;
   const int32_t* offsets;
   const int32_t* perm;
   const int32_t* inv_perm;
-  int T, H, I, E, k, A;
-  int nsplit;
-  uint16_t* h;      // [A][I] fp16, expert order
-  float* part;      // [nsplit][A][H] fp32
-  uint32_t* ctr;    // [0] ticket, [1] abort, [2, 2+E*nsplit) gate_up done, then [H/16] strip arrivals
+  int T, H, I, E, k, A, M;
+  int nsplit, split_cols;
+  uint16_t* h;
+  float* part;
+  uint32_t* ctr;           // [0] ticket, [1] abort, [2, 2+E*nsplit) gate_up done, then strip arrivals
   int32_t* status;
   uint64_t wait_ns;
   uint32_t flags;
+  int linear;
 };
 
-__device__ __forceinline__ void report(int32_t* status, int code) { atomicCAS(status, 0, code); }
+struct Unit {
+  int kind, e, strip, split, tg, off, nrows, npad, q, st0, nst, skip, combine;
+  const BlockDesc* d;
+};
 
+struct Shared {            // small per-CTA state (static shared memory)
+  Unit u;
+  uint32_t tmem;
+  int nact;
+  int act[kMaxE];
+  int ntg[kMaxE];
+  int cum_gu[kMaxE + 1];
+  int cum_dn[kMaxE + 1];
+  int arrivals_per_strip;
+  int abort;
+};
+
+__device__ __forceinline__ void report(int32_t* status, int code) {
+  if (status) atomicCAS(status, 0, code);
+}
 __device__ __forceinline__ float silu(float z) { return z / (1.0f + expf(-z)); }
+
+__device__ __forceinline__ int strip_pos_row(int strip, int pos, int half_rows) {
+  const int w = pos >> 5, i = pos & 31;
+  return (i >> 4) * half_rows + strip * 64 + 16 * w + (i & 15);
+}
 
 __device__ __forceinline__ bool desc_ok(const BlockDesc& d, int rows, int cols) {
   if (d.q < 2 || d.q > PW_MAX_BITS || d.rows != rows || d.cols != cols || d.lut == nullptr) return false;
@@ -70,276 +132,408 @@ __device__ __forceinline__ bool desc_ok(const BlockDesc& d, int rows, int cols) 
   return true;
 }
 
-template <int Q>
-__device__ void gate_up_q(const FfnParams& p, const BlockDesc& d, int off, int ne, int strip, uint16_t* lut_s,
-                          uint32_t ring_s) {
-  const int lane = static_cast<int>(pw::lane_id());
-  const int g = lane >> 2, c = lane & 3;
-  pw::load_strip_lut<Q>(d.lut, p.I, strip, lut_s);
-  __syncwarp();
-  for (int tb = 0; tb < ne; tb += 8 * kNtMax) {
-    const int nt_count = min(kNtMax, (ne - tb + 7) / 8);
-    int brow[kNtMax];
-#pragma unroll
-    for (int nt = 0; nt < kNtMax; ++nt) {
-      const int tl = min(tb + nt * 8 + g, ne - 1);
-      brow[nt] = (__ldg(p.perm + off + tl) / p.k) * p.H;
+// ---------------------------------------------------------------------------
+// Unit scheduling (thread 0)
+// ---------------------------------------------------------------------------
+template <int NMAX>
+__device__ void setup_schedule(const Params& p, Shared& sh) {
+  sh.cum_gu[0] = 0;
+  sh.cum_dn[0] = 0;
+  if (p.linear) {
+    sh.nact = 0;
+    sh.arrivals_per_strip = 0;
+    return;
+  }
+  int n = 0, gu = 0, dn = 0, arr = 0;
+  const int gu_strips = 2 * p.I / 128, dn_strips = p.H / 128;
+  for (int e = 0; e < p.E; ++e) {
+    const int ne = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+    if (ne <= 0) continue;
+    const int g = (ne + NMAX - 1) / NMAX;
+    sh.act[n] = e;
+    sh.ntg[n] = g;
+    gu += gu_strips * g;
+    dn += p.nsplit * dn_strips * g;
+    arr += p.nsplit * g;
+    ++n;
+    sh.cum_gu[n] = gu;
+    sh.cum_dn[n] = dn;
+  }
+  sh.nact = n;
+  sh.arrivals_per_strip = arr;
+}
+
+// Fetch and decode the next unit into sh.u (thread 0 only).
+template <int NMAX>
+__device__ void next_unit(const Params& p, Shared& sh) {
+  Unit u{};
+  u.kind = kNone;
+  u.combine = -1;
+  if (sh.abort || *reinterpret_cast<volatile uint32_t*>(p.ctr + 1) != 0u) {
+    sh.u = u;
+    return;
+  }
+  const uint32_t t = atomicAdd(p.ctr, 1u);
+  if (p.linear) {
+    const BlockDesc& d = p.lin;
+    const int strips = d.rows / 128, groups = (p.M + NMAX - 1) / NMAX;
+    if (t < static_cast<uint32_t>(strips * groups)) {
+      u.kind = kLinear;
+      u.strip = static_cast<int>(t % strips);
+      u.tg = static_cast<int>(t / strips);
+      u.off = 0;
+      u.nrows = min(NMAX, p.M - u.tg * NMAX);
+      u.npad = ((u.nrows + 15) / 16) * 16;
+      u.q = d.q;
+      u.st0 = 0;
+      u.nst = d.cols / pw::kStageK;
+      u.d = &p.lin;
     }
-    float acc[kNtMax][4];
+    sh.u = u;
+    return;
+  }
+  const int n_gu = sh.cum_gu[sh.nact], n_dn = sh.cum_dn[sh.nact];
+  const int gu_strips = 2 * p.I / 128, dn_strips = p.H / 128;
+  int ai = 0;
+  if (t < static_cast<uint32_t>(n_gu)) {
+    while (sh.cum_gu[ai + 1] <= static_cast<int>(t)) ++ai;
+    const int rem = static_cast<int>(t) - sh.cum_gu[ai];
+    u.kind = kGateUp;
+    u.e = sh.act[ai];
+    u.strip = rem % gu_strips;
+    u.tg = rem / gu_strips;
+    u.split = (u.strip * 64) / p.split_cols;
+    u.d = p.desc + 2 * u.e;
+    u.st0 = 0;
+    u.nst = p.H / pw::kStageK;
+  } else if (t < static_cast<uint32_t>(n_gu + n_dn)) {
+    const int v = static_cast<int>(t) - n_gu;
+    while (sh.cum_dn[ai + 1] <= v) ++ai;
+    const int rem = v - sh.cum_dn[ai];
+    u.kind = kDown;
+    u.e = sh.act[ai];
+    const int per_split = dn_strips * sh.ntg[ai];
+    u.split = rem / per_split;
+    const int r2 = rem % per_split;
+    u.strip = r2 % dn_strips;
+    u.tg = r2 / dn_strips;
+    u.d = p.desc + 2 * u.e + 1;
+    const int c0 = u.split * p.split_cols;
+    u.st0 = c0 / pw::kStageK;
+    u.nst = (min(c0 + p.split_cols, p.I) - c0) / pw::kStageK;
+  } else {
+    sh.u = u;
+    return;
+  }
+  const int off0 = __ldg(p.offsets + u.e), ne = __ldg(p.offsets + u.e + 1) - off0;
+  u.off = off0 + u.tg * NMAX;
+  u.nrows = min(NMAX, ne - u.tg * NMAX);
+  u.npad = ((u.nrows + 15) / 16) * 16;
+  u.q = u.d->q;
+  const bool ok = u.kind == kGateUp ? desc_ok(*u.d, 2 * p.I, p.H) : desc_ok(*u.d, p.H, p.I);
+  if (!ok) {
+    report(p.status, u.d->q == 0 ? PW_ERR_NOT_RESIDENT : PW_ERR_UNSUPPORTED);
+    u.skip = 1;
+  }
+  if (u.kind == kDown && !u.skip) {
+    // wait until every gate_up unit of this expert that produces h columns of
+    // this split has finished (all token groups)
+    const int c0 = u.split * p.split_cols;
+    const int strips_in_split = (min(c0 + p.split_cols, p.I) - c0) / 64;
+    const uint32_t want = static_cast<uint32_t>(strips_in_split * sh.ntg[ai]);
+    const uint32_t* ctr = p.ctr + 2 + u.e * p.nsplit + u.split;
+    const uint64_t t0 = pw::global_ns();
+    uint32_t v;
+    while (true) {
+      asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+      if (v >= want) break;
+      if (*reinterpret_cast<volatile uint32_t*>(p.ctr + 1) != 0u) {
+        u.skip = 1;
+        break;
+      }
+      if (pw::global_ns() - t0 > p.wait_ns) {
+        report(p.status, PW_ERR_TIMEOUT);
+        atomicExch(p.ctr + 1, 1u);
+        u.skip = 1;
+        break;
+      }
+      __nanosleep(200);
+    }
+  }
+  sh.u = u;
+}
+
+// ---------------------------------------------------------------------------
+// Dequant warps
+// ---------------------------------------------------------------------------
+template <int NMAX, int Q>
+__device__ void dequant_role(const Params& p, const Unit& u, uint8_t* smem, uint32_t tmem, uint32_t& a_cnt,
+                             uint32_t unit_cnt, int& abort) {
+  using C = Cfg<NMAX>;
+  constexpr int kTileStrideW = pw::kTileBytes / 4;
+  constexpr int kTileBytesLane = Q * 16;
+  constexpr int D = (kRingBytesPerLane / kTileBytesLane) > 4 ? 4 : (kRingBytesPerLane / kTileBytesLane);
+  static_assert(D >= 2, "ring too small");
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int pos = threadIdx.x;  // 0..127
+  const BlockDesc& d = *u.d;
+  const int half_rows = d.rows / 2;
+  const int row = strip_pos_row(u.strip, pos, half_rows);
+  const uint32_t lut_warp = pw::smem_u32(smem + C::kOffLut + warp * pw::kLutBytesPerWarp);
+  pw::RowDequant<Q> dq;
+  dq.load(d.lut + static_cast<long long>(row) * (1 << Q), lut_warp, lane);
+
+  const int tiles = d.cols / pw::kTileCols;
+  const int tile0 = u.st0 / 2;
+  const int ntiles = u.nst / 2;
+  const uint32_t* src[Q];
 #pragma unroll
-    for (int nt = 0; nt < kNtMax; ++nt)
+  for (int q = 0; q < Q; ++q)
+    src[q] = d.planes[q] + (static_cast<long long>(u.strip) * tiles + tile0) * kTileStrideW + pos * 4;
+  const uint32_t ring = pw::smem_u32(smem + C::kOffRing + pos * kRingBytesPerLane);
+  auto issue = [&](int t) {
+    if (t < ntiles) {
+      const uint32_t slot = ring + (t % D) * kTileBytesLane;
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-    pw::strip_mainloop<Q, false>(d, strip, 0, p.H / pw::kTileCols, lut_s, ring_s, p.x, brow, nt_count, acc);
-    const int m = strip * 8 + g;
+      for (int q = 0; q < Q; ++q) pw::cp_async_16(slot + q * 16, src[q] + static_cast<long long>(t) * kTileStrideW);
+    }
+    pw::cp_async_commit();
+  };
 #pragma unroll
-    for (int nt = 0; nt < kNtMax; ++nt) {
-      if (nt < nt_count) {
+  for (int i = 0; i < D - 1; ++i) issue(i);
+
+  const uint32_t bar = pw::smem_u32(smem + C::kOffBar);
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+  for (int t = 0; t < ntiles; ++t) {
+    issue(t + D - 1);
+    pw::cp_async_wait<D - 1>();
+    const uint32_t slot = ring + (t % D) * kTileBytesLane;
 #pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int tl = tb + nt * 8 + 2 * c + i;
-          if (tl < ne) {
-            const float hv = silu(acc[nt][i]) * acc[nt][2 + i];
-            p.h[static_cast<long long>(off + tl) * p.I + m] = __half_as_ushort(__float2half_rn(hv));
-          }
+    for (int hf = 0; hf < 2; ++hf) {
+      uint32_t words[Q][2];
+#pragma unroll
+      for (int q = 0; q < Q; ++q) pw::lds_v2(slot + q * 16 + hf * 8, words[q][0], words[q][1]);
+      uint32_t out[32];
+      dq.stage(words, out);
+      const uint32_t as = a_cnt % kAStages, use = a_cnt / kAStages;
+      if (use > 0 && !abort && !pw::mbar_wait(bar + 8 * (kAStages + as), (use - 1) & 1u, p.wait_ns)) abort = 1;
+      pw::tc_fence_after();
+      pw::tmem_st_x32(tl + as * kACols, out);
+      pw::tmem_st_wait();
+      pw::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) pw::mbar_arrive(bar + 8 * as);
+      ++a_cnt;
+    }
+  }
+  pw::cp_async_wait<0>();
+
+  // epilogue: accumulator row `pos` (TMEM lane), columns = tokens
+  if (!abort && !pw::mbar_wait(bar + 8 * (2 * kAStages + C::kBStages), unit_cnt & 1u, p.wait_ns)) abort = 1;
+  pw::tc_fence_after();
+  for (int c = 0; c < u.npad / 16; ++c) {
+    uint32_t v[16];
+    pw::tmem_ld_x16(tl + kDCol + 16 * c, v);
+    pw::tmem_ld_wait();
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int n = 16 * c + i;
+      const float val = __uint_as_float(v[i]);
+      if (u.kind == kGateUp) {
+        const float up = __shfl_down_sync(0xffffffffu, val, 16);
+        if (lane < 16 && n < u.nrows) {
+          const int m = u.strip * 64 + 16 * warp + lane;
+          p.h[static_cast<long long>(u.off + n) * p.I + m] = __half_as_ushort(__float2half_rn(silu(val) * up));
         }
+      } else if (u.kind == kDown) {
+        if (n < u.nrows) p.part[(static_cast<long long>(u.split) * p.A + u.off + n) * p.H + row] = val;
+      } else {
+        if (n < u.nrows) p.out[static_cast<long long>(u.tg * NMAX + n) * d.rows + row] = val;
       }
     }
   }
-  __syncwarp();
+  pw::tc_fence_before();
 }
 
-template <int Q>
-__device__ void down_q(const FfnParams& p, const BlockDesc& d, int off, int ne, int split, int strip,
-                       uint16_t* lut_s, uint32_t ring_s) {
-  const int lane = static_cast<int>(pw::lane_id());
-  const int g = lane >> 2, c = lane & 3;
-  pw::load_strip_lut<Q>(d.lut, p.H / 2, strip, lut_s);
-  __syncwarp();
-  const int t0 = split * kSplitTiles;
-  const int t1 = min(t0 + kSplitTiles, p.I / pw::kTileCols);
-  for (int tb = 0; tb < ne; tb += 8 * kNtMax) {
-    const int nt_count = min(kNtMax, (ne - tb + 7) / 8);
-    int brow[kNtMax];
-#pragma unroll
-    for (int nt = 0; nt < kNtMax; ++nt) {
-      const int tl = min(tb + nt * 8 + g, ne - 1);
-      brow[nt] = (off + tl) * p.I;
-    }
-    float acc[kNtMax][4];
-#pragma unroll
-    for (int nt = 0; nt < kNtMax; ++nt)
-#pragma unroll
-      for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-    pw::strip_mainloop<Q, true>(d, strip, t0, t1, lut_s, ring_s, p.h, brow, nt_count, acc);
-    const int r0 = strip * 8 + g, r1 = p.H / 2 + strip * 8 + g;
-#pragma unroll
-    for (int nt = 0; nt < kNtMax; ++nt) {
-      if (nt < nt_count) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int tl = tb + nt * 8 + 2 * c + i;
-          if (tl < ne) {
-            float* dst = p.part + (static_cast<long long>(split) * p.A + off + tl) * p.H;
-            dst[r0] = acc[nt][i];
-            dst[r1] = acc[nt][2 + i];
-          }
-        }
-      }
-    }
+// ---------------------------------------------------------------------------
+// Producer / MMA warp
+// ---------------------------------------------------------------------------
+template <int NMAX>
+__device__ void producer_role(const Params& p, const Unit& u, uint8_t* smem, uint32_t tmem, uint32_t& a_cnt,
+                              uint32_t& b_cnt, int& abort) {
+  using C = Cfg<NMAX>;
+  const int lane = threadIdx.x & 31;
+  int* rows = reinterpret_cast<int*>(smem + C::kOffRows);
+  const uint16_t* bbase = u.kind == kDown ? p.h : p.x;
+  for (int n = lane; n < u.npad; n += 32) {
+    const int nn = min(n, u.nrows - 1);
+    int r;
+    if (u.kind == kGateUp)
+      r = (__ldg(p.perm + u.off + nn) / p.k) * p.H;
+    else if (u.kind == kDown)
+      r = (u.off + nn) * p.I;
+    else
+      r = (u.tg * NMAX + nn) * u.d->cols;
+    rows[n] = r;
   }
   __syncwarp();
+  const uint32_t bring = pw::smem_u32(smem + C::kOffB);
+  const uint32_t bar = pw::smem_u32(smem + C::kOffBar);
+  const uint32_t bar_b_empty = bar + 8 * (2 * kAStages);
+  const uint32_t bar_done = bar + 8 * (2 * kAStages + C::kBStages);
+  const int chunks = u.npad * 8;
+  auto issue = [&](int st) {
+    const uint32_t slot = (b_cnt + st) % C::kBStages, use = (b_cnt + st) / C::kBStages;
+    if (use > 0 && !abort && !pw::mbar_wait(bar_b_empty + 8 * slot, (use - 1) & 1u, p.wait_ns)) abort = 1;
+    const uint32_t dst0 = bring + slot * C::kBStageBytes;
+    const long long col = static_cast<long long>(u.st0 + st) * pw::kStageK;
+    for (int i = lane; i < chunks; i += 32) {
+      const int n = i >> 3, c = i & 7;
+      pw::cp_async_16(dst0 + n * 128 + ((c ^ (n & 7)) << 4), bbase + rows[n] + col + c * 8);
+    }
+  };
+  constexpr int LA = C::kBLookahead;
+#pragma unroll
+  for (int i = 0; i < LA; ++i) {
+    if (i < u.nst) issue(i);
+    pw::cp_async_commit();
+  }
+  const uint32_t idesc = pw::idesc_f16_f32(128, u.npad);
+  for (int st = 0; st < u.nst; ++st) {
+    if (st + LA < u.nst) issue(st + LA);
+    pw::cp_async_commit();
+    pw::cp_async_wait<LA>();
+    pw::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      const uint32_t as = a_cnt % kAStages;
+      if (!abort && !pw::mbar_wait(bar + 8 * as, (a_cnt / kAStages) & 1u, p.wait_ns)) abort = 1;
+      pw::tc_fence_after();
+      const uint32_t bs = (b_cnt + st) % C::kBStages;
+      const uint64_t bdesc = pw::sdesc_kmajor_sw128(bring + bs * C::kBStageBytes);
+#pragma unroll
+      for (int j = 0; j < pw::kStageK / 16; ++j)
+        pw::tc_mma_ts(tmem + kDCol, tmem + as * kACols + 8 * j, bdesc + 2ull * j, idesc,
+                      (st > 0 || j > 0) ? 1u : 0u);
+      pw::tc_commit(bar + 8 * (kAStages + as));
+      pw::tc_commit(bar_b_empty + 8 * bs);
+    }
+    ++a_cnt;
+    __syncwarp();
+  }
+  b_cnt += u.nst;
+  pw::cp_async_wait<0>();
+  if (lane == 0) pw::tc_commit(bar_done);
+  __syncwarp();
 }
 
-// y rows of one strip for every token, in a fixed summation order.
-__device__ void combine_strip(const FfnParams& p, int strip) {
-  const int lane = static_cast<int>(pw::lane_id());
-  const int n_items = p.T * 16;
-  for (int it = lane; it < n_items; it += 32) {
-    const int t = it >> 4, ri = it & 15;
-    const int row = ri < 8 ? strip * 8 + ri : p.H / 2 + strip * 8 + (ri - 8);
+// ---------------------------------------------------------------------------
+// Combine (whole CTA): y rows of one strip for every token, fixed order.
+// ---------------------------------------------------------------------------
+__device__ void combine_strip(const Params& p, int strip) {
+  const int n_items = p.T * 128;
+  for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
+    const int t = it >> 7, pos = it & 127;
+    const int row = (pos >> 6) * (p.H / 2) + strip * 64 + (pos & 63);
     float acc = 0.f;
     for (int j = 0; j < p.k; ++j) {
       const int slot = t * p.k + j;
-      const int pos = __ldg(p.inv_perm + slot);
+      const int ps = __ldg(p.inv_perm + slot);
       const float wt = __ldg(p.w + slot);
       float s = 0.f;
-      for (int sp = 0; sp < p.nsplit; ++sp) s += __ldcg(p.part + (static_cast<long long>(sp) * p.A + pos) * p.H + row);
+      for (int sp = 0; sp < p.nsplit; ++sp) s += __ldcg(p.part + (static_cast<long long>(sp) * p.A + ps) * p.H + row);
       acc += wt * s;
     }
     p.y[static_cast<long long>(t) * p.H + row] = __half_as_ushort(__float2half_rn(acc));
   }
 }
 
-// Bounded wait of lane 0 until *ctr >= want; false if it ran out or the launch
-// was aborted (then the unit is skipped and the status word says why).
-__device__ bool wait_for(const FfnParams& p, const uint32_t* ctr, uint32_t want) {
-  bool ok = true;
-  if (pw::lane_id() == 0) {
-    const uint64_t t0 = pw::global_ns();
-    while (pw::ld_acquire_u32(ctr) < want) {
-      if (*reinterpret_cast<volatile const uint32_t*>(p.ctr + 1) != 0u) {
-        ok = false;
-        break;
-      }
-      if (pw::global_ns() - t0 > p.wait_ns) {
-        report(p.status, PW_ERR_TIMEOUT);
-        atomicExch(p.ctr + 1, 1u);
-        ok = false;
-        break;
-      }
-      __nanosleep(256);
-    }
-  }
-  return __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
-}
-
-__global__ void __launch_bounds__(kThreads) ffn_decode_kernel(FfnParams p) {
-  extern __shared__ __align__(16) uint16_t smem_lut[];
-  __shared__ int s_act[kMaxE];
-  __shared__ int s_nact;
+template <int NMAX>
+__global__ void __launch_bounds__(kThreads, 1) apl_tc_kernel(Params p) {
+  using C = Cfg<NMAX>;
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ Shared sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const uint32_t bar = pw::smem_u32(smem + C::kOffBar);
   if (threadIdx.x == 0) {
-    int n = 0;
-    for (int e = 0; e < p.E; ++e)
-      if (__ldg(p.offsets + e + 1) > __ldg(p.offsets + e)) s_act[n++] = e;
-    s_nact = n;
+    for (int i = 0; i < kAStages; ++i) {
+      pw::mbar_init(bar + 8 * i, kDeqWarps);       // A full: one arrive per dequant warp
+      pw::mbar_init(bar + 8 * (kAStages + i), 1);  // A empty: tcgen05.commit
+    }
+    for (int i = 0; i < C::kBStages; ++i) pw::mbar_init(bar + 8 * (2 * kAStages + i), 1);  // B empty
+    pw::mbar_init(bar + 8 * (2 * kAStages + C::kBStages), 1);                            // unit MMAs done
+    pw::mbar_init_fence();
+    sh.abort = 0;
+    setup_schedule<NMAX>(p, sh);
   }
+  if (warp == 0) {
+    pw::tmem_alloc(pw::smem_u32(&sh.tmem), C::kTmemCols);
+    pw::tmem_relinquish();
+  }
+  pw::tc_fence_before();
   __syncthreads();
-  const int nact = s_nact;
-  const int lane = static_cast<int>(pw::lane_id());
-  const int warp = threadIdx.x >> 5;
-  uint16_t* lut_s = smem_lut + warp * (kSmemPerWarp / sizeof(uint16_t));
-  const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(lut_s + kLutSmemPerWarp / sizeof(uint16_t)));
-  const uint32_t gu_strips = static_cast<uint32_t>(p.I / 8);
-  const uint32_t dn_strips = static_cast<uint32_t>(p.H / 16);
-  const uint32_t n_gu = static_cast<uint32_t>(nact) * gu_strips;
-  const uint32_t n_dn = static_cast<uint32_t>(nact) * dn_strips * static_cast<uint32_t>(p.nsplit);
-  uint32_t* gu_done = p.ctr + 2;
-  uint32_t* arrive = gu_done + p.E * p.nsplit;
-  const int split_cols = kSplitTiles * pw::kTileCols;
+  pw::tc_fence_after();
+  const uint32_t tmem = sh.tmem;
 
+  uint32_t a_cnt = 0, b_cnt = 0, unit_cnt = 0;
+  int abort_local = 0;
   for (;;) {
-    uint32_t u = 0;
-    if (lane == 0) u = atomicAdd(p.ctr, 1u);
-    u = __shfl_sync(0xffffffffu, u, 0);
-    if (u >= n_gu + n_dn) break;
-    if (u < n_gu) {
-      const int e = s_act[u / gu_strips];
-      const int strip = static_cast<int>(u % gu_strips);
-      const BlockDesc d = p.desc[2 * e];
-      const int off = __ldg(p.offsets + e), ne = __ldg(p.offsets + e + 1) - off;
-      if (!desc_ok(d, 2 * p.I, p.H)) {
-        if (lane == 0) report(p.status, d.q == 0 ? PW_ERR_NOT_RESIDENT : PW_ERR_UNSUPPORTED);
+    if (threadIdx.x == 0) next_unit<NMAX>(p, sh);
+    pw::tc_fence_before();
+    __syncthreads();
+    pw::tc_fence_after();
+    const Unit u = sh.u;
+    if (u.kind == kNone) break;
+    if (!u.skip) {
+      if (warp < kDeqWarps) {
+        switch (u.q) {
+          case 2: dequant_role<NMAX, 2>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 3: dequant_role<NMAX, 3>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 4: dequant_role<NMAX, 4>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 5: dequant_role<NMAX, 5>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 6: dequant_role<NMAX, 6>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 7: dequant_role<NMAX, 7>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          default: dequant_role<NMAX, 8>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+        }
       } else {
-        switch (d.q) {
-          case 2: gate_up_q<2>(p, d, off, ne, strip, lut_s, ring_s); break;
-          case 3: gate_up_q<3>(p, d, off, ne, strip, lut_s, ring_s); break;
-          case 4: gate_up_q<4>(p, d, off, ne, strip, lut_s, ring_s); break;
-          case 5: gate_up_q<5>(p, d, off, ne, strip, lut_s, ring_s); break;
-          case 6: gate_up_q<6>(p, d, off, ne, strip, lut_s, ring_s); break;
-          case 7: gate_up_q<7>(p, d, off, ne, strip, lut_s, ring_s); break;
-          default: gate_up_q<8>(p, d, off, ne, strip, lut_s, ring_s); break;
-        }
+        producer_role<NMAX>(p, u, smem, tmem, a_cnt, b_cnt, abort_local);
       }
-      const bool drop = (p.flags & PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL) && u == 0;
-      if (lane == 0 && !drop) {
-        __threadfence();
-        atomicAdd(gu_done + e * p.nsplit + (strip * 8) / split_cols, 1u);
-      }
-    } else {
-      const uint32_t v = u - n_gu;
-      const uint32_t per = dn_strips * static_cast<uint32_t>(p.nsplit);
-      const int e = s_act[v / per];
-      const uint32_t r = v % per;
-      const int split = static_cast<int>(r / dn_strips);
-      const int strip = static_cast<int>(r % dn_strips);
-      const int c0 = split * split_cols;
-      const uint32_t want = static_cast<uint32_t>((min(c0 + split_cols, p.I) - c0) / 8);
-      if (!wait_for(p, gu_done + e * p.nsplit + split, want)) continue;
-      const BlockDesc d = p.desc[2 * e + 1];
-      const int off = __ldg(p.offsets + e), ne = __ldg(p.offsets + e + 1) - off;
-      if (!desc_ok(d, p.H, p.I)) {
-        if (lane == 0) report(p.status, d.q == 0 ? PW_ERR_NOT_RESIDENT : PW_ERR_UNSUPPORTED);
-      } else {
-        switch (d.q) {
-          case 2: down_q<2>(p, d, off, ne, split, strip, lut_s, ring_s); break;
-          case 3: down_q<3>(p, d, off, ne, split, strip, lut_s, ring_s); break;
-          case 4: down_q<4>(p, d, off, ne, split, strip, lut_s, ring_s); break;
-          case 5: down_q<5>(p, d, off, ne, split, strip, lut_s, ring_s); break;
-          case 6: down_q<6>(p, d, off, ne, split, strip, lut_s, ring_s); break;
-          case 7: down_q<7>(p, d, off, ne, split, strip, lut_s, ring_s); break;
-          default: down_q<8>(p, d, off, ne, split, strip, lut_s, ring_s); break;
-        }
-      }
-      uint32_t last = 0;
-      if (lane == 0) {
-        __threadfence();
-        last = (atomicAdd(arrive + strip, 1u) == static_cast<uint32_t>(nact * p.nsplit) - 1u) ? 1u : 0u;
-        if (last) __threadfence();
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) combine_strip(p, strip);
+      ++unit_cnt;
     }
-  }
-}
-
-// ---------------------------------------------------------------------------
-// Any-precision linear (test export): out[m][n] = sum_j W[n][j] x[m][j].
-// ---------------------------------------------------------------------------
-template <int Q>
-__device__ void linear_q(const BlockDesc& d, const uint16_t* x, int M, float* out, int strip, int grp,
-                         uint16_t* lut_s, uint32_t ring_s) {
-  const int lane = static_cast<int>(pw::lane_id());
-  const int g = lane >> 2, c = lane & 3;
-  pw::load_strip_lut<Q>(d.lut, d.rows / 2, strip, lut_s);
-  __syncwarp();
-  const int tb = grp * 8 * kNtMax;
-  const int nt_count = min(kNtMax, (M - tb + 7) / 8);
-  int brow[kNtMax];
-#pragma unroll
-  for (int nt = 0; nt < kNtMax; ++nt) brow[nt] = min(tb + nt * 8 + g, M - 1) * d.cols;
-  float acc[kNtMax][4];
-#pragma unroll
-  for (int nt = 0; nt < kNtMax; ++nt)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) acc[nt][i] = 0.f;
-  pw::strip_mainloop<Q, false>(d, strip, 0, d.cols / pw::kTileCols, lut_s, ring_s, x, brow, nt_count, acc);
-  const int r0 = strip * 8 + g, r1 = d.rows / 2 + strip * 8 + g;
-#pragma unroll
-  for (int nt = 0; nt < kNtMax; ++nt) {
-    if (nt < nt_count) {
-#pragma unroll
-      for (int i = 0; i < 2; ++i) {
-        const int m = tb + nt * 8 + 2 * c + i;
-        if (m < M) {
-          out[static_cast<long long>(m) * d.rows + r0] = acc[nt][i];
-          out[static_cast<long long>(m) * d.rows + r1] = acc[nt][2 + i];
+    if (abort_local) {
+      report(p.status, PW_ERR_TIMEOUT);
+      sh.abort = 1;
+    }
+    pw::tc_fence_before();
+    __syncthreads();
+    pw::tc_fence_after();
+    if (threadIdx.x == 0) {
+      int combine = -1;
+      if (!u.skip && u.kind == kGateUp) {
+        const bool drop = (p.flags & PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL) && u.e == sh.act[0] && u.strip == 0 &&
+                          u.tg == 0;
+        if (!drop) {
+          __threadfence();
+          atomicAdd(p.ctr + 2 + u.e * p.nsplit + u.split, 1u);
+        }
+      } else if (!u.skip && u.kind == kDown) {
+        __threadfence();
+        const uint32_t prev = atomicAdd(p.ctr + 2 + p.E * p.nsplit + u.strip, 1u);
+        if (prev + 1 == static_cast<uint32_t>(sh.arrivals_per_strip)) {
+          __threadfence();
+          combine = u.strip;
         }
       }
+      sh.u.combine = combine;
     }
+    __syncthreads();
+    if (sh.u.combine >= 0) combine_strip(p, sh.u.combine);
   }
-}
-
-__global__ void __launch_bounds__(kThreads) linear_kernel(BlockDesc d, const uint16_t* x, int M, float* out) {
-  extern __shared__ __align__(16) uint16_t smem_lut[];
-  const int warp = threadIdx.x >> 5;
-  uint16_t* lut_s = smem_lut + warp * (kSmemPerWarp / sizeof(uint16_t));
-  const uint32_t ring_s = static_cast<uint32_t>(__cvta_generic_to_shared(lut_s + kLutSmemPerWarp / sizeof(uint16_t)));
-  const int strips = d.rows / 16;
-  const int groups = (M + 8 * kNtMax - 1) / (8 * kNtMax);
-  const long long unit = static_cast<long long>(blockIdx.x) * kWarps + warp;
-  if (unit >= static_cast<long long>(strips) * groups) return;
-  const int strip = static_cast<int>(unit % strips);
-  const int grp = static_cast<int>(unit / strips);
-  switch (d.q) {
-    case 2: linear_q<2>(d, x, M, out, strip, grp, lut_s, ring_s); break;
-    case 3: linear_q<3>(d, x, M, out, strip, grp, lut_s, ring_s); break;
-    case 4: linear_q<4>(d, x, M, out, strip, grp, lut_s, ring_s); break;
-    case 5: linear_q<5>(d, x, M, out, strip, grp, lut_s, ring_s); break;
-    case 6: linear_q<6>(d, x, M, out, strip, grp, lut_s, ring_s); break;
-    case 7: linear_q<7>(d, x, M, out, strip, grp, lut_s, ring_s); break;
-    default: linear_q<8>(d, x, M, out, strip, grp, lut_s, ring_s); break;
-  }
+  pw::tc_fence_before();
+  __syncthreads();
+  pw::tc_fence_after();
+  if (warp == 0) pw::tmem_dealloc(tmem, C::kTmemCols);
 }
 
 // ---------------------------------------------------------------------------
@@ -349,15 +543,22 @@ size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
   size_t ctr, h, part, total;
-  int nsplit;
+  int nsplit, split_cols;
 };
 
-WsLayout ws_layout(int T, int H, int I, int E, int k) {
+int choose_path(int T, int E, int k, int requested) {
+  if (requested == PW_PATH_DECODE || requested == PW_PATH_PREFILL) return requested;
+  // average tokens per expert: 256-token tiles pay off once experts see more
+  // than a few dozen tokens
+  return (static_cast<long long>(T) * k >= 48ll * E) ? PW_PATH_PREFILL : PW_PATH_DECODE;
+}
+
+WsLayout ws_layout(int T, int H, int I, int E, int k, int path) {
   WsLayout L{};
   const long long A = static_cast<long long>(T) * k;
-  const int split_cols = kSplitTiles * pw::kTileCols;
-  L.nsplit = (I + split_cols - 1) / split_cols;
-  const size_t ctr_words = 2 + static_cast<size_t>(E) * L.nsplit + static_cast<size_t>(H) / 16;
+  L.split_cols = path == PW_PATH_PREFILL ? I : kDecodeSplitCols;
+  L.nsplit = (I + L.split_cols - 1) / L.split_cols;
+  const size_t ctr_words = 2 + static_cast<size_t>(E) * L.nsplit + static_cast<size_t>(H) / 128;
   L.ctr = 0;
   L.h = align256(ctr_words * 4);
   L.part = L.h + align256(static_cast<size_t>(A) * I * 2);
@@ -365,12 +566,18 @@ WsLayout ws_layout(int T, int H, int I, int E, int k) {
   return L;
 }
 
+// Workspace of the path pw_moe_apl_ffn picks by itself for this size.
+WsLayout ws_layout(int T, int H, int I, int E, int k) {
+  return ws_layout(T, H, I, E, k, choose_path(T, E, k, PW_PATH_AUTO));
+}
+
 int validate_shape(int T, int H, int I, int E, int k) {
   if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxE || k < 1 || k > 8 || k > E)
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: bad sizes T=%d H=%d I=%d E=%d k=%d", T, H, I, E, k);
-  if (H % pw::kTileCols || I % pw::kTileCols)
-    return pw::set_error(PW_ERR_UNSUPPORTED, "ffn: H and I must be multiples of 256 (H=%d I=%d)", H, I);
-  if (static_cast<long long>(T) * k > (1 << 24) || static_cast<long long>(H) * I > (1ll << 31))
+  if (H % 128 || I % 128)
+    return pw::set_error(PW_ERR_UNSUPPORTED, "ffn: H and I must be multiples of 128 (H=%d I=%d)", H, I);
+  if (static_cast<long long>(T) * k > (1 << 24) || static_cast<long long>(T) * k * I > (1ll << 31) ||
+      static_cast<long long>(T) * H > (1ll << 31))
     return pw::set_error(PW_ERR_UNSUPPORTED, "ffn: problem too large");
   return PW_OK;
 }
@@ -385,10 +592,26 @@ int sm_count_cached() {
   return count;
 }
 
-int set_smem_attr(const void* fn, size_t bytes) {
-  PW_CUDA_TRY(cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes)));
+template <int NMAX>
+int launch(const Params& p, cudaStream_t s) {
+  using C = Cfg<NMAX>;
+  static bool attr_done = false;
+  if (!attr_done) {
+    PW_CUDA_TRY(cudaFuncSetAttribute(apl_tc_kernel<NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::kSmemBytes));
+    attr_done = true;
+  }
+  const int sms = sm_count_cached();
+  if (sms < 1) return pw::set_error(PW_ERR_CUDA, "could not query the SM count");
+  // one CTA per SM (the shared-memory footprint keeps it at one), each owning
+  // C::kTmemCols of the SM's 512 TMEM columns
+  apl_tc_kernel<NMAX><<<sms, kThreads, C::kSmemBytes, s>>>(p);
+  PW_CUDA_TRY(cudaGetLastError());
   return PW_OK;
 }
+
+// The linear test export's ticket counter (zeroed before each launch).
+static __device__ uint32_t g_linear_ctr[2];
 
 }  // namespace
 
@@ -396,7 +619,9 @@ extern "C" {
 
 size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k) {
   if (validate_shape(T, H, I, E, k) != PW_OK) return 0;
-  return ws_layout(T, H, I, E, k).total;
+  const size_t a = ws_layout(T, H, I, E, k, PW_PATH_DECODE).total;
+  const size_t b = ws_layout(T, H, I, E, k, PW_PATH_PREFILL).total;
+  return a > b ? a : b;
 }
 
 int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I, int E, int k,
@@ -412,16 +637,16 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
   if ((reinterpret_cast<uintptr_t>(d_desc) & 15) || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
       (reinterpret_cast<uintptr_t>(d_y) & 3))
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: descriptor/x must be 16-byte aligned, y 4-byte aligned");
-  const WsLayout L = ws_layout(T, H, I, E, k);
+  pw_ffn_options o{};
+  if (opts) o = *opts;
+  const int path = choose_path(T, E, k, o.path);
+  const WsLayout L = ws_layout(T, H, I, E, k, path);
   if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(d_ws) & 255))
     return pw::set_error(PW_ERR_WORKSPACE, "ffn: workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total,
                          ws_bytes);
-  pw_ffn_options o{};
-  if (opts) o = *opts;
-  if (o.path == PW_PATH_PREFILL) return pw::set_error(PW_ERR_UNSUPPORTED, "ffn: prefill path not built yet");
   cudaStream_t s = pw::as_stream(stream);
   char* ws = static_cast<char*>(d_ws);
-  FfnParams p{};
+  Params p{};
   p.desc = static_cast<const BlockDesc*>(d_desc) + static_cast<long long>(layer) * E * 2;
   p.x = d_x;
   p.y = d_y;
@@ -436,26 +661,16 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
   p.k = k;
   p.A = T * k;
   p.nsplit = L.nsplit;
+  p.split_cols = L.split_cols;
   p.ctr = reinterpret_cast<uint32_t*>(ws + L.ctr);
   p.h = reinterpret_cast<uint16_t*>(ws + L.h);
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.status = d_status;
   p.wait_ns = (o.wait_timeout_us ? o.wait_timeout_us : 2000000u) * 1000ull;
   p.flags = o.flags;
-
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (int e = set_smem_attr(reinterpret_cast<const void*>(ffn_decode_kernel), kSmemBytes)) return e;
-    attr_done = true;
-  }
-  int per_sm = 0;
-  PW_CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ffn_decode_kernel, kThreads, kSmemBytes));
-  const int sms = sm_count_cached();
-  if (per_sm < 1 || sms < 1) return pw::set_error(PW_ERR_CUDA, "ffn: kernel cannot be resident (occupancy 0)");
+  p.linear = 0;
   PW_CUDA_TRY(cudaMemsetAsync(p.ctr, 0, L.h - L.ctr, s));
-  ffn_decode_kernel<<<sms * per_sm, kThreads, kSmemBytes, s>>>(p);
-  PW_CUDA_TRY(cudaGetLastError());
-  return PW_OK;
+  return path == PW_PATH_PREFILL ? launch<256>(p, s) : launch<32>(p, s);
 }
 
 int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I, int E, int k,
@@ -473,23 +688,30 @@ int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,
   if (d.q < 2 || d.q > PW_MAX_BITS) return pw::set_error(PW_ERR_UNSUPPORTED, "linear: bitwidth %d", d.q);
   if (!d.lut) return pw::set_error(PW_ERR_NOT_RESIDENT, "linear: LUT %d not attached", d.q);
   if (M == 0) return PW_OK;
-  if (!d_x || !d_out || (reinterpret_cast<uintptr_t>(d_x) & 3))
+  if (!d_x || !d_out || (reinterpret_cast<uintptr_t>(d_x) & 15))
     return pw::set_error(PW_ERR_INVALID_ARG, "linear: NULL or misaligned argument");
-  static bool attr_done = false;
-  if (!attr_done) {
-    if (int e = set_smem_attr(reinterpret_cast<const void*>(linear_kernel), kSmemBytes)) return e;
-    attr_done = true;
-  }
-  const long long units = static_cast<long long>(d.rows / 16) * ((M + 8 * kNtMax - 1) / (8 * kNtMax));
-  const long long blocks = (units + kWarps - 1) / kWarps;
-  linear_kernel<<<static_cast<unsigned>(blocks), kThreads, kSmemBytes, pw::as_stream(stream)>>>(d, d_x, M, d_out);
-  PW_CUDA_TRY(cudaGetLastError());
-  return PW_OK;
+  if (static_cast<long long>(M) * d.cols > (1ll << 31))
+    return pw::set_error(PW_ERR_UNSUPPORTED, "linear: problem too large");
+  cudaStream_t s = pw::as_stream(stream);
+  void* ctr = nullptr;
+  PW_CUDA_TRY(cudaGetSymbolAddress(&ctr, g_linear_ctr));
+  PW_CUDA_TRY(cudaMemsetAsync(ctr, 0, sizeof(uint32_t) * 2, s));
+  Params p{};
+  p.lin = d;
+  p.x = d_x;
+  p.out = d_out;
+  p.M = M;
+  p.ctr = static_cast<uint32_t*>(ctr);
+  p.status = nullptr;
+  p.wait_ns = 2000000000ull;
+  p.linear = 1;
+  p.nsplit = 1;
+  p.split_cols = d.cols;
+  return M > 32 ? launch<256>(p, s) : launch<32>(p, s);
 }
 
 }  // extern "C"
 
-// ---------------------------------------------------------------------------
 // Entry point for callers that cannot allocate device memory.  Its scratch is
 // this fixed array; host code must not hand the array's name to a kernel (on
 // the host it is only a stand-in symbol), so the device address is looked up

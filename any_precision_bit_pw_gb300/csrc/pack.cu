@@ -6,13 +6,14 @@
 // index, so the top b planes carry idx >> (P-b).
 //
 // Tiled layout (the library's own choice; the pages give none): a plane is a
-// sequence of 512-byte tiles, strip-major, each covering 16 rows x 256 columns.
-// Strip s holds rows 8s..8s+7 and rows N/2+8s..N/2+8s+7, so one warp sees the
-// gate row m and the up row I+m of a gate_up block in the same lanes.  Lane l
-// owns bytes 16l..16l+15 of a tile: four uint32 words w; bit 4*elem+step%4 of
-// word step/4 is element `elem` of k-step `step` of the lane's m16n8k16
-// A-fragment (elem 0..3: row g, columns 2c, 2c+1, 2c+8, 2c+9 of the step;
-// elem 4..7: row g+8, same columns; g = l/4, c = l%4).
+// sequence of 2048-byte tiles, strip-major, each covering a 128-row strip and
+// 128 columns.  Strip s holds rows 64s..64s+63 and N/2+64s..N/2+64s+63; row
+// position pos = 32w + i within the strip is row 64s+16w+i (i < 16) or
+// N/2+64s+16w+(i-16) (i >= 16), so in a gate_up block the gate row m and the up
+// row m sit 16 lanes apart in the same warp.  Position pos owns 16 bytes of the
+// tile (four little-endian words); column 32*word + 8*js + e of the tile is
+// bit 4e + js of the word ("nibble" order: one shift and mask per plane gives
+// the indices of 8 consecutive columns).
 #include "pw_internal.h"
 
 namespace {
@@ -21,39 +22,46 @@ struct PlanePtrs {
   uint32_t* p[PW_MAX_BITS];
 };
 
-// One thread per (strip, tile, lane): gathers the lane's 128 elements and
-// writes 16 bytes to each plane.
+__device__ __forceinline__ int strip_pos_row(int strip, int pos, int half_rows) {
+  const int w = pos >> 5, i = pos & 31;
+  return (i >> 4) * half_rows + strip * 64 + 16 * w + (i & 15);
+}
+
+// One thread per (strip, tile, pos): reads 128 indices of its row and writes
+// 16 bytes to each plane.
 __global__ void pack_kernel(const uint8_t* __restrict__ idx, int rows, int cols, int P, PlanePtrs planes) {
-  const int tiles_per_strip = cols / pw::kTileCols;
-  const long long n_threads = static_cast<long long>(rows / pw::kTileRows) * tiles_per_strip * 32;
+  const int tiles = cols / pw::kTileCols;
+  const long long n_threads = static_cast<long long>(rows / pw::kTileRows) * tiles * pw::kTileRows;
   const long long tid = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   if (tid >= n_threads) return;
-  const int lane = static_cast<int>(tid & 31);
-  const long long tile_id = tid >> 5;
-  const int strip = static_cast<int>(tile_id / tiles_per_strip);
-  const int tile = static_cast<int>(tile_id % tiles_per_strip);
-  const int g = lane >> 2, c = lane & 3;
-  const int half_rows = rows / 2;
-  const uint8_t mask = static_cast<uint8_t>((1u << P) - 1u);
+  const int pos = static_cast<int>(tid % pw::kTileRows);
+  const long long tile_id = tid / pw::kTileRows;
+  const int strip = static_cast<int>(tile_id / tiles);
+  const int tile = static_cast<int>(tile_id % tiles);
+  const int n = strip_pos_row(strip, pos, rows / 2);
+  const uint32_t mask = (1u << P) - 1u;
   uint32_t words[PW_MAX_BITS][4];
 #pragma unroll
   for (int p = 0; p < PW_MAX_BITS; ++p)
 #pragma unroll
     for (int w = 0; w < 4; ++w) words[p][w] = 0u;
-  for (int step = 0; step < 16; ++step) {
-    const int w = step >> 2, js = step & 3;
+  const uint4* src = reinterpret_cast<const uint4*>(idx + static_cast<long long>(n) * cols + tile * pw::kTileCols);
 #pragma unroll
-    for (int elem = 0; elem < 8; ++elem) {
-      const int n = (elem >> 2) * half_rows + strip * 8 + g;
-      const int j = tile * pw::kTileCols + step * 16 + 2 * c + (elem & 1) + 8 * ((elem >> 1) & 1);
-      const uint32_t v = idx[static_cast<long long>(n) * cols + j] & mask;
-      const int bit = 4 * elem + js;
+  for (int v = 0; v < 8; ++v) {   // 16 columns per uint4
+    const uint4 q = src[v];
+    const uint32_t qw[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int b = 0; b < 16; ++b) {
+      const int jj = v * 16 + b;
+      const uint32_t val = (qw[b >> 2] >> (8 * (b & 3))) & mask;
+      const int w = jj >> 5, t = jj & 31;
+      const int bit = 4 * (t & 7) + (t >> 3);
 #pragma unroll
       for (int p = 0; p < PW_MAX_BITS; ++p)
-        if (p < P) words[p][w] |= ((v >> (P - 1 - p)) & 1u) << bit;
+        if (p < P) words[p][w] |= ((val >> (P - 1 - p)) & 1u) << bit;
     }
   }
-  const long long word_off = (static_cast<long long>(strip) * tiles_per_strip + tile) * (pw::kTileBytes / 4) + lane * 4;
+  const long long word_off = (static_cast<long long>(strip) * tiles + tile) * (pw::kTileBytes / 4) + pos * 4;
 #pragma unroll
   for (int p = 0; p < PW_MAX_BITS; ++p)
     if (p < P)
@@ -68,16 +76,15 @@ __global__ void unpack_kernel(pw::BlockDesc d, int b, uint8_t* __restrict__ out)
   const int n = static_cast<int>(i / d.cols), j = static_cast<int>(i % d.cols);
   const int half_rows = d.rows / 2;
   const int half = n / half_rows, r = n % half_rows;
-  const int strip = r >> 3, g = r & 7;
+  const int strip = r >> 6, rr = r & 63;
+  const int pos = 32 * (rr >> 4) + (rr & 15) + 16 * half;
   const int tile = j / pw::kTileCols, jj = j % pw::kTileCols;
-  const int step = jj >> 4, t = jj & 15;
-  const int c = (t & 7) >> 1, odd = t & 1, upper = t >> 3;
-  const int lane = 4 * g + c, elem = 4 * half + 2 * upper + odd;
-  const long long word = (static_cast<long long>(strip) * (d.cols / pw::kTileCols) + tile) * (pw::kTileBytes / 4) +
-                         lane * 4 + (step >> 2);
-  const int bit = 4 * elem + (step & 3);
+  const int word = jj >> 5, t = jj & 31;
+  const int bit = 4 * (t & 7) + (t >> 3);
+  const long long widx = (static_cast<long long>(strip) * (d.cols / pw::kTileCols) + tile) * (pw::kTileBytes / 4) +
+                         pos * 4 + word;
   uint32_t v = 0;
-  for (int p = 0; p < b; ++p) v = (v << 1) | ((__ldg(d.planes[p] + word) >> bit) & 1u);
+  for (int p = 0; p < b; ++p) v = (v << 1) | ((__ldg(d.planes[p] + widx) >> bit) & 1u);
   out[i] = static_cast<uint8_t>(v);
 }
 
@@ -94,20 +101,20 @@ size_t pw_plane_bytes(int64_t rows, int64_t cols, int layout) {
 int pw_pack_bitplanes(const uint8_t* d_idx, int64_t rows, int64_t cols, int parent_bits,
                       uint32_t* const* h_planes, int layout, void* stream) {
   if (pw_plane_bytes(rows, cols, layout) == 0)
-    return pw::set_error(PW_ERR_UNSUPPORTED, "pack: shape %lld x %lld needs rows %% 16 == 0 and cols %% 256 == 0",
+    return pw::set_error(PW_ERR_UNSUPPORTED, "pack: shape %lld x %lld needs rows and cols multiples of 128",
                          static_cast<long long>(rows), static_cast<long long>(cols));
-  if (rows > (1 << 30) || cols > (1 << 30))
-    return pw::set_error(PW_ERR_UNSUPPORTED, "pack: shape too large");
+  if (rows > (1 << 30) || cols > (1 << 30)) return pw::set_error(PW_ERR_UNSUPPORTED, "pack: shape too large");
   if (parent_bits < 1 || parent_bits > PW_MAX_BITS)
     return pw::set_error(PW_ERR_INVALID_ARG, "pack: parent_bits %d outside 1..8", parent_bits);
-  if (!d_idx || !h_planes) return pw::set_error(PW_ERR_INVALID_ARG, "pack: NULL argument");
+  if (!d_idx || !h_planes || (reinterpret_cast<uintptr_t>(d_idx) & 15))
+    return pw::set_error(PW_ERR_INVALID_ARG, "pack: NULL argument or index buffer not 16-byte aligned");
   PlanePtrs pp{};
   for (int p = 0; p < parent_bits; ++p) {
     if (!h_planes[p] || (reinterpret_cast<uintptr_t>(h_planes[p]) & 15))
       return pw::set_error(PW_ERR_INVALID_ARG, "pack: plane %d pointer NULL or not 16-byte aligned", p);
     pp.p[p] = h_planes[p];
   }
-  const long long n_threads = rows / pw::kTileRows * (cols / pw::kTileCols) * 32;
+  const long long n_threads = rows / pw::kTileRows * (cols / pw::kTileCols) * pw::kTileRows;
   const int threads = 256;
   const long long blocks = (n_threads + threads - 1) / threads;
   pack_kernel<<<static_cast<unsigned>(blocks), threads, 0, pw::as_stream(stream)>>>(

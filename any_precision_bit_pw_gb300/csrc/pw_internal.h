@@ -26,9 +26,11 @@ struct alignas(16) BlockDesc {
 };
 static_assert(sizeof(BlockDesc) == 128, "descriptor must stay 128 bytes");
 
-constexpr int kTileRows = 16;
-constexpr int kTileCols = 256;
-constexpr int kTileBytes = 512;
+// Tiled plane layout: 128-row strips x 128-column tiles, 2048 bytes per tile
+// per plane; see include/pw.h for the bit map.
+constexpr int kTileRows = 128;
+constexpr int kTileCols = 128;
+constexpr int kTileBytes = 2048;
 
 // Records a message for pw_last_error() and returns `code`.
 int set_error(int code, const char* fmt, ...);

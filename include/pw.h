@@ -53,7 +53,7 @@ const char* pw_last_error(void);
 
 /* Bytes of one bit-plane of a rows x cols block in `layout` (= rows*cols/8).
  * Returns 0 if the shape is not supported: the tiled layout needs
- * rows % 16 == 0 and cols % 256 == 0. */
+ * rows % 128 == 0 and cols % 128 == 0. */
 size_t pw_plane_bytes(int64_t rows, int64_t cols, int layout);
 
 /* Split parent-bit indices into bit-planes.
@@ -63,15 +63,15 @@ size_t pw_plane_bytes(int64_t rows, int64_t cols, int layout);
  *              16-byte aligned; plane 0 receives the most significant bit, so
  *              the top b planes hold the b-bit index idx >> (P - b)
  *  layout      PW_LAYOUT_TILED (the only layout), defined element by element:
- *                half = n / (rows/2), r = n % (rows/2), strip = r / 8, g = r % 8
- *                tile = j / 256, jj = j % 256, step = jj / 16, t = jj % 16
- *                c = (t % 8) / 2, odd = t % 2, upper = t / 8
- *                lane = 4g + c, elem = 4*half + 2*upper + odd
- *                bit (n, j) is bit 4*elem + step%4 of the little-endian uint32
- *                at byte (strip*(cols/256) + tile)*512 + 16*lane + 4*(step/4)
- *              i.e. 16-row x 256-column tiles of 512 bytes, strip-major; lane l
- *              of a warp loads the 16 bytes at 16*l of a tile and holds exactly
- *              the elements of its m16n8k16 A-fragments for 16 k-steps.
+ *                half = n / (rows/2), r = n % (rows/2), strip = r / 64, rr = r % 64
+ *                pos = 32*(rr/16) + rr%16 + 16*half
+ *                tile = j / 128, jj = j % 128, t = jj % 32
+ *                bit (n, j) is bit 4*(t%8) + t/8 of the little-endian uint32
+ *                at byte (strip*(cols/128) + tile)*2048 + 16*pos + 4*(jj/32)
+ *              i.e. 2048-byte tiles of a 128-row strip x 128 columns,
+ *              strip-major; row position pos owns 16 bytes of each tile, and
+ *              positions pos and pos+16 of a warp hold rows m and rows/2+m
+ *              (the gate and up rows of a gate_up block).
  * Values >= 2^P are masked to their low P bits.  Asynchronous on `stream`. */
 int pw_pack_bitplanes(const uint8_t* d_idx, int64_t rows, int64_t cols, int parent_bits,
                       uint32_t* const* h_planes, int layout, void* stream);
@@ -185,7 +185,10 @@ size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k);
  *  contents need not be initialised;
  *  d_status int32, set to a PW_ERR_* code on a device-side failure (left
  *  untouched on success, so the caller zeroes it beforehand).
- * Shapes: H % 256 == 0, I % 256 == 0, committed bitwidths 2..8. */
+ * Shapes: H % 128 == 0, I % 128 == 0, committed bitwidths 2..8.
+ * The call picks one of two tile shapes from the average number of tokens
+ * per expert (T*k/E): up to 32 tokens per tile below 48, else 256 (both run on
+ * the tcgen05 tensor cores; pw_moe_apl_ffn_ex can force either). */
 int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
                    int E, int k, const int32_t* d_ids, const float* d_w,
                    const int32_t* d_offsets, const int32_t* d_perm, const int32_t* d_inv_perm,
@@ -220,8 +223,8 @@ int pw_moe_apl_ffn_noalloc(const void* d_desc, int layer, const uint16_t* d_x, i
 
 /* Options of pw_moe_apl_ffn_ex (zero-initialise, then set what you need). */
 #define PW_PATH_AUTO 0
-#define PW_PATH_DECODE 1   /* CUDA-core dequant + register-fragment tensor MMA */
-#define PW_PATH_PREFILL 2  /* tcgen05/TMEM tile path */
+#define PW_PATH_DECODE 1   /* token tiles of up to 32 (decode batches) */
+#define PW_PATH_PREFILL 2  /* token tiles of up to 256 (prefill batches) */
 #define PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL 1u  /* test hook: one gate_up unit never
                                                  signals completion, so the waits
                                                  that depend on it run out */

@@ -16,17 +16,14 @@ semantics but not the memory layout; this is the library's documented
   significant) holds bit P-1-p of every index, so the b-bit index of the
   overlay is the top b bits: idx_b = idx >> (P - b)  (§1; Figure 3 draws the
   planes b7 ... b0 and the caption says subsets of planes give the lower
-  bitwidths).  Requires N % 16 == 0 and K % 256 == 0.  A plane has N*K/8 bytes.
+  bitwidths).  Requires N % 128 == 0 and K % 128 == 0.  A plane has N*K/8 bytes.
 
   Bit (n, j) of a plane sits at this position:
-    half  = n // (N/2);  r = n % (N/2);  strip = r // 8;  g = r % 8
-    tile  = j // 256;    jj = j % 256;   step = jj // 16;  t = jj % 16
-    c     = (t % 8) // 2;  odd = t % 2;   upper = t // 8
-    lane  = 4*g + c
-    elem  = 4*half + 2*upper + odd
-    word  = step // 4
-    bit   = 4*elem + step % 4                 (bit of a little-endian uint32)
-    byte offset of that uint32 = (strip * (K/256) + tile) * 512 + 16*lane + 4*word
+    half  = n // (N/2);  r = n % (N/2);  strip = r // 64;  rr = r % 64
+    w     = rr // 16;    i = rr % 16 + 16*half;  pos = 32*w + i
+    tile  = j // 128;    jj = j % 128;   word = jj // 32;  t = jj % 32
+    bit   = 4*(t % 8) + t // 8                (bit of a little-endian uint32)
+    byte offset of that uint32 = (strip * (K/128) + tile) * 2048 + 16*pos + 4*word
 """
 from __future__ import annotations
 
@@ -35,9 +32,9 @@ from typing import Callable, Dict, List, Optional, Sequence, Tuple
 
 import numpy as np
 
-TILE_ROWS = 16
-TILE_COLS = 256
-TILE_BYTES = 512
+TILE_ROWS = 128
+TILE_COLS = 128
+TILE_BYTES = 2048
 
 GATE_UP = 0
 DOWN = 1
@@ -48,7 +45,7 @@ DOWN = 1
 # ----------------------------------------------------------------------------
 def check_block_shape(N: int, K: int) -> None:
     if N <= 0 or K <= 0 or N % TILE_ROWS or K % TILE_COLS:
-        raise ValueError(f"block {N}x{K}: rows must be a multiple of 16 and cols of 256")
+        raise ValueError(f"block {N}x{K}: rows and cols must be multiples of 128")
 
 
 def plane_bytes(N: int, K: int) -> int:
@@ -65,20 +62,17 @@ def bit_address(n, j, N: int, K: int):
     half_rows = N // 2
     half = n // half_rows
     r = n % half_rows
-    strip = r // 8
-    g = r % 8
+    strip = r // 64
+    rr = r % 64
+    w = rr // 16
+    i = rr % 16 + 16 * half
+    pos = 32 * w + i
     tile = j // TILE_COLS
     jj = j % TILE_COLS
-    step = jj // 16
-    t = jj % 16
-    c = (t % 8) // 2
-    odd = t % 2
-    upper = t // 8
-    lane = 4 * g + c
-    elem = 4 * half + 2 * upper + odd
-    word = step // 4
-    bit = 4 * elem + step % 4
-    word_byte = (strip * (K // TILE_COLS) + tile) * TILE_BYTES + 16 * lane + 4 * word
+    word = jj // 32
+    t = jj % 32
+    bit = 4 * (t % 8) + t // 8
+    word_byte = (strip * (K // TILE_COLS) + tile) * TILE_BYTES + 16 * pos + 4 * word
     # little-endian uint32: bit b of the word is bit b % 8 of byte b // 8
     return 8 * word_byte + bit
 

@@ -40,7 +40,7 @@ def _planes_bytes(planes):
 # ---------------------------------------------------------------------------
 # packer / unpack
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("N,K,P", [(16, 256, 1), (16, 256, 8), (64, 512, 8), (1024, 256, 4), (48, 768, 3),
+@pytest.mark.parametrize("N,K,P", [(128, 128, 1), (128, 256, 8), (256, 512, 8), (1024, 256, 4), (384, 768, 3),
                                    (2048, 4096, 8)])
 def test_pack_bytes_match_oracle(N, K, P):
     g = torch.Generator().manual_seed(N + K + P)
@@ -69,7 +69,7 @@ def _table_for(idx_dev, P, S, luts=None, q=None):
     return t, keep
 
 
-@pytest.mark.parametrize("N,K", [(64, 512), (1024, 768)])
+@pytest.mark.parametrize("N,K", [(128, 512), (1024, 768)])
 def test_unpack_is_top_bits(N, K):
     g = torch.Generator().manual_seed(3)
     idx = torch.randint(0, 256, (N, K), generator=g, dtype=torch.uint8)
@@ -88,7 +88,7 @@ def test_unpack_is_top_bits(N, K):
 # any-precision linear
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("q", [2, 3, 4, 5, 6, 7, 8])
-@pytest.mark.parametrize("N,K,M", [(64, 512, 1), (48, 768, 7), (32, 256, 64), (64, 1024, 70)])
+@pytest.mark.parametrize("N,K,M", [(128, 512, 1), (384, 768, 7), (128, 256, 64), (256, 1024, 70), (128, 128, 300)])
 def test_apl_linear_matches_oracle(q, N, K, M):
     g = torch.Generator().manual_seed(q * 100 + N + K + M)
     idx = torch.randint(0, 256, (N, K), generator=g, dtype=torch.uint8)
@@ -107,7 +107,7 @@ def test_apl_linear_matches_oracle(q, N, K, M):
         pw.pw_page_table_destroy(t)
 
 
-@pytest.mark.parametrize("q,N,K,M", [(8, 64, 512, 5), (3, 32, 768, 9), (5, 16, 4096, 3)])
+@pytest.mark.parametrize("q,N,K,M", [(8, 128, 512, 5), (3, 256, 768, 40), (5, 128, 4096, 3), (2, 128, 128, 17)])
 def test_apl_linear_identity_lut_is_exact(q, N, K, M):
     """LUT_q[n][c] = c and integer x: the GPU result equals the integer matmul
     of the q-bit indices exactly (every partial sum is an integer < 2^24)."""
@@ -231,19 +231,34 @@ def test_ffn_is_deterministic():
     assert s1 == 0 and np.array_equal(y1, y2)
 
 
+@pytest.mark.parametrize("path", [pw.PW_PATH_DECODE, pw.PW_PATH_PREFILL])
 @pytest.mark.parametrize("H,I,E,k,T,bits", [
     (256, 256, 1, 1, 5, (3, 5)),          # single expert, k = 1
-    (256, 512, 2, 2, 80, (8, 2)),         # 80 tokens per expert: two token groups of 64 + 16
+    (256, 512, 2, 2, 80, (8, 2)),         # 80 tokens per expert: several token tiles on the decode path
     (512, 768, 4, 2, 1, (4, 7)),          # one token
     (256, 2304, 3, 1, 9, (6, 3)),         # I not a multiple of the 2048-column down split
+    (384, 640, 2, 2, 300, (5, 4)),        # odd strip counts, 300 tokens per expert
 ])
-def test_ffn_edge_shapes(H, I, E, k, T, bits):
+def test_ffn_edge_shapes(H, I, E, k, T, bits, path):
     wl = synth.Workload("edge", synth.MoEShape(H, I, E, k), tokens=T, parent_bits=8, seed_bits=2, seed=H + I + T,
                         bits_mode="uniform_choice", bits_choices=bits)
     li = synth.layer_inputs(wl)
-    y, status, _, _ = _run_gpu(li)
+    opts = pw.pw_ffn_options()
+    opts.path = path
+    y, status, _, _ = _run_gpu(li, options=opts)
     assert status == 0
     y_ref, _ = _oracle_y(li)
+    _assert_close(y_ref, y)
+
+
+@pytest.mark.parametrize("path", [pw.PW_PATH_DECODE, pw.PW_PATH_PREFILL])
+def test_ffn_tiny_workload_both_paths(path):
+    li = synth.layer_inputs(synth.TINY_LAYER)
+    opts = pw.pw_ffn_options()
+    opts.path = path
+    y, status, _, _ = _run_gpu(li, options=opts)
+    assert status == 0
+    y_ref, _ = _oracle_y(li, from_planes=True)
     _assert_close(y_ref, y)
 
 

@@ -44,7 +44,7 @@ def test_plane_bytes(L):
     assert pw.pw_plane_bytes(16, 256, layout=0) == 0
 
 
-def _table(blocks=2, rows=64, cols=512, P=8, S=3):
+def _table(blocks=2, rows=128, cols=512, P=8, S=3):
     infos = [pw.pw_block_info(rows, cols, P, S, pw.PW_LAYOUT_TILED, 0) for _ in range(blocks)]
     return pw.pw_page_table_create(infos)
 

@@ -23,17 +23,17 @@ def test_lsb_first_plane_order_is_caught(monkeypatch):
             rev |= ((out >> i) & 1) << (b - 1 - i)
         return rev
     monkeypatch.setattr(apl, "unpack_indices", lsb_first)
-    _fails(pins.test_overlay_invariant_and_round_trip, 32, 512, 8)
+    _fails(pins.test_overlay_invariant_and_round_trip, 128, 512, 8)
 
 
 def test_wrong_layout_lane_is_caught(monkeypatch):
     real = apl.bit_address
 
-    def swapped(n, j, N, K):   # swap the two column pairs of a lane
+    def swapped(n, j, N, K):   # swap neighbouring 8-column groups of a word
         j = np.asarray(j)
         return real(n, j ^ 8, N, K)
     monkeypatch.setattr(apl, "bit_address", swapped)
-    _fails(pins.test_layout_hand_derived_points, 32, 512, 0, 8, 1, 0)
+    _fails(pins.test_layout_hand_derived_points, 256, 256, 0, 8, 0, 1)
 
 
 def test_sigmoid_instead_of_silu_is_caught(monkeypatch):

@@ -43,7 +43,7 @@ def test_layout_hand_derived_points(N, K, n, j, byte, bit):
     assert int(plane[byte]) == 1 << bit
 
 
-@pytest.mark.parametrize("N,K", [(16, 256), (32, 512), (48, 768), (1024, 256)])
+@pytest.mark.parametrize("N,K", [(128, 128), (256, 256), (384, 640), (1024, 128)])
 def test_layout_is_a_bijection(N, K):
     n = np.arange(N)[:, None]
     j = np.arange(K)[None, :]
@@ -51,7 +51,7 @@ def test_layout_is_a_bijection(N, K):
     assert np.array_equal(np.sort(a), np.arange(N * K))
 
 
-@pytest.mark.parametrize("N,K,P", [(32, 512, 8), (1024, 256, 4), (256, 512, 4), (64, 256, 3)])
+@pytest.mark.parametrize("N,K,P", [(128, 512, 8), (1024, 256, 4), (256, 512, 4), (128, 256, 3)])
 def test_overlay_invariant_and_round_trip(N, K, P):
     """For every b: the b-bit index read from the top b planes equals the
     parent index shifted right by P - b; at b = P it is the input."""
@@ -72,26 +72,26 @@ def test_lower_planes_do_not_change_higher_bitwidths():
     """Dropping planes >= b leaves the b-bit view untouched (pages above the
     committed bitwidth can be released, §3.1)."""
     rng = np.random.default_rng(5)
-    idx = _rand_idx(rng, 64, 512, 8)
+    idx = _rand_idx(rng, 128, 512, 8)
     planes = apl.pack_bitplanes(idx, 8)
     for b in range(1, 8):
-        assert np.array_equal(apl.unpack_indices(planes[:b], b, 64, 512),
-                              apl.unpack_indices(planes, b, 64, 512))
+        assert np.array_equal(apl.unpack_indices(planes[:b], b, 128, 512),
+                              apl.unpack_indices(planes, b, 128, 512))
 
 
 def test_shape_rules():
     with pytest.raises(ValueError):
-        apl.pack_bitplanes(np.zeros((8, 256), np.uint8), 4)
+        apl.pack_bitplanes(np.zeros((64, 256), np.uint8), 4)
     with pytest.raises(ValueError):
-        apl.pack_bitplanes(np.zeros((16, 128), np.uint8), 4)
+        apl.pack_bitplanes(np.zeros((128, 64), np.uint8), 4)
     with pytest.raises(ValueError):
-        apl.pack_bitplanes(np.full((16, 256), 16, np.uint8), 4)
+        apl.pack_bitplanes(np.full((128, 128), 16, np.uint8), 4)
 
 
 # ---------------------------------------------------------------------------
 # Dequant + linear: identity LUT and constant LUT
 # ---------------------------------------------------------------------------
-@pytest.mark.parametrize("N,K,P,b,M", [(32, 512, 8, 8, 5), (64, 256, 8, 3, 3), (48, 768, 4, 2, 7)])
+@pytest.mark.parametrize("N,K,P,b,M", [(128, 512, 8, 8, 5), (128, 256, 8, 3, 3), (384, 768, 4, 2, 7)])
 def test_identity_lut_is_an_integer_matmul(N, K, P, b, M):
     """LUT_b[n][c] = c makes the layer an exact integer matmul of the b-bit
     indices (sums stay far below 2^53)."""
@@ -109,10 +109,10 @@ def test_identity_lut_is_an_integer_matmul(N, K, P, b, M):
 def test_constant_lut_closed_form():
     """LUT rows constant c_n: out[m][n] = c_n * sum_j x[m][j]."""
     rng = np.random.default_rng(11)
-    N, K, P = 32, 512, 6
+    N, K, P = 128, 512, 6
     idx = _rand_idx(rng, N, K, P)
     planes = apl.pack_bitplanes(idx, P)
-    c = (np.arange(N) - 16).astype(np.float16) / np.float16(8)
+    c = (np.arange(N) - 64).astype(np.float16) / np.float16(16)
     lut = np.repeat(c[:, None], 1 << 4, axis=1)
     x = rng.standard_normal((3, K)).astype(np.float16)
     got = apl.apl_linear(planes, lut, 4, N, K, x)
@@ -123,7 +123,7 @@ def test_constant_lut_closed_form():
 def test_lut_row_selects_output_row():
     """Only LUT row n affects output n (one LUT per output row)."""
     rng = np.random.default_rng(12)
-    N, K, P = 32, 256, 4
+    N, K, P = 128, 256, 4
     idx = _rand_idx(rng, N, K, P)
     planes = apl.pack_bitplanes(idx, P)
     lut = np.zeros((N, 16), np.float16)
@@ -309,7 +309,7 @@ def test_index_block_equals_plane_block():
     """The definition path (idx >> (P - q)) and the packed-plane path agree
     exactly, so either may serve as the oracle of a block."""
     rng = np.random.default_rng(41)
-    N, K, P = 64, 512, 8
+    N, K, P = 128, 512, 8
     idx = _rand_idx(rng, N, K, P)
     planes = apl.pack_bitplanes(idx, P)
     luts = {b: np.sort(rng.standard_normal((N, 1 << b)).astype(np.float16), axis=1) for b in range(2, 9)}
