@@ -91,20 +91,13 @@ struct RowDequant<Q, true> {
     p23 = prmt(l, h, 0x7362u);
   }
 
-  // w[p][wd]: word wd (columns 32wd..32wd+31 of the stage) of plane p.
-  __device__ __forceinline__ void stage(const uint32_t (&w)[Q][2], uint32_t (&out)[32]) const {
+  // ww[p]: one 32-column word of plane p -> 16 fp16 pairs (columns in order).
+  __device__ __forceinline__ void word(const uint32_t (&ww)[Q], uint32_t (&out)[16]) const {
 #pragma unroll
-    for (int wd = 0; wd < 2; ++wd) {
-      uint32_t ww[Q];
-#pragma unroll
-      for (int p = 0; p < Q; ++p) ww[p] = w[p][wd];
-#pragma unroll
-      for (int js = 0; js < 4; ++js) {
-        const uint32_t s = nibble_sel<0, Q>(ww, js);
-        const int c0 = 16 * wd + 4 * js;
-        quad(s, out[c0], out[c0 + 1]);
-        quad(s >> 16, out[c0 + 2], out[c0 + 3]);
-      }
+    for (int js = 0; js < 4; ++js) {
+      const uint32_t s = nibble_sel<0, Q>(ww, js);
+      quad(s, out[4 * js], out[4 * js + 1]);
+      quad(s >> 16, out[4 * js + 2], out[4 * js + 3]);
     }
   }
 };
@@ -142,26 +135,19 @@ struct RowDequant<Q, false> {
     return lds_u16(tbl + (idx << 7));
   }
 
-  __device__ __forceinline__ void stage(const uint32_t (&w)[Q][2], uint32_t (&out)[32]) const {
+  __device__ __forceinline__ void word(const uint32_t (&ww)[Q], uint32_t (&out)[16]) const {
 #pragma unroll
-    for (int wd = 0; wd < 2; ++wd) {
-      uint32_t ww[Q];
+    for (int js = 0; js < 4; ++js) {
+      const uint32_t hi = nibble_sel<0, Q - 4>(ww, js);
+      const uint32_t lo = nibble_sel<Q - 4, Q>(ww, js);
+      uint32_t v[8];
 #pragma unroll
-      for (int p = 0; p < Q; ++p) ww[p] = w[p][wd];
-#pragma unroll
-      for (int js = 0; js < 4; ++js) {
-        const uint32_t hi = nibble_sel<0, Q - 4>(ww, js);
-        const uint32_t lo = nibble_sel<Q - 4, Q>(ww, js);
-        uint32_t v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const uint32_t idx = ((lo >> (4 * e)) & 0xFu) | (((hi >> (4 * e)) & 0xFu) << 4);
-          v[e] = look(idx);
-        }
-        const int c0 = 16 * wd + 4 * js;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) out[c0 + i] = v[2 * i] | (v[2 * i + 1] << 16);
+      for (int e = 0; e < 8; ++e) {
+        const uint32_t idx = ((lo >> (4 * e)) & 0xFu) | (((hi >> (4 * e)) & 0xFu) << 4);
+        v[e] = look(idx);
       }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) out[4 * js + i] = v[2 * i] | (v[2 * i + 1] << 16);
     }
   }
 };

@@ -24,20 +24,20 @@
 //     forms y[t][rows] = sum_j w[t][j] * sum_p partial[p][pos(t,j)][row] in a
 //     fixed order, rounds to fp16 and writes y.
 //
-// Inside a unit (warp roles):
-//   warps 0-3 (128 threads, thread = one row = one TMEM lane): stream their
-//     rows' committed bit-planes into shared memory with cp.async, dequantise
-//     64 columns per stage through the row's LUT (dequant.cuh) and write the
-//     fp16 operand A straight into a 4-stage TMEM ring with tcgen05.st;
-//   warp 4: gathers the B operand (the tokens' x rows, or h rows) for each
-//     stage into a 128-byte-swizzled shared ring with cp.async, and its lane 0
-//     issues tcgen05.mma (A from TMEM, B from shared memory, fp32 accumulator
-//     in TMEM), releasing ring slots with tcgen05.commit;
-//   epilogue: warps 0-3 read the accumulator rows from TMEM.
-// Every mbarrier wait is bounded; a thread whose wait runs out reports
-// PW_ERR_TIMEOUT, stops waiting for the rest of the unit (it still arrives
-// where it must, so the other roles reach the end of the unit) and the CTA
-// takes no further units.  TMEM is always released before the CTA exits.
+// Inside a unit (warp roles), for each of G groups (G = 2 on the decode path,
+// where the two groups split the unit's K range over the same strip):
+//   4 dequant warps (128 threads, thread = one row = one TMEM lane): stream the
+//     strip's committed bit-planes into a shared ring with cp.async (one
+//     16-byte slice per row and plane per 128 columns, rows interleaved so
+//     the reads are conflict-free), dequantise 64 columns per stage through
+//     the row's LUT (dequant.cuh) and write the fp16 operand A straight into a
+//     4-stage TMEM ring with tcgen05.st;
+//   1 producer warp: gathers the B operand (the tokens' x rows, or h rows) for
+//     each stage into a 128-byte-swizzled shared ring with cp.async, and its
+//     lane 0 issues tcgen05.mma (A from TMEM, B from shared memory, fp32
+//     accumulator in TMEM), releasing ring slots with tcgen05.commit;
+//   epilogue: the dequant warps read the accumulator rows from TMEM (group 1
+//     hands its partial sums to group 0 through shared memory).
 #include <cuda_fp16.h>
 
 #include <mutex>
@@ -49,32 +49,41 @@ namespace {
 
 using pw::BlockDesc;
 
-constexpr int kDeqWarps = 4;
+constexpr int kDeqWarps = 4;                // per group: one warp per TMEM lane quadrant
 constexpr int kDeqThreads = 128;
-constexpr int kThreads = kDeqThreads + 32;
 constexpr int kAStages = 4;
 constexpr int kACols = pw::kStageK / 2;     // 32 TMEM columns (fp16 pairs) per stage
-constexpr int kDCol = kAStages * kACols;    // accumulator columns start here
-constexpr int kRingBytesPerLane = 256;      // per-row plane staging ring
+constexpr int kDCol = kAStages * kACols;    // accumulator columns start here (per group)
+constexpr int kRingBytes = 32768;           // per group: plane staging ring [slot][plane][pos][16 B]
 constexpr int kDecodeSplitCols = 2048;      // down K-split of the decode path
 constexpr int kMaxE = 256;
+constexpr int kBarsPerGroup = 16;
 
 enum UnitKind : int { kNone = -1, kGateUp = 0, kDown = 1, kLinear = 2 };
 
-template <int NMAX>
+// NMAX: tokens per tile.  G: dequant groups per CTA; with G = 2 both groups
+// work on the same strip (sharing its LUT) and split the unit's K range, and
+// their accumulators are summed through shared memory in the epilogue.
+template <int NMAX, int G>
 struct Cfg {
+  static constexpr int kThreads = G * (kDeqThreads + 32);
   static constexpr int kBStages = NMAX <= 64 ? 4 : 3;
   static constexpr int kBLookahead = kBStages - 2;
   static constexpr int kBStageBytes = NMAX * 128;
-  static constexpr int kTmemCols = (kDCol + NMAX) <= 256 ? 256 : 512;
+  static constexpr int kGroupTmemCols = (kDCol + NMAX) <= 256 ? 256 : 512;
+  static constexpr int kTmemCols = G * kGroupTmemCols;
   static constexpr int kOffB = 0;
-  static constexpr int kOffRing = kOffB + kBStages * kBStageBytes;
-  static constexpr int kOffLut = kOffRing + kDeqThreads * kRingBytesPerLane;
-  static constexpr int kOffBar = kOffLut + kDeqWarps * pw::kLutBytesPerWarp;
-  static constexpr int kOffRows = kOffBar + 256;
-  static constexpr int kSmemUsed = kOffRows + NMAX * 4;
+  static constexpr int kOffRing = kOffB + G * kBStages * kBStageBytes;
+  static constexpr int kOffLut = kOffRing + G * kRingBytes;
+  static constexpr int kOffX = kOffLut + kDeqWarps * pw::kLutBytesPerWarp;
+  static constexpr int kXBytes = G == 2 ? NMAX * kDeqThreads * 4 : 0;
+  static constexpr int kOffBar = kOffX + kXBytes;
+  static constexpr int kOffRows = kOffBar + G * kBarsPerGroup * 8;
+  static constexpr int kSmemUsed = kOffRows + G * NMAX * 4;
   static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
   static_assert(kBStageBytes % 1024 == 0, "B stages must keep 1024-byte alignment");
+  static_assert(kTmemCols <= 512, "TMEM has 512 columns");
+  static_assert(2 * kAStages + kBStages + 1 <= kBarsPerGroup, "barrier slots");
 };
 
 struct Params {
@@ -264,61 +273,87 @@ __device__ void next_unit(const Params& p, Shared& sh) {
 }
 
 // ---------------------------------------------------------------------------
-// Dequant warps
+// Dequant warps (group g: warps 4g..4g+3; pos = row position in the strip)
 // ---------------------------------------------------------------------------
-template <int NMAX, int Q>
-__device__ void dequant_role(const Params& p, const Unit& u, uint8_t* smem, uint32_t tmem, uint32_t& a_cnt,
+__device__ __forceinline__ void dequant_bar_sync(int G) {
+  if (G == 2) asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+
+__device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t (&v)[4]) {
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(addr));
+}
+
+template <int NMAX, int G, int Q>
+__device__ __noinline__ void dequant_role(const Params& p, const Unit& u, uint8_t* smem, uint32_t tmem, uint32_t& a_cnt,
                              uint32_t unit_cnt, int& abort) {
-  using C = Cfg<NMAX>;
+  using C = Cfg<NMAX, G>;
   constexpr int kTileStrideW = pw::kTileBytes / 4;
-  constexpr int kTileBytesLane = Q * 16;
-  constexpr int D = (kRingBytesPerLane / kTileBytesLane) > 4 ? 4 : (kRingBytesPerLane / kTileBytesLane);
+  constexpr int kSlotBytes = Q * pw::kTileBytes;      // one tile of every plane, all 128 rows
+  constexpr int D = (kRingBytes / kSlotBytes) > 4 ? 4 : (kRingBytes / kSlotBytes);
   static_assert(D >= 2, "ring too small");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int pos = threadIdx.x;  // 0..127
+  const int g = warp >> 2;
+  const int pos = (warp & 3) * 32 + lane;
   const BlockDesc& d = *u.d;
-  const int half_rows = d.rows / 2;
-  const int row = strip_pos_row(u.strip, pos, half_rows);
-  const uint32_t lut_warp = pw::smem_u32(smem + C::kOffLut + warp * pw::kLutBytesPerWarp);
+  const int row = strip_pos_row(u.strip, pos, d.rows / 2);
+  const uint32_t lut_warp = pw::smem_u32(smem + C::kOffLut + (warp & 3) * pw::kLutBytesPerWarp);
   pw::RowDequant<Q> dq;
-  dq.load(d.lut + static_cast<long long>(row) * (1 << Q), lut_warp, lane);
+  if constexpr (Q <= 4) {
+    dq.load(d.lut + static_cast<long long>(row) * (1 << Q), lut_warp, lane);
+  } else {
+    if (g == 0) dq.load(d.lut + static_cast<long long>(row) * (1 << Q), lut_warp, lane);
+    dq.tbl = lut_warp + static_cast<uint32_t>(lane) * 4u;
+    dequant_bar_sync(G);   // group 0 filled the shared table both groups read
+  }
 
+  // this group's share of the unit's tiles
   const int tiles = d.cols / pw::kTileCols;
-  const int tile0 = u.st0 / 2;
-  const int ntiles = u.nst / 2;
+  const int ntiles_all = u.nst / 2;
+  const int half = (ntiles_all + 1) / 2;
+  const int tb = (G == 2 && g == 1) ? half : 0;
+  const int te = (G == 2 && g == 0) ? half : ntiles_all;
+  const int ntiles = te - tb;
+  const int tile0 = u.st0 / 2 + tb;
   const uint32_t* src[Q];
 #pragma unroll
   for (int q = 0; q < Q; ++q)
     src[q] = d.planes[q] + (static_cast<long long>(u.strip) * tiles + tile0) * kTileStrideW + pos * 4;
-  const uint32_t ring = pw::smem_u32(smem + C::kOffRing + pos * kRingBytesPerLane);
+  const uint32_t ring = pw::smem_u32(smem + C::kOffRing + g * kRingBytes) + pos * 16;
   auto issue = [&](int t) {
     if (t < ntiles) {
-      const uint32_t slot = ring + (t % D) * kTileBytesLane;
+      const uint32_t slot = ring + (t % D) * kSlotBytes;
 #pragma unroll
-      for (int q = 0; q < Q; ++q) pw::cp_async_16(slot + q * 16, src[q] + static_cast<long long>(t) * kTileStrideW);
+      for (int q = 0; q < Q; ++q)
+        pw::cp_async_16(slot + q * pw::kTileBytes, src[q] + static_cast<long long>(t) * kTileStrideW);
     }
     pw::cp_async_commit();
   };
 #pragma unroll
   for (int i = 0; i < D - 1; ++i) issue(i);
 
-  const uint32_t bar = pw::smem_u32(smem + C::kOffBar);
-  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * warp) << 16);
+  const uint32_t bar = pw::smem_u32(smem + C::kOffBar + g * kBarsPerGroup * 8);
+  const uint32_t tl = tmem + g * C::kGroupTmemCols + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
   for (int t = 0; t < ntiles; ++t) {
     issue(t + D - 1);
     pw::cp_async_wait<D - 1>();
-    const uint32_t slot = ring + (t % D) * kTileBytesLane;
+    const uint32_t slot = ring + (t % D) * kSlotBytes;
+    uint32_t w4[Q][4];
+#pragma unroll
+    for (int q = 0; q < Q; ++q) lds_v4(slot + q * pw::kTileBytes, w4[q]);
 #pragma unroll
     for (int hf = 0; hf < 2; ++hf) {
-      uint32_t words[Q][2];
-#pragma unroll
-      for (int q = 0; q < Q; ++q) pw::lds_v2(slot + q * 16 + hf * 8, words[q][0], words[q][1]);
-      uint32_t out[32];
-      dq.stage(words, out);
       const uint32_t as = a_cnt % kAStages, use = a_cnt / kAStages;
       if (use > 0 && !abort && !pw::mbar_wait(bar + 8 * (kAStages + as), (use - 1) & 1u, p.wait_ns)) abort = 1;
       pw::tc_fence_after();
-      pw::tmem_st_x32(tl + as * kACols, out);
+#pragma unroll
+      for (int wd = 0; wd < 2; ++wd) {
+        uint32_t ww[Q];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) ww[q] = w4[q][2 * hf + wd];
+        uint32_t out[16];
+        dq.word(ww, out);
+        pw::tmem_st_x16(tl + as * kACols + 16 * wd, out);
+      }
       pw::tmem_st_wait();
       pw::tc_fence_before();
       __syncwarp();
@@ -331,6 +366,23 @@ __device__ void dequant_role(const Params& p, const Unit& u, uint8_t* smem, uint
   // epilogue: accumulator row `pos` (TMEM lane), columns = tokens
   if (!abort && !pw::mbar_wait(bar + 8 * (2 * kAStages + C::kBStages), unit_cnt & 1u, p.wait_ns)) abort = 1;
   pw::tc_fence_after();
+  float* xch = reinterpret_cast<float*>(smem + C::kOffX);
+  if (G == 2 && g == 1) {
+    // hand this group's partial sums to group 0 ([token][pos] layout)
+    for (int c = 0; c < u.npad / 16; ++c) {
+      uint32_t v[16];
+      if (ntiles > 0) {
+        pw::tmem_ld_x16(tl + kDCol + 16 * c, v);
+        pw::tmem_ld_wait();
+      }
+#pragma unroll
+      for (int i = 0; i < 16; ++i) xch[(16 * c + i) * kDeqThreads + pos] = ntiles > 0 ? __uint_as_float(v[i]) : 0.f;
+    }
+    pw::tc_fence_before();
+    dequant_bar_sync(G);
+    return;
+  }
+  if (G == 2) dequant_bar_sync(G);
   for (int c = 0; c < u.npad / 16; ++c) {
     uint32_t v[16];
     pw::tmem_ld_x16(tl + kDCol + 16 * c, v);
@@ -338,11 +390,12 @@ __device__ void dequant_role(const Params& p, const Unit& u, uint8_t* smem, uint
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int n = 16 * c + i;
-      const float val = __uint_as_float(v[i]);
+      float val = __uint_as_float(v[i]);
+      if (G == 2) val += xch[n * kDeqThreads + pos];
       if (u.kind == kGateUp) {
         const float up = __shfl_down_sync(0xffffffffu, val, 16);
         if (lane < 16 && n < u.nrows) {
-          const int m = u.strip * 64 + 16 * warp + lane;
+          const int m = u.strip * 64 + 16 * (warp & 3) + lane;
           p.h[static_cast<long long>(u.off + n) * p.I + m] = __half_as_ushort(__float2half_rn(silu(val) * up));
         }
       } else if (u.kind == kDown) {
@@ -356,14 +409,15 @@ __device__ void dequant_role(const Params& p, const Unit& u, uint8_t* smem, uint
 }
 
 // ---------------------------------------------------------------------------
-// Producer / MMA warp
+// Producer / MMA warp of group g (warp 4G + g)
 // ---------------------------------------------------------------------------
-template <int NMAX>
+template <int NMAX, int G>
 __device__ void producer_role(const Params& p, const Unit& u, uint8_t* smem, uint32_t tmem, uint32_t& a_cnt,
                               uint32_t& b_cnt, int& abort) {
-  using C = Cfg<NMAX>;
+  using C = Cfg<NMAX, G>;
   const int lane = threadIdx.x & 31;
-  int* rows = reinterpret_cast<int*>(smem + C::kOffRows);
+  const int g = (threadIdx.x >> 5) - 4 * G;
+  int* rows = reinterpret_cast<int*>(smem + C::kOffRows) + g * NMAX;
   const uint16_t* bbase = u.kind == kDown ? p.h : p.x;
   for (int n = lane; n < u.npad; n += 32) {
     const int nn = min(n, u.nrows - 1);
@@ -377,16 +431,23 @@ __device__ void producer_role(const Params& p, const Unit& u, uint8_t* smem, uin
     rows[n] = r;
   }
   __syncwarp();
-  const uint32_t bring = pw::smem_u32(smem + C::kOffB);
-  const uint32_t bar = pw::smem_u32(smem + C::kOffBar);
+  // this group's stages
+  const int ntiles_all = u.nst / 2;
+  const int half = (ntiles_all + 1) / 2;
+  const int sb = 2 * ((G == 2 && g == 1) ? half : 0);
+  const int se = 2 * ((G == 2 && g == 0) ? half : ntiles_all);
+  const int nst = se - sb;
+  const uint32_t bring = pw::smem_u32(smem + C::kOffB + g * C::kBStages * C::kBStageBytes);
+  const uint32_t bar = pw::smem_u32(smem + C::kOffBar + g * kBarsPerGroup * 8);
   const uint32_t bar_b_empty = bar + 8 * (2 * kAStages);
   const uint32_t bar_done = bar + 8 * (2 * kAStages + C::kBStages);
+  const uint32_t tg = tmem + g * C::kGroupTmemCols;
   const int chunks = u.npad * 8;
   auto issue = [&](int st) {
     const uint32_t slot = (b_cnt + st) % C::kBStages, use = (b_cnt + st) / C::kBStages;
     if (use > 0 && !abort && !pw::mbar_wait(bar_b_empty + 8 * slot, (use - 1) & 1u, p.wait_ns)) abort = 1;
     const uint32_t dst0 = bring + slot * C::kBStageBytes;
-    const long long col = static_cast<long long>(u.st0 + st) * pw::kStageK;
+    const long long col = static_cast<long long>(u.st0 + sb + st) * pw::kStageK;
     for (int i = lane; i < chunks; i += 32) {
       const int n = i >> 3, c = i & 7;
       pw::cp_async_16(dst0 + n * 128 + ((c ^ (n & 7)) << 4), bbase + rows[n] + col + c * 8);
@@ -395,12 +456,12 @@ __device__ void producer_role(const Params& p, const Unit& u, uint8_t* smem, uin
   constexpr int LA = C::kBLookahead;
 #pragma unroll
   for (int i = 0; i < LA; ++i) {
-    if (i < u.nst) issue(i);
+    if (i < nst) issue(i);
     pw::cp_async_commit();
   }
   const uint32_t idesc = pw::idesc_f16_f32(128, u.npad);
-  for (int st = 0; st < u.nst; ++st) {
-    if (st + LA < u.nst) issue(st + LA);
+  for (int st = 0; st < nst; ++st) {
+    if (st + LA < nst) issue(st + LA);
     pw::cp_async_commit();
     pw::cp_async_wait<LA>();
     pw::fence_proxy_async_smem();
@@ -413,17 +474,21 @@ __device__ void producer_role(const Params& p, const Unit& u, uint8_t* smem, uin
       const uint64_t bdesc = pw::sdesc_kmajor_sw128(bring + bs * C::kBStageBytes);
 #pragma unroll
       for (int j = 0; j < pw::kStageK / 16; ++j)
-        pw::tc_mma_ts(tmem + kDCol, tmem + as * kACols + 8 * j, bdesc + 2ull * j, idesc,
-                      (st > 0 || j > 0) ? 1u : 0u);
+        pw::tc_mma_ts(tg + kDCol, tg + as * kACols + 8 * j, bdesc + 2ull * j, idesc, (st > 0 || j > 0) ? 1u : 0u);
       pw::tc_commit(bar + 8 * (kAStages + as));
       pw::tc_commit(bar_b_empty + 8 * bs);
     }
     ++a_cnt;
     __syncwarp();
   }
-  b_cnt += u.nst;
+  b_cnt += nst;
   pw::cp_async_wait<0>();
-  if (lane == 0) pw::tc_commit(bar_done);
+  if (lane == 0) {
+    if (nst > 0)
+      pw::tc_commit(bar_done);
+    else
+      pw::mbar_arrive(bar_done);
+  }
   __syncwarp();
 }
 
@@ -448,21 +513,23 @@ __device__ void combine_strip(const Params& p, int strip) {
   }
 }
 
-template <int NMAX>
-__global__ void __launch_bounds__(kThreads, 1) apl_tc_kernel(Params p) {
-  using C = Cfg<NMAX>;
+template <int NMAX, int G>
+__global__ void __launch_bounds__(Cfg<NMAX, G>::kThreads, 1) apl_tc_kernel(Params p) {
+  using C = Cfg<NMAX, G>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ Shared sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
-  const uint32_t bar = pw::smem_u32(smem + C::kOffBar);
   if (threadIdx.x == 0) {
-    for (int i = 0; i < kAStages; ++i) {
-      pw::mbar_init(bar + 8 * i, kDeqWarps);       // A full: one arrive per dequant warp
-      pw::mbar_init(bar + 8 * (kAStages + i), 1);  // A empty: tcgen05.commit
+    for (int g = 0; g < G; ++g) {
+      const uint32_t bar = pw::smem_u32(smem + C::kOffBar + g * kBarsPerGroup * 8);
+      for (int i = 0; i < kAStages; ++i) {
+        pw::mbar_init(bar + 8 * i, kDeqWarps);       // A full: one arrive per dequant warp
+        pw::mbar_init(bar + 8 * (kAStages + i), 1);  // A empty: tcgen05.commit
+      }
+      for (int i = 0; i < C::kBStages; ++i) pw::mbar_init(bar + 8 * (2 * kAStages + i), 1);  // B empty
+      pw::mbar_init(bar + 8 * (2 * kAStages + C::kBStages), 1);                            // unit MMAs done
     }
-    for (int i = 0; i < C::kBStages; ++i) pw::mbar_init(bar + 8 * (2 * kAStages + i), 1);  // B empty
-    pw::mbar_init(bar + 8 * (2 * kAStages + C::kBStages), 1);                            // unit MMAs done
     pw::mbar_init_fence();
     sh.abort = 0;
     setup_schedule<NMAX>(p, sh);
@@ -483,21 +550,22 @@ __global__ void __launch_bounds__(kThreads, 1) apl_tc_kernel(Params p) {
     pw::tc_fence_before();
     __syncthreads();
     pw::tc_fence_after();
-    const Unit u = sh.u;
+    const Unit& u = sh.u;   // read from shared memory where used (keeps registers free)
     if (u.kind == kNone) break;
-    if (!u.skip) {
-      if (warp < kDeqWarps) {
+    const int u_skip = u.skip;
+    if (!u_skip) {
+      if (warp < kDeqWarps * G) {
         switch (u.q) {
-          case 2: dequant_role<NMAX, 2>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 3: dequant_role<NMAX, 3>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 4: dequant_role<NMAX, 4>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 5: dequant_role<NMAX, 5>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 6: dequant_role<NMAX, 6>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 7: dequant_role<NMAX, 7>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          default: dequant_role<NMAX, 8>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 2: dequant_role<NMAX, G, 2>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 3: dequant_role<NMAX, G, 3>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 4: dequant_role<NMAX, G, 4>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 5: dequant_role<NMAX, G, 5>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 6: dequant_role<NMAX, G, 6>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 7: dequant_role<NMAX, G, 7>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          default: dequant_role<NMAX, G, 8>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
         }
       } else {
-        producer_role<NMAX>(p, u, smem, tmem, a_cnt, b_cnt, abort_local);
+        producer_role<NMAX, G>(p, u, smem, tmem, a_cnt, b_cnt, abort_local);
       }
       ++unit_cnt;
     }
@@ -510,14 +578,14 @@ __global__ void __launch_bounds__(kThreads, 1) apl_tc_kernel(Params p) {
     pw::tc_fence_after();
     if (threadIdx.x == 0) {
       int combine = -1;
-      if (!u.skip && u.kind == kGateUp) {
+      if (!u_skip && u.kind == kGateUp) {
         const bool drop = (p.flags & PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL) && u.e == sh.act[0] && u.strip == 0 &&
                           u.tg == 0;
         if (!drop) {
           __threadfence();
           atomicAdd(p.ctr + 2 + u.e * p.nsplit + u.split, 1u);
         }
-      } else if (!u.skip && u.kind == kDown) {
+      } else if (!u_skip && u.kind == kDown) {
         __threadfence();
         const uint32_t prev = atomicAdd(p.ctr + 2 + p.E * p.nsplit + u.strip, 1u);
         if (prev + 1 == static_cast<uint32_t>(sh.arrivals_per_strip)) {
@@ -592,12 +660,12 @@ int sm_count_cached() {
   return count;
 }
 
-template <int NMAX>
+template <int NMAX, int G>
 int launch(const Params& p, cudaStream_t s) {
-  using C = Cfg<NMAX>;
+  using C = Cfg<NMAX, G>;
   static bool attr_done = false;
   if (!attr_done) {
-    PW_CUDA_TRY(cudaFuncSetAttribute(apl_tc_kernel<NMAX>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    PW_CUDA_TRY(cudaFuncSetAttribute(apl_tc_kernel<NMAX, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::kSmemBytes));
     attr_done = true;
   }
@@ -605,7 +673,7 @@ int launch(const Params& p, cudaStream_t s) {
   if (sms < 1) return pw::set_error(PW_ERR_CUDA, "could not query the SM count");
   // one CTA per SM (the shared-memory footprint keeps it at one), each owning
   // C::kTmemCols of the SM's 512 TMEM columns
-  apl_tc_kernel<NMAX><<<sms, kThreads, C::kSmemBytes, s>>>(p);
+  apl_tc_kernel<NMAX, G><<<sms, C::kThreads, C::kSmemBytes, s>>>(p);
   PW_CUDA_TRY(cudaGetLastError());
   return PW_OK;
 }
@@ -670,7 +738,7 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
   p.flags = o.flags;
   p.linear = 0;
   PW_CUDA_TRY(cudaMemsetAsync(p.ctr, 0, L.h - L.ctr, s));
-  return path == PW_PATH_PREFILL ? launch<256>(p, s) : launch<32>(p, s);
+  return path == PW_PATH_PREFILL ? launch<256, 1>(p, s) : launch<32, 2>(p, s);
 }
 
 int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I, int E, int k,
@@ -707,7 +775,7 @@ int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,
   p.linear = 1;
   p.nsplit = 1;
   p.split_cols = d.cols;
-  return M > 32 ? launch<256>(p, s) : launch<32>(p, s);
+  return M > 32 ? launch<256, 1>(p, s) : launch<32, 2>(p, s);
 }
 
 }  // extern "C"
