@@ -12,10 +12,9 @@
 //  * q <= 4: the LUT lives in registers as a low-byte and a high-byte table
 //    and one prmt looks up four 8-bit halves at once (q = 4 selects between
 //    two 8-entry halves with a byte mask built from the index MSB);
-//  * q >= 5: the LUT lives in shared memory, one 4-byte column per lane
-//    ("bank per lane": entry c of lane l's row at word c*32 + l), so the 32
-//    lanes of a warp never conflict; for q = 8 a word holds entries c and
-//    c+128.
+//  * q >= 5: an 8x8 bit transpose of the plane words yields byte indices;
+//    the LUT lives in a 64 KB-aligned shared region with one bank per lane,
+//    so one prmt forms each lookup address and lookups never conflict.
 #pragma once
 
 #include "tc_ptx.cuh"
@@ -23,7 +22,7 @@
 namespace pw {
 
 constexpr int kStageK = 64;                      // columns per pipeline stage
-constexpr int kLutBytesPerWarp = 128 * 128;      // shared LUT table of one warp (q >= 5)
+constexpr int kLutRegionBytes = 65536;           // shared LUT region of a strip (q >= 5), 64 KB aligned
 
 // Nibble selector of 8 consecutive columns (sub-block js) from one word per
 // plane, using planes [P0, P1) as index bits (P1-1-p) .. 0.
@@ -103,51 +102,79 @@ struct RowDequant<Q, true> {
 };
 
 // ---------------------------------------------------------------- q >= 5
+// 8x8 bit-matrix transpose of the bytes of eight words (three rounds of delta
+// swaps, all four byte lanes at once): afterwards bit c of byte j of X[i]
+// holds what was bit i of byte j of X[c].
+__device__ __forceinline__ void transpose8x8(uint32_t (&X)[8]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t t = ((X[i] >> 4) ^ X[i + 4]) & 0x0F0F0F0Fu;
+    X[i + 4] ^= t;
+    X[i] ^= t << 4;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    if (i & 2) continue;
+    const uint32_t t = ((X[i] >> 2) ^ X[i + 2]) & 0x33333333u;
+    X[i + 2] ^= t;
+    X[i] ^= t << 2;
+  }
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    const uint32_t t = ((X[i] >> 1) ^ X[i + 1]) & 0x55555555u;
+    X[i + 1] ^= t;
+    X[i] ^= t << 1;
+  }
+}
+
+// The LUTs of a 128-row strip live in one shared region aligned to 64 KB:
+// entry c of every row is the 256-byte line c of the region; within a line,
+// rows of warps 0/1 of the group use the low half-words and rows of warps 2/3
+// the high half-words of words (warp & 1) * 32 + lane.  Every lane of a warp
+// owns its own bank, so lookups never conflict, and the shared address of a
+// lookup is the region base with the index byte dropped into byte 1 -- one
+// prmt per column.
 template <int Q>
 struct RowDequant<Q, false> {
-  static constexpr int kWords = (Q == 8) ? 128 : (1 << Q);
-  uint32_t tbl;  // shared address of this lane's column
+  uint32_t tblw;  // region | this row's offset within a line
 
-  // Fill this lane's column of the warp's table from its LUT row.
-  __device__ __forceinline__ void load(const uint16_t* __restrict__ lut_row, uint32_t warp_tbl, int lane) {
-    tbl = warp_tbl + static_cast<uint32_t>(lane) * 4u;
+  __device__ __forceinline__ void set_row(uint32_t region, int wq, int lane) {
+    tblw = region | (static_cast<uint32_t>((wq & 1) * 32 + lane) * 4u + static_cast<uint32_t>(wq >> 1) * 2u);
+  }
+
+  // Write this row's LUT (2^Q fp16) into its column of the region.
+  __device__ __forceinline__ void load(const uint16_t* __restrict__ lut_row) const {
     const uint4* src = reinterpret_cast<const uint4*>(lut_row);
 #pragma unroll 4
-    for (int c8 = 0; c8 < kWords / 8; ++c8) {
+    for (int c8 = 0; c8 < (1 << Q) / 8; ++c8) {
       const uint4 a = __ldg(src + c8);
-      uint4 b = make_uint4(0u, 0u, 0u, 0u);
-      if (Q == 8) b = __ldg(src + c8 + 16);   // entries c + 128
       const uint32_t av[4] = {a.x, a.y, a.z, a.w};
-      const uint32_t bv[4] = {b.x, b.y, b.z, b.w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const int c = c8 * 8 + 2 * i;
-        const uint32_t e0 = av[i] & 0xFFFFu, e1 = av[i] >> 16;
-        const uint32_t f0 = bv[i] & 0xFFFFu, f1 = bv[i] >> 16;
-        sts_u32(tbl + static_cast<uint32_t>(c) * 128u, e0 | (f0 << 16));
-        sts_u32(tbl + static_cast<uint32_t>(c + 1) * 128u, e1 | (f1 << 16));
+        const uint32_t c = static_cast<uint32_t>(c8 * 8 + 2 * i);
+        sts_u16(tblw + c * 256u, av[i] & 0xFFFFu);
+        sts_u16(tblw + (c + 1u) * 256u, av[i] >> 16);
       }
     }
   }
 
-  __device__ __forceinline__ uint32_t look(uint32_t idx) const {
-    if (Q == 8) return lds_u16(tbl + ((idx & 127u) << 7) + ((idx >> 7) << 1));
-    return lds_u16(tbl + (idx << 7));
-  }
-
+  // ww[p]: one 32-column word of plane p -> 16 fp16 pairs (columns in order).
   __device__ __forceinline__ void word(const uint32_t (&ww)[Q], uint32_t (&out)[16]) const {
+    // row i of the bit matrix = index bit i = plane Q-1-i; missing bits are 0
+    uint32_t X[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) X[i] = i < Q ? ww[Q - 1 - i] : 0u;
+    transpose8x8(X);
+    // column 8*js + e now has its full index in byte e/2 of X[4*(e%2) + js]
 #pragma unroll
     for (int js = 0; js < 4; ++js) {
-      const uint32_t hi = nibble_sel<0, Q - 4>(ww, js);
-      const uint32_t lo = nibble_sel<Q - 4, Q>(ww, js);
-      uint32_t v[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const uint32_t idx = ((lo >> (4 * e)) & 0xFu) | (((hi >> (4 * e)) & 0xFu) << 4);
-        v[e] = look(idx);
+      for (int j = 0; j < 4; ++j) {
+        const uint32_t sel = 0x7604u | (static_cast<uint32_t>(j) << 4);
+        const uint32_t v0 = lds_u16(prmt(X[js], tblw, sel));
+        const uint32_t v1 = lds_u16(prmt(X[4 + js], tblw, sel));
+        out[4 * js + j] = prmt(v0, v1, 0x5410u);
       }
-#pragma unroll
-      for (int i = 0; i < 4; ++i) out[4 * js + i] = v[2 * i] | (v[2 * i + 1] << 16);
     }
   }
 };

@@ -64,6 +64,10 @@ enum UnitKind : int { kNone = -1, kGateUp = 0, kDown = 1, kLinear = 2 };
 // NMAX: tokens per tile.  G: dequant groups per CTA; with G = 2 both groups
 // work on the same strip (sharing its LUT) and split the unit's K range, and
 // their accumulators are summed through shared memory in the epilogue.
+//
+// Dynamic shared memory: [pre][64 KB LUT region, 64 KB aligned][post].  The
+// smaller of the two rings goes in front of the region (the gap up to the
+// next 64 KB boundary), the larger one after it.
 template <int NMAX, int G>
 struct Cfg {
   static constexpr int kThreads = G * (kDeqThreads + 32);
@@ -72,18 +76,21 @@ struct Cfg {
   static constexpr int kBStageBytes = NMAX * 128;
   static constexpr int kGroupTmemCols = (kDCol + NMAX) <= 256 ? 256 : 512;
   static constexpr int kTmemCols = G * kGroupTmemCols;
-  static constexpr int kOffB = 0;
-  static constexpr int kOffRing = kOffB + G * kBStages * kBStageBytes;
-  static constexpr int kOffLut = kOffRing + G * kRingBytes;
-  static constexpr int kOffX = kOffLut + kDeqWarps * pw::kLutBytesPerWarp;
+  static constexpr int kBRingBytes = G * kBStages * kBStageBytes;
+  static constexpr int kPlaneRingBytes = G * kRingBytes;
   static constexpr int kXBytes = G == 2 ? NMAX * kDeqThreads * 4 : 0;
-  static constexpr int kOffBar = kOffX + kXBytes;
-  static constexpr int kOffRows = kOffBar + G * kBarsPerGroup * 8;
-  static constexpr int kSmemUsed = kOffRows + G * NMAX * 4;
-  static constexpr int kSmemBytes = kSmemUsed + 1024;  // room to align the base to 1024
+  static constexpr int kBarBytes = G * kBarsPerGroup * 8;
+  static constexpr int kRowsBytes = G * NMAX * 4;
+  static constexpr bool kBInPre = kBRingBytes <= kPlaneRingBytes;
+  static constexpr int kPreRing = kBInPre ? kBRingBytes : kPlaneRingBytes;
+  static constexpr int kPostRing = kBInPre ? kPlaneRingBytes : kBRingBytes;
+  static constexpr int kPreBytes = kPreRing + kXBytes + kBarBytes + kRowsBytes + 8192;  // + Shared
+  static constexpr int kSmemBytes = 65536 + pw::kLutRegionBytes + kPostRing;
   static_assert(kBStageBytes % 1024 == 0, "B stages must keep 1024-byte alignment");
   static_assert(kTmemCols <= 512, "TMEM has 512 columns");
   static_assert(2 * kAStages + kBStages + 1 <= kBarsPerGroup, "barrier slots");
+  static_assert(kPreBytes <= 65536 - 4096, "front part must fit below the first 64 KB boundary");
+  static_assert(kSmemBytes <= 232448, "shared memory per CTA");
 };
 
 struct Params {
@@ -122,6 +129,16 @@ struct Shared {            // small per-CTA state (static shared memory)
   int cum_dn[kMaxE + 1];
   int arrivals_per_strip;
   int abort;
+};
+
+// Shared-memory carve-up of one CTA (computed at kernel start).
+struct Smem {
+  uint8_t* b_ring;       // G x kBStages x kBStageBytes, 1024-aligned
+  uint8_t* plane_ring;   // G x kRingBytes
+  float* xch;            // group-1 partial sums [token][pos]
+  uint32_t bar;          // G x kBarsPerGroup mbarriers (shared address)
+  int* rows;             // G x NMAX B-row offsets
+  uint32_t lut_region;   // 64 KB-aligned LUT region (shared address)
 };
 
 __device__ __forceinline__ void report(int32_t* status, int code) {
@@ -284,26 +301,28 @@ __device__ __forceinline__ void lds_v4(uint32_t addr, uint32_t (&v)[4]) {
 }
 
 template <int NMAX, int G, int Q>
-__device__ __noinline__ void dequant_role(const Params& p, const Unit& u, uint8_t* smem, uint32_t tmem, uint32_t& a_cnt,
-                             uint32_t unit_cnt, int& abort) {
+__device__ __noinline__ void dequant_role(const Params& p, const Unit& u, const Smem& sm, uint32_t tmem,
+                                          uint32_t& a_cnt, uint32_t unit_cnt, int& abort) {
   using C = Cfg<NMAX, G>;
   constexpr int kTileStrideW = pw::kTileBytes / 4;
   constexpr int kSlotBytes = Q * pw::kTileBytes;      // one tile of every plane, all 128 rows
   constexpr int D = (kRingBytes / kSlotBytes) > 4 ? 4 : (kRingBytes / kSlotBytes);
   static_assert(D >= 2, "ring too small");
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = warp >> 2;
-  const int pos = (warp & 3) * 32 + lane;
+  const int g = warp >> 2, wq = warp & 3;
+  const int pos = wq * 32 + lane;
   const BlockDesc& d = *u.d;
   const int row = strip_pos_row(u.strip, pos, d.rows / 2);
-  const uint32_t lut_warp = pw::smem_u32(smem + C::kOffLut + (warp & 3) * pw::kLutBytesPerWarp);
   pw::RowDequant<Q> dq;
   if constexpr (Q <= 4) {
-    dq.load(d.lut + static_cast<long long>(row) * (1 << Q), lut_warp, lane);
+    dq.load(d.lut + static_cast<long long>(row) * (1 << Q), 0u, lane);
   } else {
-    if (g == 0) dq.load(d.lut + static_cast<long long>(row) * (1 << Q), lut_warp, lane);
-    dq.tbl = lut_warp + static_cast<uint32_t>(lane) * 4u;
-    dequant_bar_sync(G);   // group 0 filled the shared table both groups read
+    dq.set_row(sm.lut_region, wq, lane);
+    if (g == 0) dq.load(d.lut + static_cast<long long>(row) * (1 << Q));
+    if (G == 2)
+      dequant_bar_sync(G);   // group 0 filled the table both groups read
+    else
+      __syncwarp();
   }
 
   // this group's share of the unit's tiles
@@ -318,7 +337,7 @@ __device__ __noinline__ void dequant_role(const Params& p, const Unit& u, uint8_
 #pragma unroll
   for (int q = 0; q < Q; ++q)
     src[q] = d.planes[q] + (static_cast<long long>(u.strip) * tiles + tile0) * kTileStrideW + pos * 4;
-  const uint32_t ring = pw::smem_u32(smem + C::kOffRing + g * kRingBytes) + pos * 16;
+  const uint32_t ring = pw::smem_u32(sm.plane_ring + g * kRingBytes) + pos * 16;
   auto issue = [&](int t) {
     if (t < ntiles) {
       const uint32_t slot = ring + (t % D) * kSlotBytes;
@@ -331,8 +350,8 @@ __device__ __noinline__ void dequant_role(const Params& p, const Unit& u, uint8_
 #pragma unroll
   for (int i = 0; i < D - 1; ++i) issue(i);
 
-  const uint32_t bar = pw::smem_u32(smem + C::kOffBar + g * kBarsPerGroup * 8);
-  const uint32_t tl = tmem + g * C::kGroupTmemCols + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+  const uint32_t bar = sm.bar + g * kBarsPerGroup * 8;
+  const uint32_t tl = tmem + g * C::kGroupTmemCols + (static_cast<uint32_t>(32 * wq) << 16);
   for (int t = 0; t < ntiles; ++t) {
     issue(t + D - 1);
     pw::cp_async_wait<D - 1>();
@@ -366,7 +385,7 @@ __device__ __noinline__ void dequant_role(const Params& p, const Unit& u, uint8_
   // epilogue: accumulator row `pos` (TMEM lane), columns = tokens
   if (!abort && !pw::mbar_wait(bar + 8 * (2 * kAStages + C::kBStages), unit_cnt & 1u, p.wait_ns)) abort = 1;
   pw::tc_fence_after();
-  float* xch = reinterpret_cast<float*>(smem + C::kOffX);
+  float* xch = sm.xch;
   if (G == 2 && g == 1) {
     // hand this group's partial sums to group 0 ([token][pos] layout)
     for (int c = 0; c < u.npad / 16; ++c) {
@@ -395,7 +414,7 @@ __device__ __noinline__ void dequant_role(const Params& p, const Unit& u, uint8_
       if (u.kind == kGateUp) {
         const float up = __shfl_down_sync(0xffffffffu, val, 16);
         if (lane < 16 && n < u.nrows) {
-          const int m = u.strip * 64 + 16 * (warp & 3) + lane;
+          const int m = u.strip * 64 + 16 * wq + lane;
           p.h[static_cast<long long>(u.off + n) * p.I + m] = __half_as_ushort(__float2half_rn(silu(val) * up));
         }
       } else if (u.kind == kDown) {
@@ -412,12 +431,12 @@ __device__ __noinline__ void dequant_role(const Params& p, const Unit& u, uint8_
 // Producer / MMA warp of group g (warp 4G + g)
 // ---------------------------------------------------------------------------
 template <int NMAX, int G>
-__device__ void producer_role(const Params& p, const Unit& u, uint8_t* smem, uint32_t tmem, uint32_t& a_cnt,
+__device__ void producer_role(const Params& p, const Unit& u, const Smem& sm, uint32_t tmem, uint32_t& a_cnt,
                               uint32_t& b_cnt, int& abort) {
   using C = Cfg<NMAX, G>;
   const int lane = threadIdx.x & 31;
   const int g = (threadIdx.x >> 5) - 4 * G;
-  int* rows = reinterpret_cast<int*>(smem + C::kOffRows) + g * NMAX;
+  int* rows = sm.rows + g * NMAX;
   const uint16_t* bbase = u.kind == kDown ? p.h : p.x;
   for (int n = lane; n < u.npad; n += 32) {
     const int nn = min(n, u.nrows - 1);
@@ -437,8 +456,8 @@ __device__ void producer_role(const Params& p, const Unit& u, uint8_t* smem, uin
   const int sb = 2 * ((G == 2 && g == 1) ? half : 0);
   const int se = 2 * ((G == 2 && g == 0) ? half : ntiles_all);
   const int nst = se - sb;
-  const uint32_t bring = pw::smem_u32(smem + C::kOffB + g * C::kBStages * C::kBStageBytes);
-  const uint32_t bar = pw::smem_u32(smem + C::kOffBar + g * kBarsPerGroup * 8);
+  const uint32_t bring = pw::smem_u32(sm.b_ring + g * C::kBStages * C::kBStageBytes);
+  const uint32_t bar = sm.bar + g * kBarsPerGroup * 8;
   const uint32_t bar_b_empty = bar + 8 * (2 * kAStages);
   const uint32_t bar_done = bar + 8 * (2 * kAStages + C::kBStages);
   const uint32_t tg = tmem + g * C::kGroupTmemCols;
@@ -516,13 +535,41 @@ __device__ void combine_strip(const Params& p, int strip) {
 template <int NMAX, int G>
 __global__ void __launch_bounds__(Cfg<NMAX, G>::kThreads, 1) apl_tc_kernel(Params p) {
   using C = Cfg<NMAX, G>;
-  extern __shared__ uint8_t smem_raw[];
-  __shared__ Shared sh;
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // carve up dynamic shared memory around a 64 KB-aligned LUT region
+  const uint32_t base = pw::smem_u32(smem_raw);
+  const uint32_t pre = (base + 1023u) & ~1023u;
+  const uint32_t region = (pre + static_cast<uint32_t>(C::kPreBytes) + 0xFFFFu) & ~0xFFFFu;
+  const uint32_t post = region + static_cast<uint32_t>(pw::kLutRegionBytes);
+  if (post + static_cast<uint32_t>(C::kPostRing) > base + static_cast<uint32_t>(C::kSmemBytes)) {
+    if (threadIdx.x == 0) report(p.status, PW_ERR_UNSUPPORTED);   // unexpected shared-window base
+    return;
+  }
+  auto at = [&](uint32_t addr) { return smem_raw + (addr - base); };
+  Smem sm;
+  uint32_t cur = pre;
+  uint8_t* pre_ring = at(cur);
+  cur += C::kPreRing;
+  sm.xch = reinterpret_cast<float*>(at(cur));
+  cur += C::kXBytes;
+  sm.bar = cur;
+  cur += C::kBarBytes;
+  sm.rows = reinterpret_cast<int*>(at(cur));
+  cur += C::kRowsBytes;
+  Shared& sh = *reinterpret_cast<Shared*>(at((cur + 15u) & ~15u));
+  sm.lut_region = region;
+  if (C::kBInPre) {
+    sm.b_ring = pre_ring;
+    sm.plane_ring = at(post);
+  } else {
+    sm.plane_ring = pre_ring;
+    sm.b_ring = at(post);
+  }
+
   const int warp = threadIdx.x >> 5;
   if (threadIdx.x == 0) {
     for (int g = 0; g < G; ++g) {
-      const uint32_t bar = pw::smem_u32(smem + C::kOffBar + g * kBarsPerGroup * 8);
+      const uint32_t bar = sm.bar + g * kBarsPerGroup * 8;
       for (int i = 0; i < kAStages; ++i) {
         pw::mbar_init(bar + 8 * i, kDeqWarps);       // A full: one arrive per dequant warp
         pw::mbar_init(bar + 8 * (kAStages + i), 1);  // A empty: tcgen05.commit
@@ -556,16 +603,16 @@ __global__ void __launch_bounds__(Cfg<NMAX, G>::kThreads, 1) apl_tc_kernel(Param
     if (!u_skip) {
       if (warp < kDeqWarps * G) {
         switch (u.q) {
-          case 2: dequant_role<NMAX, G, 2>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 3: dequant_role<NMAX, G, 3>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 4: dequant_role<NMAX, G, 4>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 5: dequant_role<NMAX, G, 5>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 6: dequant_role<NMAX, G, 6>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          case 7: dequant_role<NMAX, G, 7>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
-          default: dequant_role<NMAX, G, 8>(p, u, smem, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 2: dequant_role<NMAX, G, 2>(p, u, sm, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 3: dequant_role<NMAX, G, 3>(p, u, sm, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 4: dequant_role<NMAX, G, 4>(p, u, sm, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 5: dequant_role<NMAX, G, 5>(p, u, sm, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 6: dequant_role<NMAX, G, 6>(p, u, sm, tmem, a_cnt, unit_cnt, abort_local); break;
+          case 7: dequant_role<NMAX, G, 7>(p, u, sm, tmem, a_cnt, unit_cnt, abort_local); break;
+          default: dequant_role<NMAX, G, 8>(p, u, sm, tmem, a_cnt, unit_cnt, abort_local); break;
         }
       } else {
-        producer_role<NMAX, G>(p, u, smem, tmem, a_cnt, b_cnt, abort_local);
+        producer_role<NMAX, G>(p, u, sm, tmem, a_cnt, b_cnt, abort_local);
       }
       ++unit_cnt;
     }
