@@ -1,0 +1,89 @@
+"""The 32-layer decode stack workload: a seeded commit schedule over the page
+table, run at step boundaries.
+
+"PagedWeight" arXiv text: the weight page table records the committed
+bitwidth q_i of every per-expert linear-block (§3, §3.1); lowering a block
+releases M_i^b - M_i^b' bytes (Eq. 3); routing mass (Eq. 1) measures how much
+traffic an expert receives, and hot experts are protected (§3.2); commits
+happen only at safe boundaries (§3.3).  The paper's planner (Algorithm 1,
+Eqs. 4-8) is not built here.  This module is the plain, seeded stand-in that
+drives the page table for the stack workload:
+
+  every ``commit_every`` steps (step 8j, j = 1..7) the byte target is
+  (1 - 0.6 * j / 7) * F8, F8 = sum_i M_i^8; the block with the lowest
+  accumulated routing mass among those with q > seed (ties by layer, expert,
+  then down before gate_up) is lowered by one bit, repeatedly, until
+  sum_i M_i^{q_i} <= target or no block can be lowered.
+
+The function is pure host logic over plain numbers, so it is tested on the CPU;
+the GPU supplies the routing-mass numerators (pw_moe_route_topk) and the page
+table executes the commits.
+"""
+from __future__ import annotations
+
+from typing import Callable, Dict, List, Sequence, Tuple
+
+GATE_UP, DOWN = 0, 1
+
+
+def byte_target(step: int, commit_every: int, n_commits: int, f8: int, final_fraction: float = 0.4) -> int:
+    """Target bytes after the commit at ``step`` (a multiple of commit_every)."""
+    j = step // commit_every
+    j = max(0, min(j, n_commits))
+    return int((1.0 - (1.0 - final_fraction) * j / n_commits) * f8)
+
+
+def plan_lowering(bits: Dict[Tuple[int, int, int], int], mass: Dict[Tuple[int, int], float],
+                  block_bytes: Callable[[Tuple[int, int, int], int], int], seed_bits: int, target: int
+                  ) -> List[Tuple[Tuple[int, int, int], int, int]]:
+    """Greedy lowering.  ``bits`` maps (layer, expert, u) -> committed q;
+    ``mass`` maps (layer, expert) -> accumulated routing mass; ``block_bytes``
+    gives M_i^b.  Returns the list of (block, q_old, q_new) steps, one bit at
+    a time, in order.  ``bits`` is not modified."""
+    q = dict(bits)
+    total = sum(block_bytes(b, qb) for b, qb in q.items())
+    steps: List[Tuple[Tuple[int, int, int], int, int]] = []
+
+    def key(b):
+        layer, expert, u = b
+        return (mass.get((layer, expert), 0.0), layer, expert, 0 if u == DOWN else 1)
+
+    order = sorted(q, key=key)
+    for b in order:
+        while total > target and q[b] > seed_bits:
+            old = q[b]
+            total -= block_bytes(b, old) - block_bytes(b, old - 1)
+            q[b] = old - 1
+            steps.append((b, old, old - 1))
+        if total <= target:
+            break
+    return steps
+
+
+class StackSchedule:
+    """Drives one APLMoEStack through the stack workload's commits."""
+
+    def __init__(self, layers: int, experts: int, seed_bits: int, parent_bits: int,
+                 block_bytes: Callable[[Tuple[int, int, int], int], int], commit_every: int = 8,
+                 n_commits: int = 7, final_fraction: float = 0.4):
+        self.L, self.E, self.S, self.P = layers, experts, seed_bits, parent_bits
+        self.block_bytes = block_bytes
+        self.commit_every, self.n_commits, self.final_fraction = commit_every, n_commits, final_fraction
+        self.bits = {(l, e, u): parent_bits for l in range(layers) for e in range(experts) for u in (GATE_UP, DOWN)}
+        self.f8 = sum(block_bytes(b, parent_bits) for b in self.bits)
+
+    def resident_bytes(self) -> int:
+        return sum(self.block_bytes(b, q) for b, q in self.bits.items())
+
+    def at_boundary(self, step: int, mass_numerators: Sequence[Sequence[float]]
+                    ) -> List[Tuple[Tuple[int, int, int], int, int]]:
+        """Called after ``step`` steps.  Returns the lowering steps to commit
+        now (empty between commit points) and updates the planned bits."""
+        if step == 0 or step % self.commit_every or step // self.commit_every > self.n_commits:
+            return []
+        mass = {(l, e): float(mass_numerators[l][e]) for l in range(self.L) for e in range(self.E)}
+        target = byte_target(step, self.commit_every, self.n_commits, self.f8, self.final_fraction)
+        plan = plan_lowering(self.bits, mass, self.block_bytes, self.S, target)
+        for b, _, new in plan:
+            self.bits[b] = new
+        return plan
