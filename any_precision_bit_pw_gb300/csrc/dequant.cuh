@@ -142,16 +142,21 @@ struct RowDequant<Q, false> {
     tblw = region | (static_cast<uint32_t>((wq & 1) * 32 + lane) * 4u + static_cast<uint32_t>(wq >> 1) * 2u);
   }
 
-  // Write this row's LUT (2^Q fp16) into its column of the region.
-  __device__ __forceinline__ void load(const uint16_t* __restrict__ lut_row) const {
-    const uint4* src = reinterpret_cast<const uint4*>(lut_row);
-#pragma unroll 4
-    for (int c8 = 0; c8 < (1 << Q) / 8; ++c8) {
-      const uint4 a = __ldg(src + c8);
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w};
+  // Write part `part` of `nparts` of this row's LUT (2^Q fp16) into its
+  // column of the region; all loads of the part are issued before any store.
+  template <int kParts = 1>
+  __device__ __forceinline__ void load(const uint16_t* __restrict__ lut_row, int part = 0) const {
+    constexpr int kVec = (1 << Q) / 8 / kParts;    // uint4 (8 entries) per part
+    const uint4* src = reinterpret_cast<const uint4*>(lut_row) + part * kVec;
+    uint4 a[kVec];
+#pragma unroll
+    for (int c8 = 0; c8 < kVec; ++c8) a[c8] = __ldg(src + c8);
+#pragma unroll
+    for (int c8 = 0; c8 < kVec; ++c8) {
+      const uint32_t av[4] = {a[c8].x, a[c8].y, a[c8].z, a[c8].w};
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
-        const uint32_t c = static_cast<uint32_t>(c8 * 8 + 2 * i);
+        const uint32_t c = static_cast<uint32_t>((part * kVec + c8) * 8 + 2 * i);
         sts_u16(tblw + c * 256u, av[i] & 0xFFFFu);
         sts_u16(tblw + (c + 1u) * 256u, av[i] >> 16);
       }
