@@ -285,9 +285,9 @@ inline int sm_count_cached() {
 // ---------------------------------------------------------------------------
 // Combine (whole CTA): y rows of one strip for every token, fixed order.
 // ---------------------------------------------------------------------------
-__device__ inline void combine_strip(const Params& p, int strip) {
+__device__ inline void combine_strip(const Params& p, int strip, int tid, int nthreads) {
   const int n_items = p.T * 128;
-  for (int it = threadIdx.x; it < n_items; it += blockDim.x) {
+  for (int it = tid; it < n_items; it += nthreads) {
     const int t = it >> 7, pos = it & 127;
     const int row = (pos >> 6) * (p.H / 2) + strip * 64 + (pos & 63);
     float acc = 0.f;

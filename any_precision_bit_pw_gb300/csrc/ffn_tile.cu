@@ -363,7 +363,7 @@ __global__ void __launch_bounds__(Cfg<NMAX, G>::kThreads, 1) apl_tc_kernel(Param
     pw::tc_fence_after();
     if (threadIdx.x == 0) sh.u.combine = finish_unit(p, sh, u, u_skip);
     __syncthreads();
-    if (sh.u.combine >= 0) combine_strip(p, sh.u.combine);
+    if (sh.u.combine >= 0) combine_strip(p, sh.u.combine, threadIdx.x, blockDim.x);
   }
   pw::tc_fence_before();
   __syncthreads();
