@@ -94,6 +94,10 @@ class APLMoEStack:
                 self.luts[block].pop(b, None)
         return before - self.resident_bytes_of(block)
 
+    def block_bytes_at(self, block: int, q: int) -> int:
+        """M_i^q of Eq. 3 for a block (page-table arithmetic)."""
+        return pw.pw_page_table_bytes(self.table, block, q)
+
     def resident_bytes_of(self, block: int) -> int:
         q, _, _ = pw.pw_page_table_get(self.table, block)
         return pw.pw_page_table_bytes(self.table, block, q) if q > 0 else 0

@@ -87,3 +87,69 @@ class StackSchedule:
         for b, _, new in plan:
             self.bits[b] = new
         return plan
+
+
+# ---------------------------------------------------------------------------
+# GPU driver of the stack workload (torch plumbing around the libpw calls)
+# ---------------------------------------------------------------------------
+class StackRun:
+    """L independent MoE layers on one GPU, stepped with fresh seeded inputs;
+    every ``commit_every`` steps the schedule lowers blocks and the released
+    plane/LUT tensors are dropped (their memory returns to the caching
+    allocator for later allocations on the stream)."""
+
+    def __init__(self, wl, device, layers=None, commit_every: int = 8, n_commits: int = 7,
+                 final_fraction: float = 0.4):
+        from . import synth
+        from .layer import APLMoEStack, MoECall, load_layer
+        import torch
+        self.torch, self.synth = torch, synth
+        self.wl = wl
+        self.L = wl.layers if layers is None else layers
+        sh = wl.shape
+        self.stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, self.L, wl.parent_bits,
+                                 wl.seed_bits, device)
+        for layer in range(self.L):
+            li = synth.layer_inputs(wl, layer=layer, device=device)
+            load_layer(self.stack, layer, li)
+            del li
+        self.stack.sync()
+        self.call = MoECall(self.stack, wl.tokens)
+
+        def block_bytes(b, q):
+            return self.stack.block_bytes_at(self.stack.block_id(*b), q)
+        self.schedule = StackSchedule(self.L, sh.experts, wl.seed_bits, wl.parent_bits, block_bytes,
+                                      commit_every, n_commits, final_fraction)
+        self.step_no = 0
+
+    def inputs(self, layer: int, step: int):
+        dev = self.stack.device
+        return (self.synth.activations(self.wl, layer, step, dev),
+                self.synth.router_logits(self.wl, layer, step, dev))
+
+    def step(self, xs=None, logits=None, on_layer=None):
+        """One step: every layer routes and runs its fused expert layer, then
+        the step boundary commits any lowering due.  ``on_layer(layer, y)`` is
+        called after each layer's call is enqueued (``y`` is reused by the next
+        layer)."""
+        for layer in range(self.L):
+            x, lg = (xs[layer], logits[layer]) if xs is not None else self.inputs(layer, self.step_no)
+            y = self.call(layer, x, lg)
+            if on_layer is not None:
+                on_layer(layer, y)
+        self.step_no += 1
+        return self.boundary()
+
+    def boundary(self):
+        """Commit the schedule's lowering at a step boundary; returns the
+        (block, q_old, q_new) steps committed and the bytes released."""
+        if self.step_no % self.schedule.commit_every:
+            return [], 0
+        mass = self.call.mass.float().cpu().tolist()    # routing-mass numerators (Eq. 1)
+        plan = self.schedule.at_boundary(self.step_no, mass)
+        released = 0
+        for (layer, e, u), _, new in plan:
+            released += self.stack.commit(self.stack.block_id(layer, e, u), new)
+        if plan:
+            self.stack.sync()
+        return plan, released

@@ -53,6 +53,26 @@ def _peaks():
         return 6800.0, "fallback"
 
 
+def _tensor_peak():
+    """Dense fp16 tensor peak in TFLOP/s: the measured bf16 cuBLAS figure
+    (fp16 and bf16 share the nominal rate), sustained (the kernel is timed
+    inside a long loop)."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured sustained bf16 cuBLAS (fp16 same nominal rate)"
+    except Exception:
+        return 1700.0, "fallback sustained"
+
+
+def algorithmic_flops(wl, offsets):
+    """2 * A * (2I*H + H*I): the gate_up and down contractions of every assignment."""
+    sh = wl.shape
+    A = int(offsets[-1])
+    return 2.0 * A * (2 * sh.intermediate * sh.hidden + sh.hidden * sh.intermediate)
+
+
 # ---------------------------------------------------------------------------
 # clocks during the timed region
 # ---------------------------------------------------------------------------
@@ -117,6 +137,21 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # the GPU arm
 # ---------------------------------------------------------------------------
+def max_over_ranks(ms: float, world: int, device) -> float:
+    """The slowest replica's time: every rank contributes its own timed-region
+    milliseconds and all get the maximum (the job finishes with its slowest
+    replica)."""
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    if world > 1:
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(tokens_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """Whole-job tokens/s: the tokens of all replicas over the slowest one's time."""
+    return tokens_per_step * steps * world / (max_ms * 1e-3)
+
+
 def algorithmic_bytes(wl, bits, offsets):
     """Bytes one fused-layer launch must move: the committed planes and LUT_q
     of every block of every active expert, x, y and the h write + read."""
@@ -156,10 +191,12 @@ def gpu_arm(args, rank, world, local_rank):
 
     # routing of each batch (for the algorithmic byte count)
     bytes_per_batch = []
+    offsets_per_batch = []
     for s in range(n_batches):
         call(0, xs[s], lgs[s])
         torch.cuda.synchronize()
         off = call.route.offsets.cpu().numpy()
+        offsets_per_batch.append(off)
         bytes_per_batch.append(algorithmic_bytes(wl, li.bits, off))
     assert int(call.status.item()) == 0, "device status after warm-up calls"
 
@@ -219,19 +256,28 @@ def gpu_arm(args, rank, world, local_rank):
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / K2
 
-    # max over ranks
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     mean_bytes = float(np.mean([b[0] for b in bytes_per_batch]))
     mean_planes = float(np.mean([b[1] for b in bytes_per_batch]))
     ffn_avg_ms = float(np.mean(ffn_ms))
     achieved = mean_bytes / (ffn_avg_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
+    hbm_roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "apl_decode_kernel / apl_tc_kernel (pw_moe_apl_ffn)",
+                "algorithmic_bytes_per_launch": mean_bytes, "plane_bytes_per_launch": mean_planes,
+                "launch_ms": ffn_avg_ms, "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"}
+    prefill = wl.tokens * sh.top_k >= 48 * sh.experts
+    roofline = hbm_roof
+    if prefill:
+        flops = float(np.mean([algorithmic_flops(wl, o) for o in offsets_per_batch]))
+        tpk, tkind = _tensor_peak()
+        ach_t = flops / (ffn_avg_ms * 1e-3) / 1e12
+        roofline = {"bound": "tensor", "achieved": ach_t, "peak": tpk, "unit": "TFLOP/s", "frac": ach_t / tpk,
+                    "traffic": None, "kernel": "apl_tc_kernel (pw_moe_apl_ffn, 256-token tiles)",
+                    "algorithmic_flops_per_launch": flops, "launch_ms": ffn_avg_ms, "peak_kind": tkind}
     clocks = clk.summary()
-    value = wl.tokens * K * world / (total_ms * 1e-3)
+    value = job_throughput(wl.tokens, K, world, total_ms)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -240,11 +286,8 @@ def gpu_arm(args, rank, world, local_rank):
                    "top_k": sh.top_k, "tokens": T, "parent_bits": wl.parent_bits, "seed_bits": wl.seed_bits,
                    "committed_bits": li.bits, "parallelism": f"replicas x{world}",
                    "l2": "no flush: the planes read per step (%.0f MB) exceed the 129 MB L2" % (mean_planes / 1e6)},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
-                     "kernel": "ffn_decode_kernel (pw_moe_apl_ffn)",
-                     "algorithmic_bytes_per_launch": mean_bytes, "plane_bytes_per_launch": mean_planes,
-                     "launch_ms": ffn_avg_ms, "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"},
+        "roofline": roofline,
+        "roofline_hbm": hbm_roof if prefill else None,
         "e2e": {"value": wl.tokens / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2},
         "gpu_launches": 2 * K,
@@ -252,6 +295,131 @@ def gpu_arm(args, rank, world, local_rank):
         "status": status,
     }
     return line
+
+
+def stack_arm(args, rank, world, local_rank):
+    """The 32-layer decode stack: every step runs routing + the fused layer
+    for each of the L layers on fresh seeded inputs; every 8 steps the step
+    boundary reads the accumulated routing mass, lowers blocks to the byte
+    target and releases their pages (all inside the timed region)."""
+    from any_precision_bit_pw_gb300 import pw
+    from any_precision_bit_pw_gb300.stack import StackRun
+
+    dev = torch.device(f"cuda:{local_rank}")
+    torch.cuda.set_device(dev)
+    pw.lib()
+    wl = synth.WORKLOADS[args.workload]
+    sh = wl.shape
+    T, H, E, L = wl.tokens, sh.hidden, sh.experts, wl.layers
+    run = StackRun(wl, dev, commit_every=synth.STACK_COMMIT_EVERY,
+                   n_commits=synth.STACK_STEPS // synth.STACK_COMMIT_EVERY - 1)
+    f8 = run.schedule.f8
+    K = args.steps
+    n_in = min(K, 16)
+    xs = [[synth.activations(wl, l, s, dev) for l in range(L)] for s in range(n_in)]
+    lgs = [[synth.router_logits(wl, l, s, dev) for l in range(L)] for s in range(n_in)]
+    call, stack = run.call, run.stack
+    stream = torch.cuda.current_stream()
+
+    # warm-up: the layer calls without step boundaries (no commits, no mass)
+    for i in range(args.warmup):
+        for l in range(L):
+            call(l, xs[i % n_in][l], lgs[i % n_in][l], accumulate_mass=False)
+    torch.cuda.synchronize()
+    call.mass.zero_()
+
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+          for _ in range(K)]
+    bits_at = []            # committed bits of every block during each step
+    resident = []
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    released_total = 0
+    commits = 0
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    smi_index = vis.split(",")[local_rank] if vis and len(vis.split(",")) > local_rank else str(local_rank)
+    r = call.route
+    with ClockSampler(smi_index) as clk:
+        start.record(stream)
+        for i in range(K):
+            bits_at.append([stack.committed_bits(b) for b in range(stack.n_blocks)])
+            resident.append(stack.resident_bytes())
+            s = i % n_in
+            for l in range(L):
+                pw.pw_moe_route_topk(lgs[s][l], sh.top_k, r.ids, r.w, r.offsets, r.perm, r.inv_perm, call.mass[l])
+                ev[i][l][0].record(stream)
+                pw.pw_moe_apl_ffn(stack.desc, l, xs[s][l], sh.intermediate, E, sh.top_k, r.ids, r.w, r.offsets,
+                                  r.perm, r.inv_perm, call.ws, call.y, call.status)
+                ev[i][l][1].record(stream)
+            run.step_no += 1
+            plan, released = run.boundary()
+            released_total += released
+            commits += bool(plan)
+        stop.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = start.elapsed_time(stop)
+    ffn_ms = np.array([[ev[i][l][0].elapsed_time(ev[i][l][1]) for l in range(L)] for i in range(K)])
+    status = int(call.status.item())
+
+    # algorithmic bytes of each launch: replay the routing (deterministic) untimed
+    nbytes = np.zeros((K, L))
+    for i in range(K):
+        for l in range(L):
+            pw.pw_moe_route_topk(lgs[i % n_in][l], sh.top_k, r.ids, r.w, r.offsets, r.perm, r.inv_perm, None)
+            off = r.offsets.cpu().numpy()
+            bl = bits_at[i][2 * E * l: 2 * E * (l + 1)]
+            nbytes[i, l] = algorithmic_bytes(wl, bl, off)[0]
+
+    # end to end: per step, every layer's x and logits from pinned host
+    # memory and every layer's y back to it
+    K2 = max(1, min(K, 8))
+    hx = [[xs[s][l].cpu().pin_memory() for l in range(L)] for s in range(min(n_in, 2))]
+    hl = [[lgs[s][l].cpu().pin_memory() for l in range(L)] for s in range(min(n_in, 2))]
+    hy = torch.empty((L, T, H), dtype=torch.float16).pin_memory()
+    dx, dl = torch.empty_like(xs[0][0]), torch.empty_like(lgs[0][0])
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(K2):
+        s = i % len(hx)
+        for l in range(L):
+            dx.copy_(hx[s][l], non_blocking=True)
+            dl.copy_(hl[s][l], non_blocking=True)
+            hy[l].copy_(call(l, dx, dl, accumulate_mass=False), non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / K2
+
+    total_ms = max_over_ranks(total_ms, world, dev)
+    peak, peak_kind = _peaks()
+    achieved = float(nbytes.sum() / (ffn_ms.sum() * 1e-3) / 1e9)
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                "traffic": None, "kernel": "apl_decode_kernel (pw_moe_apl_ffn)",
+                "algorithmic_bytes_per_launch": float(nbytes.mean()), "launch_ms": float(ffn_ms.mean()),
+                "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"}
+    value = job_throughput(T, K, world, total_ms)
+    return {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic (seeded; bit-plane indices uniform, LUTs sorted N(0,0.02), x N(0,1), "
+                                "router logits N(0,1) + per-expert N(0,1) bias)",
+        "config": {"workload": wl.name, "layers": L, "hidden": H, "intermediate": sh.intermediate, "experts": E,
+                   "top_k": sh.top_k, "tokens": T, "parent_bits": wl.parent_bits, "seed_bits": wl.seed_bits,
+                   "commit_every": synth.STACK_COMMIT_EVERY, "commits_in_timed_region": commits,
+                   "released_bytes": released_total, "resident_bytes_first_last": [resident[0], resident[-1]],
+                   "f8_bytes": f8, "parallelism": f"replicas x{world}",
+                   "l2": "no flush: the planes read per step (%.1f GB) exceed the 129 MB L2" % (nbytes.sum() / K / 1e9)},
+        "roofline": roofline,
+        "e2e": {"value": T / (e2e_ms * 1e-3), "unit": UNIT,
+                "h2d_bytes_per_step": L * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": L * T * H * 2},
+        "gpu_launches": 2 * L * K,
+        "clocks": clk.summary(),
+        "status": status,
+    }
 
 
 def sweep(args, dev, out_path):
@@ -333,11 +501,12 @@ def oracle_sample(workload: str, experts_in_sample: int = 1) -> dict:
     ids_s = np.where(mask, ids, -1)
     apl.moe_layer(x, ids_s, r["w"], sh.intermediate, lambda e, u: blocks[(e, u)], tokens=toks)
     dt = time.perf_counter() - t0
-    est_layer_s = dt * len(active) / len(sample)
+    est_layer_s = dt * len(active) / len(sample) * wl.layers
     return {"sample_s": dt, "est_layer_s": est_layer_s, "tokens_per_s": wl.tokens / est_layer_s,
             "sample": f"oracle layer contribution of {len(sample)} of {len(active)} active experts "
                       f"({sh.intermediate * 2}x{sh.hidden} gate_up + {sh.hidden}x{sh.intermediate} down each, "
-                      f"read from packed bit-planes), scaled by {len(active)}/{len(sample)}"}
+                      f"read from packed bit-planes), scaled by {len(active)}/{len(sample)}"
+                      + (f" and by {wl.layers} layers" if wl.layers > 1 else "")}
 
 
 def cpu_baseline(workload: str) -> dict:
@@ -413,7 +582,8 @@ def main():
         cpu = cpu_baseline(args.workload)
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    line = gpu_arm(args, rank, world, local_rank)
+    arm = stack_arm if synth.WORKLOADS[args.workload].layers > 1 else gpu_arm
+    line = arm(args, rank, world, local_rank)
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if args.sweep and rank == 0:

@@ -342,3 +342,19 @@ def test_ffn_mixtral_8x7b_uniform_sweep_points(b, T):
     toks = _sample_tokens(li, 1, seed=b)
     y_ref, _ = _oracle_y(li, tokens=toks)
     _assert_close(y_ref, y, rows=toks)
+
+
+def test_ffn_mixtral_8x22b_prefill():
+    """The 8x22B-shaped prefill layer: 4096 tokens, Zipf-skewed routing, hot
+    experts at 8 bits and the rest at 3-4 bits (256-token tiles)."""
+    wl = synth.MIXTRAL_8X22B_PREFILL
+    li = synth.layer_inputs(wl, device=DEV)
+    y, status, call, _ = _run_gpu(li)
+    assert status == 0
+    r_ids = call.route.ids.cpu().numpy()
+    toks = _sample_tokens(li, 2, seed=7)
+    y_ref, r = _oracle_y(li, tokens=toks)
+    assert np.array_equal(r_ids, r["ids"])
+    assert np.array_equal(call.route.perm.cpu().numpy(), r["perm"])
+    _assert_close(y_ref, y, rows=toks)
+    assert np.all(np.isfinite(y))
