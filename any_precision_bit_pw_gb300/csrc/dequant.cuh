@@ -70,6 +70,30 @@ struct RowDequant<Q, true> {
     }
   }
 
+  // The same tables from this row's LUT in shared memory (2^Q fp16 at `saddr`).
+  __device__ __forceinline__ void load_shared(uint32_t saddr) {
+    if (Q == 2) {
+      uint32_t a, b;
+      lds_v2(saddr, a, b);
+      lo[0] = lo[1] = prmt(a, b, 0x6420u);
+      hi[0] = hi[1] = prmt(a, b, 0x7531u);
+    } else {
+      uint32_t v[4];
+      lds_v4u(saddr, v);
+      lo[0] = prmt(v[0], v[1], 0x6420u);
+      lo[1] = prmt(v[2], v[3], 0x6420u);
+      hi[0] = prmt(v[0], v[1], 0x7531u);
+      hi[1] = prmt(v[2], v[3], 0x7531u);
+      if (kT == 4) {
+        lds_v4u(saddr + 16, v);
+        lo[kT - 2] = prmt(v[0], v[1], 0x6420u);
+        lo[kT - 1] = prmt(v[2], v[3], 0x6420u);
+        hi[kT - 2] = prmt(v[0], v[1], 0x7531u);
+        hi[kT - 1] = prmt(v[2], v[3], 0x7531u);
+      }
+    }
+  }
+
   // Four columns whose indices are the nibbles of s[15:0] -> two fp16 pairs.
   __device__ __forceinline__ void quad(uint32_t s, uint32_t& p01, uint32_t& p23) const {
     uint32_t l, h;
@@ -136,10 +160,17 @@ __device__ __forceinline__ void transpose8x8(uint32_t (&X)[8]) {
 // prmt per column.
 template <int Q>
 struct RowDequant<Q, false> {
-  uint32_t tblw;  // region | this row's offset within a line
+  uint32_t tblw;      // region | this row's offset within a line
+  uint32_t hi7 = 0u;  // index bit 7 forced to 1: the table in lines 128..255 (Q < 8)
 
   __device__ __forceinline__ void set_row(uint32_t region, int wq, int lane) {
     tblw = region | (static_cast<uint32_t>((wq & 1) * 32 + lane) * 4u + static_cast<uint32_t>(wq >> 1) * 2u);
+  }
+  // Same, for a table written to half `half` of the region (Q < 8: lines
+  // 128*half + c; Q = 8 uses the whole region).
+  __device__ __forceinline__ void set_row(uint32_t region, int wq, int lane, int half) {
+    set_row(region, wq, lane);
+    hi7 = (Q < 8 && half) ? 0xFFFFFFFFu : 0u;
   }
 
   // Write part `part` of `nparts` of this row's LUT (2^Q fp16) into its
@@ -163,12 +194,39 @@ struct RowDequant<Q, false> {
     }
   }
 
+  // Copy this row's LUT from a row-major copy in shared memory (2^Q fp16 at
+  // `srow`) into its column of the region.  kSets threads share the row; the
+  // thread of set `set` writes 8-entry chunks set, set + kSets, ...  rotated by
+  // the lane so that the lanes of a warp read different bank groups.
+  template <int kSets>
+  __device__ __forceinline__ void fill(uint32_t srow, int set, int lane) const {
+    constexpr int kCh = (1 << Q) / 8;
+    static_assert(kCh % kSets == 0, "chunks per set");
+    constexpr int kPer = kCh / kSets;
+    uint32_t v[kPer][4];
+    int ch[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      ch[j] = (set + kSets * j + lane) & (kCh - 1);
+      lds_v4u(srow + ch[j] * 16, v[j]);
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c = static_cast<uint32_t>(ch[j] * 8 + 2 * i);
+        sts_u16(tblw + c * 256u, v[j][i] & 0xFFFFu);
+        sts_u16(tblw + (c + 1u) * 256u, v[j][i] >> 16);
+      }
+    }
+  }
+
   // ww[p]: one 32-column word of plane p -> 16 fp16 pairs (columns in order).
   __device__ __forceinline__ void word(const uint32_t (&ww)[Q], uint32_t (&out)[16]) const {
     // row i of the bit matrix = index bit i = plane Q-1-i; missing bits are 0
     uint32_t X[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) X[i] = i < Q ? ww[Q - 1 - i] : 0u;
+    for (int i = 0; i < 8; ++i) X[i] = i < Q ? ww[Q - 1 - i] : (i == 7 ? hi7 : 0u);
     transpose8x8(X);
     // column 8*js + e now has its full index in byte e/2 of X[4*(e%2) + js]
 #pragma unroll
@@ -183,5 +241,32 @@ struct RowDequant<Q, false> {
     }
   }
 };
+
+// Write one row's LUT (2^Q fp16 at `lut_row`, global) into its column of the
+// region: entry c at line c + 128*half (Q < 8) or line c (Q = 8).  `tblw` is
+// the row's set_row() address.  Loads go out in batches of up to 8 x 16 bytes.
+template <int Q>
+__device__ __forceinline__ void region_fill(uint32_t tblw, const uint16_t* __restrict__ lut_row, int half) {
+  constexpr int kCh = (1 << Q) / 8;
+  constexpr int kB = kCh < 8 ? kCh : 8;
+  const uint32_t base = tblw + ((Q < 8 && half) ? 128u * 256u : 0u);
+  const uint4* src = reinterpret_cast<const uint4*>(lut_row);
+#pragma unroll
+  for (int c0 = 0; c0 < kCh; c0 += kB) {
+    uint4 a[kB];
+#pragma unroll
+    for (int j = 0; j < kB; ++j) a[j] = __ldg(src + c0 + j);
+#pragma unroll
+    for (int j = 0; j < kB; ++j) {
+      const uint32_t av[4] = {a[j].x, a[j].y, a[j].z, a[j].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const uint32_t c = static_cast<uint32_t>((c0 + j) * 8 + 2 * i);
+        sts_u16(base + c * 256u, av[i] & 0xFFFFu);
+        sts_u16(base + (c + 1u) * 256u, av[i] >> 16);
+      }
+    }
+  }
+}
 
 }  // namespace pw

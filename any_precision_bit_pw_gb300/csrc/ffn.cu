@@ -19,7 +19,7 @@ using pw_ffn::kMaxE;
 size_t align256(size_t v) { return (v + 255) & ~static_cast<size_t>(255); }
 
 struct WsLayout {
-  size_t ctr, h, part, total;
+  size_t ctr, gather, h, part, xp, total;
   int nsplit, split_cols;
 };
 
@@ -37,9 +37,11 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int path) {
   L.nsplit = (I + L.split_cols - 1) / L.split_cols;
   const size_t ctr_words = 2 + static_cast<size_t>(E) * L.nsplit + static_cast<size_t>(H) / 128;
   L.ctr = 0;
-  L.h = align256(ctr_words * 4);
+  L.gather = ctr_words * 4;
+  L.h = align256(L.gather + 4);
   L.part = L.h + align256(static_cast<size_t>(A) * I * 2);
-  L.total = L.part + align256(static_cast<size_t>(L.nsplit) * A * H * 4);
+  L.xp = L.part + align256(static_cast<size_t>(L.nsplit) * A * H * 4);
+  L.total = L.xp + (path == PW_PATH_PREFILL ? 0 : align256(static_cast<size_t>(A) * H * 2));
   return L;
 }
 
@@ -84,8 +86,8 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
   if (!d_desc || !d_x || !d_w || !d_offsets || !d_perm || !d_inv_perm || !d_y || !d_status || !d_ws)
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: NULL argument");
   if ((reinterpret_cast<uintptr_t>(d_desc) & 15) || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
-      (reinterpret_cast<uintptr_t>(d_y) & 3))
-    return pw::set_error(PW_ERR_INVALID_ARG, "ffn: descriptor/x must be 16-byte aligned, y 4-byte aligned");
+      (reinterpret_cast<uintptr_t>(d_y) & 7))
+    return pw::set_error(PW_ERR_INVALID_ARG, "ffn: descriptor/x must be 16-byte aligned, y 8-byte aligned");
   pw_ffn_options o{};
   if (opts) o = *opts;
   const int path = choose_path(T, E, k, o.path);
@@ -114,6 +116,8 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
   p.ctr = reinterpret_cast<uint32_t*>(ws + L.ctr);
   p.h = reinterpret_cast<uint16_t*>(ws + L.h);
   p.part = reinterpret_cast<float*>(ws + L.part);
+  p.xp = reinterpret_cast<uint16_t*>(ws + L.xp);
+  p.gather_ctr = reinterpret_cast<uint32_t*>(ws + L.gather);
   p.status = d_status;
   p.wait_ns = (o.wait_timeout_us ? o.wait_timeout_us : 2000000u) * 1000ull;
   p.flags = o.flags;

@@ -60,7 +60,9 @@ struct Params {
   int nsplit, split_cols;
   uint16_t* h;
   float* part;
+  uint16_t* xp;            // decode path: x rows in expert order [A][H]
   uint32_t* ctr;           // [0] ticket, [1] abort, [2, 2+E*nsplit) gate_up done, then strip arrivals
+  uint32_t* gather_ctr;    // decode path: CTAs that finished their share of xp
   int32_t* status;
   uint64_t wait_ns;
   uint32_t flags;
@@ -284,22 +286,38 @@ inline int sm_count_cached() {
 
 // ---------------------------------------------------------------------------
 // Combine (whole CTA): y rows of one strip for every token, fixed order.
+// An item is one token and four consecutive rows (float4 partial sums); the
+// k x nsplit loads of an item are independent.
 // ---------------------------------------------------------------------------
 __device__ inline void combine_strip(const Params& p, int strip, int tid, int nthreads) {
-  const int n_items = p.T * 128;
+  const int n_items = p.T * 32;
   for (int it = tid; it < n_items; it += nthreads) {
-    const int t = it >> 7, pos = it & 127;
-    const int row = (pos >> 6) * (p.H / 2) + strip * 64 + (pos & 63);
-    float acc = 0.f;
+    const int t = it >> 5, r4 = (it & 31) * 4;
+    const int row = (r4 >> 6) * (p.H / 2) + strip * 64 + (r4 & 63);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     for (int j = 0; j < p.k; ++j) {
       const int slot = t * p.k + j;
       const int ps = __ldg(p.inv_perm + slot);
       const float wt = __ldg(p.w + slot);
-      float s = 0.f;
-      for (int sp = 0; sp < p.nsplit; ++sp) s += __ldcg(p.part + (static_cast<long long>(sp) * p.A + ps) * p.H + row);
-      acc += wt * s;
+      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int sp = 0; sp < p.nsplit; ++sp) {
+        const float4 v =
+            __ldcg(reinterpret_cast<const float4*>(p.part + (static_cast<long long>(sp) * p.A + ps) * p.H + row));
+        s.x += v.x;
+        s.y += v.y;
+        s.z += v.z;
+        s.w += v.w;
+      }
+      acc.x += wt * s.x;
+      acc.y += wt * s.y;
+      acc.z += wt * s.z;
+      acc.w += wt * s.w;
     }
-    p.y[static_cast<long long>(t) * p.H + row] = __half_as_ushort(__float2half_rn(acc));
+    const uint32_t lo = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.x))) |
+                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.y))) << 16);
+    const uint32_t hi = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.z))) |
+                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.w))) << 16);
+    *reinterpret_cast<uint2*>(p.y + static_cast<long long>(t) * p.H + row) = make_uint2(lo, hi);
   }
 }
 

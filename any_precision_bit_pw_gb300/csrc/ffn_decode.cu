@@ -1,357 +1,569 @@
-// Fused MoE layer kernel for decode batches: token tiles of up to 16 and one
-// 128-column tile per pipeline stage.  See ffn_common.cuh for the work units
-// and their scheduling.
+// Fused MoE layer kernel for decode batches: token tiles of up to 16, one
+// 128-row strip x 128-column tile of a block per pipeline step.  See
+// ffn_common.cuh for the work units and their scheduling.
 //
-// Each CTA (one per SM) runs two groups on the same 128-row strip of a unit,
-// splitting its K range; both share the strip's LUT.  Warp roles:
-//   warps 0-7, two groups of 4 dequant warps (thread = one row = one TMEM
-//     lane): per tile, each thread copies its 16-byte slice of every committed
-//     plane plus its share of the B operand (the tokens' x or h columns of the
-//     tile, two 16-byte chunks of a 128-byte-swizzled layout) into shared rings
-//     with cp.async, several tiles ahead; dequantises the tile's 128 columns of
-//     its row (dequant.cuh), stores them as operand A into a 3-slot TMEM ring
-//     (tcgen05.st) and arrives on the tile's "full" barrier;
-//   warps 8-9, one MMA warp per group (lane 0): per tile, waits for "full",
-//     issues the tile's 8 tcgen05.mma (A from TMEM, B from shared memory, fp32
-//     accumulator in TMEM) and one tcgen05.commit to the tile's "free" barrier,
-//     which releases the tile's A slot and B slot together;
-//   warp 10, the scheduler (lane 0): takes the next ticket, decodes it (for a
-//     down unit: waits until its h columns exist) and publishes it in one of
-//     two unit slots while the current unit runs.
-// Consecutive units overlap: when the next unit is already published as the
-// dequant warps finish a unit's tiles, they issue its first plane and B loads
-// before running the current unit's epilogue.  They never block on the next
-// unit there (that unit may be waiting for this one), so the unit order stays
-// deadlock-free.
-// The epilogue reads the accumulator rows from TMEM; group 1 hands its partial
-// sums to group 0 through shared memory.  All mbarrier waits are bounded
-// (PW_ERR_TIMEOUT); TMEM is released before the CTA exits.
+// One CTA per SM (persistent), 26 warps in six roles:
+//   warps 0-15, dequant: four sets of four warps (one warp per TMEM lane
+//     quadrant, one thread per row of the strip); tile x of the CTA's tile
+//     stream goes to set x % 4.  A thread copies its row's 16 bytes of every
+//     committed plane of its set's coming tiles into its own slots of the
+//     set's ring (cp.async; it is the only reader of those slots, so no
+//     barrier guards them), turns the row's 128 columns into fp16 through its
+//     LUT (dequant.cuh) and stores them as operand A in one of six TMEM slots;
+//   warp 16, loader: copies each tile's B operand (the 16 tokens' x or h
+//     columns: two 2-D tensor-map boxes in the 128-byte-swizzled layout the
+//     tensor core reads) into a six-slot ring, and prefetches each unit's LUT
+//     rows into L2;
+//   warp 17, MMA (one thread): per tile, eight tcgen05.mma (A from TMEM, B
+//     from the ring, fp32 accumulator in TMEM) committed to the tile's "free"
+//     barrier, which releases its TMEM slot and its B slot;
+//   warps 18-21, epilogue: write a unit's LUT (q >= 5) into a shared region
+//     one unit ahead (two halves used alternately for q <= 7), read the
+//     unit's accumulator (double-buffered in TMEM) and write h =
+//     silu(gate)*up, down-projection partial sums or the linear output; then
+//     publish the unit and run the deterministic combine of a finished strip;
+//   warp 22, scheduler (one thread): takes tickets and publishes units into
+//     four slots ahead of the other roles.
+// Gate_up B rows are the routed tokens' x rows in expert order; every CTA
+// gathers a share of them into the workspace at the start and the loader
+// waits for all shares before the first gate_up copy.
+// All waits are bounded (PW_ERR_TIMEOUT); no role waits without a time limit
+// on a barrier that a failed role could leave unfinished, every copy lands
+// before its CTA exits, and TMEM is released before the CTA exits.
+#include <cuda.h>
+
 #include "ffn_common.cuh"
 
 namespace pw_ffn {
 namespace {
 
-constexpr int kN = 16;                          // tokens per tile
-constexpr int kG = 2;                           // dequant groups (split K)
-constexpr int kDeqAll = kG * kDeqThreads;       // 256 dequant threads
-constexpr int kMmaWarp0 = kG * kDeqWarps;       // warps 8, 9
-constexpr int kSchedWarp = kMmaWarp0 + kG;      // warp 10
-constexpr int kThreads = (kSchedWarp + 1) * 32;
-constexpr int kSA = 3;                          // TMEM A slots per group (tiles)
-constexpr int kATileCols = 64;                  // TMEM columns per A tile (128 fp16 per row)
-constexpr int kDColT = kSA * kATileCols;        // accumulator columns start here
-constexpr int kGroupCols = 256;
-constexpr int kTmemColsT = kG * kGroupCols;
-constexpr int kF = 8;                           // completion barriers per group (tile index mod 8)
-constexpr int kBSlots = 6;                      // B slots per group
-constexpr int kBAtomBytes = kN * 128;           // 16 rows x 64 columns fp16, 128-byte swizzle
-constexpr int kBSlotBytes = 2 * kBAtomBytes;    // 128 columns
-constexpr int kPlaneRing = 32768;               // per group
-constexpr int kBRingBytes = kG * kBSlots * kBSlotBytes;
-constexpr int kXBytes = kN * kDeqThreads * 4;
-constexpr int kBarBytes = 512;
-constexpr int kRowsBytes = 2 * kN * 4;
-constexpr int kStateBytes = 6144;
-constexpr int kPreBytes = kBRingBytes + kBarBytes + kRowsBytes + kStateBytes;
-constexpr int kPostBytes = kG * kPlaneRing + kXBytes;
-constexpr int kSmemBytes = 65536 + pw::kLutRegionBytes + kPostBytes;
-static_assert(kDColT + kN <= kGroupCols, "TMEM columns per group");
-static_assert(kPreBytes <= 65536 - 4096, "front part must fit below the first 64 KB boundary");
-static_assert(kSmemBytes <= 232448, "shared memory per CTA");
+constexpr int kN = 16;                            // tokens per tile
+constexpr int kSets = 4;                          // dequant warp sets
+constexpr int kDeqWarpsAll = kSets * 4;           // warps 0-15
+constexpr int kMmaWarp0 = kDeqWarpsAll;           // warps 16-19: one MMA issuer per set
+constexpr int kEpiWarp0 = kMmaWarp0 + kSets;      // warps 20-23
+constexpr int kEpiThreads = 128;
+constexpr int kLoadWarp = kEpiWarp0 + 4;          // warp 24
+constexpr int kSchedWarp = kLoadWarp + 1;         // warp 25
+constexpr int kThreads = (kSchedWarp + 1) * 32;   // 832
+constexpr int kSA = 6;                            // TMEM A slots
+constexpr int kATileCols = 64;                    // TMEM columns per A tile (128 fp16 per row)
+constexpr int kDCol0 = kSA * kATileCols;          // accumulators: [buffer][set] x kN columns from here
+constexpr int kTmemCols = 512;
+constexpr int kF = 16;                            // tile barrier slots (tile index mod 16)
+constexpr int kUS = 4;                            // unit slots
+constexpr int kBS = 6;                            // B ring slots
+constexpr int kBAtom = kN * 128;                  // 16 rows x 64 fp16, 128-byte swizzle
+constexpr int kBBytes = 2 * kBAtom;               // B of one tile
+constexpr int kPSlots = 16;                       // plane ring: 2 x 8-byte slots per thread
+constexpr int kPRingBytes = kPSlots * pw::kTileBytes;   // per set
+constexpr int kSmemBytes = 232448;
+constexpr uint32_t kHintNs = 20000;
+static_assert(kDCol0 + 2 * kSets * kN <= kTmemCols, "TMEM columns");
+static_assert(kSA <= kF && 2 * kBS <= kF, "barrier reuse distances");
+static_assert(kPSlots >= 2 * PW_MAX_BITS, "two tiles of the widest bitwidth in flight");
 
-// barrier slots: per group g at 8*(20*g + i): full[kF], free[kF], done; then unit_ready[2], unit_free[2]
-__device__ __forceinline__ uint32_t bar_full(uint32_t g0, int i) { return g0 + 8 * i; }
-__device__ __forceinline__ uint32_t bar_free(uint32_t g0, int i) { return g0 + 8 * (kF + i); }
-__device__ __forceinline__ uint32_t bar_done(uint32_t g0) { return g0 + 8 * (2 * kF); }
-constexpr int kBarsPerGroupT = 20;
-static_assert(2 * kF + 1 <= kBarsPerGroupT && (kG * kBarsPerGroupT + 4) * 8 <= kBarBytes, "barrier slots");
+enum : int {
+  kBarAFull = 0,                  // [kF]  A slot written (4 warps of a set)
+  kBarTFree = kF,                 // [kF]  tile's MMAs done (tcgen05.commit)
+  kBarBFull = 2 * kF,             // [kBS] B slot loaded (transaction bytes)
+  kBarDone = 2 * kF + kBS,        // [2]   unit's accumulators complete (one arrival per set issuer)
+  kBarDFree = kBarDone + 2,       // [2]   accumulator read (4 epilogue warps)
+  kBarRegReady = kBarDFree + 2,   // [2]   region half written for the unit (4 epilogue warps)
+  kBarEpiDone = kBarRegReady + 2,
+  kBarEpiGo = kBarEpiDone + 1,
+  kBarUReady = kBarEpiGo + 1,     // [kUS]
+  kBarUFree = kBarUReady + kUS,   // [kUS]
+  kNumBars = kBarUFree + kUS
+};
+constexpr int kBarBytes = 512;
+static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
+constexpr uint32_t kUnitFreeCount = kDeqWarpsAll + kSets + 4 + 1;
 
 struct DecState {
-  Shared sched;          // ticket decoding state (scheduler thread)
-  Unit units[2];         // published units (double buffer)
-  int combine;           // strip to combine after a unit, or -1
-  int early;             // the next unit's first loads are already in flight
+  Shared sched;                              // ticket decoding state (scheduler thread)
+  Unit units[kUS];                           // published units
+  const uint32_t* planes[kUS][PW_MAX_BITS];  // each published unit's first tile, per plane
+  uint32_t deq_done;                         // units finished, summed over the 16 dequant warps
+  int combine;
+  int abort;                                 // CTA-wide: give up waiting
 };
-static_assert(sizeof(DecState) <= kStateBytes, "state size");
 
-struct SmemT {
-  uint8_t* b_ring;      // kG x kBSlots x kBSlotBytes
-  uint8_t* plane_ring;  // kG x kPlaneRing
-  float* xch;           // group-1 partial sums [token][pos]
-  uint32_t bar;         // barriers (shared address)
-  int* rows;            // [2][kN] B row offsets of the published units
-  uint32_t lut_region;
+struct Sm {
+  uint32_t bar;              // first barrier (shared address)
+  uint32_t region;           // 64 KB-aligned LUT region (q >= 5)
+  uint32_t bring;            // B ring
+  uint32_t pring[kSets];     // plane rings
   DecState* st;
 };
 
-__device__ __forceinline__ uint32_t group_bar(const SmemT& sm, int g) { return sm.bar + 8 * kBarsPerGroupT * g; }
-__device__ __forceinline__ uint32_t unit_ready_bar(const SmemT& sm, int s) {
-  return sm.bar + 8 * (kG * kBarsPerGroupT + s);
-}
-__device__ __forceinline__ uint32_t unit_free_bar(const SmemT& sm, int s) {
-  return sm.bar + 8 * (kG * kBarsPerGroupT + 2 + s);
-}
+__device__ __forceinline__ uint32_t bar(const Sm& sm, int i) { return sm.bar + 8u * static_cast<uint32_t>(i); }
 
-// Wait until the MMAs of this group's tile x have completed.
-__device__ __forceinline__ void wait_tile_free(uint32_t g0, uint32_t x, const Params& p, int& abort) {
-  if (!abort && !pw::mbar_wait(bar_free(g0, x % kF), (x / kF) & 1u, p.wait_ns)) abort = 1;
+__device__ __forceinline__ void fail(const Params& p, DecState& st) {
+  st.abort = 1;
+  report(p.status, PW_ERR_TIMEOUT);
+  atomicExch(p.ctr + 1, 1u);
 }
 
-__device__ __forceinline__ void named_sync_dequant() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// This group's share [tb, te) of a unit's 128-column tiles (group 0 takes the
-// larger half).
-__device__ __forceinline__ void group_tiles(const Unit& u, int g, int& tb, int& te) {
-  const int ntiles_all = u.nst / 2;
-  const int half = (ntiles_all + 1) / 2;
-  tb = g == 1 ? half : 0;
-  te = g == 0 ? half : ntiles_all;
-}
-
-// Per-thread tile loader of one unit: its plane slices and its B chunks.
-template <int Q>
-struct TileLoader {
-  static constexpr int kTileStrideW = pw::kTileBytes / 4;
-  static constexpr int kSlotBytes = Q * pw::kTileBytes;
-  static constexpr int D = (kPlaneRing / kSlotBytes) > 4 ? 4 : (kPlaneRing / kSlotBytes);
-  static_assert(D >= 2 && D + 2 <= kBSlots, "ring depths");
-  const uint32_t* src[Q];
-  const uint16_t* bbase;
-  const int* rows;
-  uint32_t ring, bring, g0, tcnt;
-  int ntiles, tile0, pos, nchunk;
-
-  __device__ __forceinline__ void init(const Params& p, const Unit& u, const SmemT& sm, const int* urows, int g,
-                                       int pos_, uint32_t tcnt_) {
-    const BlockDesc& d = *u.d;
-    int tb, te;
-    group_tiles(u, g, tb, te);
-    ntiles = te - tb;
-    tile0 = u.st0 / 2 + tb;
-    pos = pos_;
-    tcnt = tcnt_;
-    const int tiles = d.cols / pw::kTileCols;
-#pragma unroll
-    for (int q = 0; q < Q; ++q)
-      src[q] = d.planes[q] + (static_cast<long long>(u.strip) * tiles + tile0) * kTileStrideW + pos * 4;
-    ring = pw::smem_u32(sm.plane_ring + g * kPlaneRing) + pos * 16;
-    bring = pw::smem_u32(sm.b_ring + g * kBSlots * kBSlotBytes);
-    g0 = group_bar(sm, g);
-    bbase = u.kind == kDown ? p.h : p.x;
-    rows = urows;
-    nchunk = u.npad / 8;   // i = pos + 128 m (m < npad / 8): row n = i / 16, chunk c = i % 16
-  }
-
-  // Copy tile t (this group's numbering) into ring slot t % D and B slot
-  // (tcnt + t) % kBSlots; always commits one cp.async group.
-  __device__ __forceinline__ void issue(int t, const Params& p, int& abort) const {
-    if (t < ntiles) {
-      const uint32_t x = tcnt + t;
-      if (x >= kBSlots) wait_tile_free(g0, x - kBSlots, p, abort);
-      const uint32_t slot = ring + (t % D) * kSlotBytes;
-#pragma unroll
-      for (int q = 0; q < Q; ++q)
-        pw::cp_async_16(slot + q * pw::kTileBytes, src[q] + static_cast<long long>(t) * kTileStrideW);
-      const uint32_t bslot = bring + (x % kBSlots) * kBSlotBytes;
-      const long long col = static_cast<long long>(tile0 + t) * pw::kTileCols;
-      for (int m = 0; m < nchunk; ++m) {
-        const int i = pos + 128 * m;
-        const int n = i >> 4, c = i & 15;
-        pw::cp_async_16(bslot + (c >> 3) * kBAtomBytes + n * 128 + (((c & 7) ^ (n & 7)) << 4),
-                        bbase + rows[n] + col + c * 8);
-      }
+// Bounded wait for phase `parity`; gives up early once the CTA aborts.
+__device__ __forceinline__ bool wait_bar(const Sm& sm, int i, uint32_t parity, const Params& p) {
+  const uint32_t b = bar(sm, i);
+  if (pw::mbar_try_wait_hint(b, parity, kHintNs)) return true;
+  const uint64_t t0 = pw::global_ns();
+  volatile int* abort = &sm.st->abort;
+  while (true) {
+    if (pw::mbar_try_wait_hint(b, parity, kHintNs)) return true;
+    if (*abort) return false;
+    if (pw::global_ns() - t0 > p.wait_ns) {
+      fail(p, *sm.st);
+      return false;
     }
-    pw::cp_async_commit();
   }
+}
 
-  __device__ __forceinline__ void prologue(const Params& p, int& abort) const {
-#pragma unroll
-    for (int i = 0; i < D - 1; ++i) issue(i, p, abort);
+// Bounded wait that ignores the abort flag (copies and MMAs already issued
+// must land before the CTA exits).
+__device__ __forceinline__ void drain_bar(const Sm& sm, int i, uint32_t parity) {
+  const uint64_t t0 = pw::global_ns();
+  while (!pw::mbar_try_wait_hint(bar(sm, i), parity, kHintNs))
+    if (pw::global_ns() - t0 > 100000000ull) return;
+}
+
+// Bounded wait until a shared counter reaches `target`.
+__device__ __forceinline__ bool wait_count(const Sm& sm, const uint32_t* ctr, uint32_t target, const Params& p) {
+  const volatile uint32_t* c = ctr;
+  if (*c >= target) {
+    __threadfence_block();
+    return true;
   }
+  const uint64_t t0 = pw::global_ns();
+  volatile int* abort = &sm.st->abort;
+  while (*c < target) {
+    if (*abort) return false;
+    if (pw::global_ns() - t0 > p.wait_ns) {
+      fail(p, *sm.st);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  __threadfence_block();
+  return true;
+}
+
+// Lane 0 waits for unit i to be published; the warp then reads it.
+__device__ __forceinline__ bool wait_unit(const Sm& sm, uint32_t i, const Params& p) {
+  int ok = 1;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(sm, kBarUReady + static_cast<int>(i % kUS), (i / kUS) & 1u, p);
+  return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+__device__ __forceinline__ void cp_async_wait_dyn(int n) {
+  switch (n) {
+    case 0: pw::cp_async_wait<0>(); break;
+    case 1: pw::cp_async_wait<1>(); break;
+    case 2: pw::cp_async_wait<2>(); break;
+    case 3: pw::cp_async_wait<3>(); break;
+    case 4: pw::cp_async_wait<4>(); break;
+    case 5: pw::cp_async_wait<5>(); break;
+    case 6: pw::cp_async_wait<6>(); break;
+    default: pw::cp_async_wait<7>(); break;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// dequant warps
+// ---------------------------------------------------------------------------
+// A thread's plane-copy cursor over its set's tiles, across units.
+struct PlaneLoads {
+  uint32_t head, tail;   // ring slots taken / given back
+  uint32_t li, lx0;      // unit being copied and its first tile in the CTA's stream
+  int lt;                // its next tile for this set (unit-relative)
+  int ahead;             // tiles copied (commit groups) not yet consumed
+  bool end;
 };
 
-template <int Q>
-__device__ __noinline__ void issue_prologue(const Params& p, const Unit& u, const SmemT& sm, const int* urows,
-                                            int g, int pos, uint32_t tcnt, int& abort) {
-  TileLoader<Q> ld;
-  ld.init(p, u, sm, urows, g, pos, tcnt);
-  ld.prologue(p, abort);
-  // warm L2 with this row's LUT for the unit's start
-  const int row = strip_pos_row(u.strip, pos, u.d->rows / 2);
-  const char* lut = reinterpret_cast<const char*>(u.d->lut + static_cast<long long>(row) * (1 << Q));
-  for (int off = 0; off < (2 << Q); off += 128) asm volatile("prefetch.global.L2 [%0];" ::"l"(lut + off));
+// Copy the next tile of this set (all committed planes, this thread's row);
+// false when the ring is full, the next unit is not published yet (unless
+// `block`) or there are no more units.
+__device__ __forceinline__ bool issue_next(PlaneLoads& L, const Sm& sm, int set, int pos, uint32_t ring, bool block,
+                                           const Params& p) {
+  const DecState& st = *sm.st;
+  while (!L.end) {
+    const int us = static_cast<int>(L.li % kUS);
+    const uint32_t par = (L.li / kUS) & 1u;
+    if (!pw::mbar_test(bar(sm, kBarUReady + us), par)) {
+      if (!block) return false;
+      if (!wait_bar(sm, kBarUReady + us, par, p)) {
+        L.end = true;
+        return false;
+      }
+    }
+    const Unit& u = st.units[us];
+    if (u.kind == kNone) {
+      L.end = true;
+      return false;
+    }
+    const int nt = u.nst / 2;
+    if (L.lt >= nt) {
+      L.lx0 += static_cast<uint32_t>(nt);
+      ++L.li;
+      L.lt = static_cast<int>((static_cast<uint32_t>(set) - L.lx0) & 3u);
+      continue;
+    }
+    const int q = u.q;
+    if (L.head + static_cast<uint32_t>(q) - L.tail > static_cast<uint32_t>(kPSlots)) return false;
+    // slot layout: [half][pos][8 bytes] so that a warp reads 256 contiguous
+    // bytes per half
+    const long long off = static_cast<long long>(L.lt) * (pw::kTileBytes / 4) + pos * 4;
+    for (int pl = 0; pl < q; ++pl) {
+      const uint32_t dst = ring + ((L.head + pl) % kPSlots) * pw::kTileBytes + pos * 8;
+      const uint32_t* src = st.planes[us][pl] + off;
+      pw::cp_async_8(dst, src);
+      pw::cp_async_8(dst + pw::kTileBytes / 2, src + 2);
+    }
+    pw::cp_async_commit();
+    L.head += static_cast<uint32_t>(q);
+    ++L.ahead;
+    L.lt += kSets;
+    return true;
+  }
+  return false;
 }
 
-// One unit for a dequant thread: LUT, tiles, early start of the next unit,
-// epilogue.  Returns whether the next unit's first loads were issued.
 template <int Q>
-__device__ __noinline__ bool dequant_unit(const Params& p, const Unit& u, const SmemT& sm, const int* urows,
-                                          uint32_t tmem, uint32_t& tcnt, uint32_t unit_cnt, int slot, bool early,
-                                          int& abort) {
+__device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, const Sm& sm, uint32_t tmem, uint32_t x0,
+                                             uint32_t ui, PlaneLoads& L) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int g = warp >> 2, wq = warp & 3;
-  const int pos = wq * 32 + lane;
-  const BlockDesc& d = *u.d;
-  const int row = strip_pos_row(u.strip, pos, d.rows / 2);
+  const int set = warp >> 2, qd = warp & 3;
+  const int pos = qd * 32 + lane;
+  const uint32_t ring = sm.pring[set];
+  bool ok = true;
   pw::RowDequant<Q> dq;
   if constexpr (Q <= 4) {
+    const BlockDesc& d = *u.d;
+    const int row = strip_pos_row(u.strip, pos, d.rows / 2);
     dq.load(d.lut + static_cast<long long>(row) * (1 << Q), 0u, lane);
   } else {
-    dq.set_row(sm.lut_region, wq, lane);
-    dq.template load<kG>(d.lut + static_cast<long long>(row) * (1 << Q), g);
-    named_sync_dequant();   // both halves of every row's table are in place
+    dq.set_row(sm.region, qd, lane, static_cast<int>(ui & 1u));
+    ok = wait_bar(sm, kBarRegReady + static_cast<int>(ui & 1u), (ui >> 1) & 1u, p);
   }
-  TileLoader<Q> ld;
-  ld.init(p, u, sm, urows, g, pos, tcnt);
-  constexpr int D = TileLoader<Q>::D;
-  if (!early) ld.prologue(p, abort);
-
-  const uint32_t g0 = ld.g0;
-  const uint32_t tl = tmem + g * kGroupCols + (static_cast<uint32_t>(32 * wq) << 16);
-  for (int t = 0; t < ld.ntiles; ++t) {
-    ld.issue(t + D - 1, p, abort);
-    pw::cp_async_wait<D - 1>();
-    pw::fence_proxy_async_smem();   // this thread's B chunks of tile t, for the tensor core
-    const uint32_t rs = ld.ring + (t % D) * TileLoader<Q>::kSlotBytes;
-    uint32_t w4[Q][4];
-#pragma unroll
-    for (int q = 0; q < Q; ++q) lds_v4(rs + q * pw::kTileBytes, w4[q]);
-    const uint32_t x = tcnt + t;
-    if (x >= kSA) wait_tile_free(g0, x - kSA, p, abort);
+  const uint32_t nt = static_cast<uint32_t>(u.nst / 2);
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+  for (uint32_t x = x0 + ((static_cast<uint32_t>(set) - x0) & 3u); ok && x < x0 + nt; x += kSets) {
+    if (L.ahead == 0 && !issue_next(L, sm, set, pos, ring, true, p)) break;
+    while (issue_next(L, sm, set, pos, ring, false, p)) {
+    }
+    cp_async_wait_dyn(L.ahead - 1);
+    const uint32_t slot0 = L.tail;
+    L.tail += Q;
+    --L.ahead;
+    const int fs = static_cast<int>(x % kF);
+    if (x >= kSA && !wait_bar(sm, kBarTFree + static_cast<int>((x - kSA) % kF), ((x - kSA) / kF) & 1u, p)) break;
     pw::tc_fence_after();
     const uint32_t acol = tl + (x % kSA) * kATileCols;
 #pragma unroll
-    for (int wd = 0; wd < 4; ++wd) {
-      uint32_t ww[Q];
+    for (int hh = 0; hh < 2; ++hh) {
+      uint32_t w2[Q][2];
 #pragma unroll
-      for (int q = 0; q < Q; ++q) ww[q] = w4[q][wd];
-      uint32_t out[16];
-      dq.word(ww, out);
-      pw::tmem_st_x16(acol + 16 * wd, out);
+      for (int q = 0; q < Q; ++q)
+        pw::lds_v2(ring + ((slot0 + q) % kPSlots) * pw::kTileBytes + hh * (pw::kTileBytes / 2) + pos * 8, w2[q][0],
+                   w2[q][1]);
+#pragma unroll
+      for (int wd = 0; wd < 2; ++wd) {
+        uint32_t ww[Q];
+#pragma unroll
+        for (int q = 0; q < Q; ++q) ww[q] = w2[q][wd];
+        uint32_t out[16];
+        dq.word(ww, out);
+        pw::tmem_st_x16(acol + 16 * (2 * hh + wd), out);
+      }
     }
     pw::tmem_st_wait();
     pw::tc_fence_before();
     __syncwarp();
-    if (lane == 0) pw::mbar_arrive(bar_full(g0, x % kF));
+    if (lane == 0) pw::mbar_arrive(bar(sm, kBarAFull + fs));
   }
-  const int ntiles = ld.ntiles;
-  tcnt += ntiles;
-  pw::cp_async_wait<0>();
-
-  // start the next unit's loads now if it is already published
-  const int ns = slot ^ 1;
-  if (threadIdx.x == 0) {
-    const Unit& nu = sm.st->units[ns];
-    sm.st->early = mbar_test(unit_ready_bar(sm, ns), ((unit_cnt + 1) >> 1) & 1u) && nu.kind != kNone;
-  }
-  named_sync_dequant();   // also: both groups are done with this unit's LUT region
-  const bool next_early = sm.st->early != 0;
-  if (next_early) {
-    const Unit& nu = sm.st->units[ns];
-    const int* nrows = sm.rows + ns * kN;
-    switch (nu.q) {
-      case 2: issue_prologue<2>(p, nu, sm, nrows, g, pos, tcnt, abort); break;
-      case 3: issue_prologue<3>(p, nu, sm, nrows, g, pos, tcnt, abort); break;
-      case 4: issue_prologue<4>(p, nu, sm, nrows, g, pos, tcnt, abort); break;
-      case 5: issue_prologue<5>(p, nu, sm, nrows, g, pos, tcnt, abort); break;
-      case 6: issue_prologue<6>(p, nu, sm, nrows, g, pos, tcnt, abort); break;
-      case 7: issue_prologue<7>(p, nu, sm, nrows, g, pos, tcnt, abort); break;
-      default: issue_prologue<8>(p, nu, sm, nrows, g, pos, tcnt, abort); break;
-    }
-  }
-
-  // epilogue: accumulator row `pos` (TMEM lane), columns = tokens
-  if (!abort && !pw::mbar_wait(bar_done(g0), unit_cnt & 1u, p.wait_ns)) abort = 1;
-  pw::tc_fence_after();
-  float* xch = sm.xch;
-  uint32_t v[16];
-  if (ntiles > 0) {
-    pw::tmem_ld_x16(tl + kDColT, v);
-    pw::tmem_ld_wait();
-  } else {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) v[i] = 0u;
-  }
-  pw::tc_fence_before();
-  if (g == 1) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) xch[i * kDeqThreads + pos] = __uint_as_float(v[i]);
-  }
-  named_sync_dequant();
-  if (g == 0) {
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float val = __uint_as_float(v[i]) + xch[i * kDeqThreads + pos];
-      if (u.kind == kGateUp) {
-        const float up = __shfl_down_sync(0xffffffffu, val, 16);
-        if (lane < 16 && i < u.nrows) {
-          const int m = u.strip * 64 + 16 * wq + lane;
-          p.h[static_cast<long long>(u.off + i) * p.I + m] = __half_as_ushort(__float2half_rn(silu(val) * up));
-        }
-      } else if (u.kind == kDown) {
-        if (i < u.nrows) p.part[(static_cast<long long>(u.split) * p.A + u.off + i) * p.H + row] = val;
-      } else {
-        if (i < u.nrows) p.out[static_cast<long long>(u.tg * kN + i) * d.rows + row] = val;
-      }
-    }
-  }
-  return next_early;
 }
 
-__device__ void mma_unit(const Unit& u, const SmemT& sm, uint32_t tmem, uint32_t& tcnt, const Params& p,
-                         int& abort) {
-  const int g = (threadIdx.x >> 5) - kMmaWarp0;
-  int tb, te;
-  group_tiles(u, g, tb, te);
-  const int ntiles = te - tb;
-  const uint32_t g0 = group_bar(sm, g);
-  if ((threadIdx.x & 31) == 0) {
-    const uint32_t bring = pw::smem_u32(sm.b_ring + g * kBSlots * kBSlotBytes);
-    const uint32_t tg = tmem + g * kGroupCols;
-    const uint32_t idesc = pw::idesc_f16_f32(128, u.npad);
-    for (int t = 0; t < ntiles; ++t) {
-      const uint32_t x = tcnt + t;
-      if (!abort && !pw::mbar_wait(bar_full(g0, x % kF), (x / kF) & 1u, p.wait_ns)) abort = 1;
+__device__ void dequant_role(const Params& p, const Sm& sm, uint32_t tmem) {
+  const int set = (threadIdx.x >> 5) >> 2;
+  PlaneLoads L;
+  L.head = L.tail = 0;
+  L.li = 0;
+  L.lx0 = 0;
+  L.lt = set;
+  L.ahead = 0;
+  L.end = false;
+  uint32_t x = 0;
+  for (uint32_t i = 0;; ++i) {
+    if (!wait_unit(sm, i, p)) break;
+    const Unit& u = sm.st->units[i % kUS];
+    if (u.kind == kNone) break;
+    switch (u.q) {
+      case 2: dequant_unit<2>(p, u, sm, tmem, x, i, L); break;
+      case 3: dequant_unit<3>(p, u, sm, tmem, x, i, L); break;
+      case 4: dequant_unit<4>(p, u, sm, tmem, x, i, L); break;
+      case 5: dequant_unit<5>(p, u, sm, tmem, x, i, L); break;
+      case 6: dequant_unit<6>(p, u, sm, tmem, x, i, L); break;
+      case 7: dequant_unit<7>(p, u, sm, tmem, x, i, L); break;
+      default: dequant_unit<8>(p, u, sm, tmem, x, i, L); break;
+    }
+    x += static_cast<uint32_t>(u.nst / 2);
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) {
+      // a monotonic count, not a barrier phase: the LUT writers may look at it
+      // several units later
+      __threadfence_block();
+      atomicAdd(&sm.st->deq_done, 1u);
+      pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(i % kUS)));
+    }
+  }
+  pw::cp_async_wait<0>();   // every plane copy lands before the CTA exits
+}
+
+// ---------------------------------------------------------------------------
+// loader (one thread): B operands and LUT prefetch
+// ---------------------------------------------------------------------------
+__device__ void loader_role(const Params& p, const Sm& sm, const void* map_gu, const void* map_dn) {
+  DecState& st = *sm.st;
+  bool gathered = p.linear != 0;
+  uint32_t x = 0;
+  for (uint32_t u = 0;; ++u) {
+    if (!wait_bar(sm, kBarUReady + static_cast<int>(u % kUS), (u / kUS) & 1u, p)) break;
+    const Unit& un = st.units[u % kUS];
+    if (un.kind == kNone) break;
+    const BlockDesc& d = *un.d;
+    // the unit's LUT rows (two runs of 64 rows) into L2 for the LUT readers
+    const long long rowb = static_cast<long long>(2) << un.q;
+    const char* lut = reinterpret_cast<const char*>(d.lut);
+    pw::prefetch_l2(lut + un.strip * 64 * rowb, static_cast<uint32_t>(64 * rowb));
+    pw::prefetch_l2(lut + (static_cast<long long>(d.rows / 2) + un.strip * 64) * rowb, static_cast<uint32_t>(64 * rowb));
+    if (un.kind == kGateUp && !gathered) {
+      const uint64_t t0 = pw::global_ns();
+      bool g = true;
+      while (pw::ld_acquire_gpu(p.gather_ctr) < gridDim.x) {
+        if (st.abort || pw::global_ns() - t0 > p.wait_ns) {
+          if (!st.abort) fail(p, st);
+          g = false;
+          break;
+        }
+        __nanosleep(100);
+      }
+      if (!g) break;
+      gathered = true;
+    }
+    if (un.kind != kLinear) pw::fence_proxy_async_global();   // x / h rows written by this kernel
+    const void* map = un.kind == kDown ? map_dn : map_gu;
+    const int brow = un.kind == kLinear ? un.tg * kN : un.off;
+    const int tile0 = un.st0 / 2, ntl = un.nst / 2;
+    bool ok = true;
+    for (int t = 0; t < ntl; ++t, ++x) {
+      const int b = static_cast<int>(x % kBS);
+      const uint32_t fb = bar(sm, kBarBFull + b);
+      // the slot's previous tile (x - kBS) must be consumed by its MMAs
+      if (x >= kBS && !wait_bar(sm, kBarTFree + static_cast<int>((x - kBS) % kF), ((x - kBS) / kF) & 1u, p)) {
+        ok = false;
+        break;
+      }
+      pw::mbar_arrive_expect_tx(fb, kBBytes);
+      const uint32_t dst = sm.bring + static_cast<uint32_t>(b) * kBBytes;
+      const int col = (tile0 + t) * pw::kTileCols;
+      pw::tma_load_2d(dst, map, col, brow, fb);
+      pw::tma_load_2d(dst + kBAtom, map, col + 64, brow, fb);
+    }
+    if (!ok) break;
+    pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(u % kUS)));
+  }
+  // the last copies land before the CTA exits
+  for (uint32_t y = x > static_cast<uint32_t>(kBS) ? x - kBS : 0u; y < x; ++y)
+    drain_bar(sm, kBarBFull + static_cast<int>(y % kBS), (y / kBS) & 1u);
+}
+
+// ---------------------------------------------------------------------------
+// MMA issuers: one thread per set, its own accumulators
+// ---------------------------------------------------------------------------
+__device__ void mma_role(const Params& p, const Sm& sm, uint32_t tmem, int set) {
+  DecState& st = *sm.st;
+  const uint32_t idesc = pw::idesc_f16_f32(128, kN);
+  uint32_t x0 = 0;
+  uint32_t last = 0;
+  bool issued = false;
+  for (uint32_t mu = 0;; ++mu) {
+    if (!wait_bar(sm, kBarUReady + static_cast<int>(mu % kUS), (mu / kUS) & 1u, p)) break;
+    const Unit& um = st.units[mu % kUS];
+    if (um.kind == kNone) break;
+    const uint32_t nt = static_cast<uint32_t>(um.nst / 2);
+    const uint32_t db = mu & 1u;
+    // this set's accumulator in buffer db is free once unit mu - 2's epilogue read it
+    if (mu >= 2 && !wait_bar(sm, kBarDFree + static_cast<int>(db), ((mu - 2) >> 1) & 1u, p)) break;
+    const uint32_t dcol = tmem + kDCol0 + (db * kSets + static_cast<uint32_t>(set)) * kN;
+    bool ok = true, any = false;
+    for (uint32_t x = x0 + ((static_cast<uint32_t>(set) - x0) & 3u); x < x0 + nt; x += kSets) {
+      const int fs = static_cast<int>(x % kF), b = static_cast<int>(x % kBS);
+      if (!wait_bar(sm, kBarBFull + b, (x / kBS) & 1u, p) || !wait_bar(sm, kBarAFull + fs, (x / kF) & 1u, p)) {
+        ok = false;
+        break;
+      }
       pw::tc_fence_after();
-      const uint32_t a = tg + (x % kSA) * kATileCols;
-      const uint32_t b = bring + (x % kBSlots) * kBSlotBytes;
+      const uint32_t a = tmem + (x % kSA) * kATileCols;
+      const uint32_t bsm = sm.bring + static_cast<uint32_t>(b) * kBBytes;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        const uint64_t bdesc = pw::sdesc_kmajor_sw128(b + (j >> 2) * kBAtomBytes) + 2ull * (j & 3);
-        pw::tc_mma_ts(tg + kDColT, a + 8 * j, bdesc, idesc, (t > 0 || j > 0) ? 1u : 0u);
+        const uint64_t bdesc = pw::sdesc_kmajor_sw128(bsm + (j >> 2) * kBAtom) + 2ull * (j & 3);
+        pw::tc_mma_ts(dcol, a + 8 * j, bdesc, idesc, (any || j > 0) ? 1u : 0u);
       }
-      pw::tc_commit(bar_free(g0, x % kF));
+      pw::tc_commit(bar(sm, kBarTFree + fs));
+      any = issued = true;
+      last = x;
     }
-    if (ntiles > 0)
-      pw::tc_commit(bar_done(g0));
+    if (!ok) break;
+    // one arrival per set on the unit's "done" barrier, after its MMAs
+    if (any)
+      pw::tc_commit(bar(sm, kBarDone + static_cast<int>(db)));
     else
-      pw::mbar_arrive(bar_done(g0));
+      pw::mbar_arrive(bar(sm, kBarDone + static_cast<int>(db)));
+    x0 += nt;
+    pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(mu % kUS)));
   }
-  tcnt += ntiles;
-  __syncwarp();
+  // the last MMAs complete before the CTA exits
+  if (issued) drain_bar(sm, kBarTFree + static_cast<int>(last % kF), (last / kF) & 1u);
 }
 
-// Scheduler (one thread): publish units into the two slots, one ahead.
-__device__ void scheduler(const Params& p, const SmemT& sm) {
+// ---------------------------------------------------------------------------
+// epilogue warps: LUT region one unit ahead, then the unit's epilogue
+// ---------------------------------------------------------------------------
+// Write unit i's LUT into region half i & 1 (q >= 5; q = 8 takes the whole
+// region) once every earlier user of those lines is finished, then signal the
+// half ready (also for q <= 4, which keeps the barrier phases one per unit).
+// Returns 1 when done, 0 when unit i is the end marker, and -1 without
+// waiting when `block` is false and unit i is not published yet.
+__device__ int lut_fill(const Params& p, const Sm& sm, uint32_t i, bool& prev_q8, bool block) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (!block) {
+    int pub = 0;
+    if (lane == 0) pub = pw::mbar_test(bar(sm, kBarUReady + static_cast<int>(i % kUS)), (i / kUS) & 1u);
+    if (!__shfl_sync(0xffffffffu, pub, 0)) return -1;
+  }
+  if (!wait_unit(sm, i, p)) return 0;
+  const Unit& u = sm.st->units[i % kUS];
+  if (u.kind == kNone) return 0;
+  const int qd = warp & 3, pos = qd * 32 + lane;
+  const int h = static_cast<int>(i & 1u);
+  // units up to i - 2 (the half's previous user), or up to i - 1 when unit
+  // i or i - 1 takes the whole region, are finished by every dequant warp
+  const uint32_t need = static_cast<uint32_t>(kDeqWarpsAll) * ((u.q == 8 || prev_q8) ? i : (i >= 1 ? i - 1 : 0u));
+  const bool ok = wait_count(sm, &sm.st->deq_done, need, p);
+  if (ok && u.q >= 5) {
+    const BlockDesc& d = *u.d;
+    const int row = strip_pos_row(u.strip, pos, d.rows / 2);
+    const uint16_t* lut = d.lut + (static_cast<long long>(row) << u.q);
+    const uint32_t tblw =
+        sm.region | (static_cast<uint32_t>((qd & 1) * 32 + lane) * 4u + static_cast<uint32_t>(qd >> 1) * 2u);
+    switch (u.q) {
+      case 5: pw::region_fill<5>(tblw, lut, h); break;
+      case 6: pw::region_fill<6>(tblw, lut, h); break;
+      case 7: pw::region_fill<7>(tblw, lut, h); break;
+      default: pw::region_fill<8>(tblw, lut, h); break;
+    }
+  }
+  prev_q8 = u.q == 8;
+  __syncwarp();
+  if (lane == 0) pw::mbar_arrive(bar(sm, kBarRegReady + h));
+  return 1;
+}
+
+__device__ void epilogue_unit(const Params& p, const Sm& sm, uint32_t tmem, uint32_t i, uint32_t x0) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int qd = warp & 3;
+  const int pos = qd * 32 + lane;
+  const int etid = threadIdx.x - kEpiWarp0 * 32;
+  DecState& st = *sm.st;
+  const Unit& u = st.units[i % kUS];
+  const uint32_t db = i & 1u;
+  const bool ok = wait_bar(sm, kBarDone + static_cast<int>(db), (i >> 1) & 1u, p);
+  // sum of the accumulators of the sets that hold a tile of the unit (set s
+  // holds the tiles x0 <= x < x0 + nt with x % 4 == s)
+  float acc[16];
+#pragma unroll
+  for (int n = 0; n < 16; ++n) acc[n] = 0.f;
+  if (ok) {
+    pw::tc_fence_after();
+    const uint32_t nt = static_cast<uint32_t>(u.nst / 2);
+    for (int s2 = 0; s2 < kSets; ++s2) {
+      if (((static_cast<uint32_t>(s2) - x0) & 3u) >= nt) continue;
+      uint32_t v[16];
+      pw::tmem_ld_x16(tmem + kDCol0 + (db * kSets + static_cast<uint32_t>(s2)) * kN + (static_cast<uint32_t>(32 * qd) << 16),
+                      v);
+      pw::tmem_ld_wait();
+#pragma unroll
+      for (int n = 0; n < 16; ++n) acc[n] += __uint_as_float(v[n]);
+    }
+  }
+  pw::tc_fence_before();
+  __syncwarp();
+  if (lane == 0) pw::mbar_arrive(bar(sm, kBarDFree + static_cast<int>(db)));
+  if (ok) {
+    const BlockDesc& d = *u.d;
+    const int row = strip_pos_row(u.strip, pos, d.rows / 2);
+#pragma unroll
+    for (int n = 0; n < 16; ++n) {
+      const float val = acc[n];
+      if (u.kind == kGateUp) {
+        const float up = __shfl_down_sync(0xffffffffu, val, 16);
+        if (lane < 16 && n < u.nrows) {
+          const int m = u.strip * 64 + 16 * qd + lane;
+          p.h[static_cast<long long>(u.off + n) * p.I + m] = __half_as_ushort(__float2half_rn(silu(val) * up));
+        }
+      } else if (u.kind == kDown) {
+        if (n < u.nrows) p.part[(static_cast<long long>(u.split) * p.A + u.off + n) * p.H + row] = val;
+      } else {
+        if (n < u.nrows) p.out[static_cast<long long>(u.tg * kN + n) * d.rows + row] = val;
+      }
+    }
+    if (u.kind == kGateUp) pw::fence_proxy_async_global();   // h is read back through TMA
+  }
+  __syncwarp();
+  if (lane == 0) pw::mbar_arrive(bar(sm, kBarEpiDone));
+  if (etid == 0) {
+    int c = -1;
+    if (wait_bar(sm, kBarEpiDone, i & 1u, p) && ok) c = finish_unit(p, st.sched, u, 0);
+    st.combine = c;
+    pw::mbar_arrive(bar(sm, kBarEpiGo));
+  }
+  const bool go = wait_bar(sm, kBarEpiGo, i & 1u, p);
+  const int c = *reinterpret_cast<volatile int*>(&st.combine);
+  if (go && c >= 0) combine_strip(p, c, etid, kEpiThreads);
+  __syncwarp();
+  if (lane == 0) pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(i % kUS)));
+}
+
+// The next unit's LUT goes first when that unit is already published; the
+// role never waits for a publication before finishing the current unit's
+// epilogue (the scheduler may be waiting, for a down unit, on exactly that
+// epilogue's gate_up completion).
+__device__ void epilogue_role(const Params& p, const Sm& sm, uint32_t tmem) {
+  bool prev_q8 = false;
+  int more = lut_fill(p, sm, 0, prev_q8, true);
+  uint32_t x0 = 0;
+  for (uint32_t i = 0; more == 1; ++i) {
+    int next = lut_fill(p, sm, i + 1, prev_q8, false);
+    const uint32_t nt = static_cast<uint32_t>(sm.st->units[i % kUS].nst / 2);
+    epilogue_unit(p, sm, tmem, i, x0);
+    x0 += nt;
+    if (next < 0) next = lut_fill(p, sm, i + 1, prev_q8, true);
+    more = next;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// scheduler (one thread)
+// ---------------------------------------------------------------------------
+__device__ void scheduler_role(const Params& p, const Sm& sm) {
   DecState& st = *sm.st;
   for (uint32_t i = 0;; ++i) {
-    const int s = static_cast<int>(i & 1u);
-    if (i >= 2 && !pw::mbar_wait(unit_free_bar(sm, s), ((i - 2) >> 1) & 1u, p.wait_ns)) {
-      report(p.status, PW_ERR_TIMEOUT);
-      st.sched.abort = 1;
-    }
+    const int s = static_cast<int>(i % kUS);
+    if (i >= kUS && !wait_bar(sm, kBarUFree + s, ((i - kUS) / kUS) & 1u, p)) st.sched.abort = 1;
+    if (st.abort) st.sched.abort = 1;
     Unit u;
     do {
       next_unit<kN>(p, st.sched);
@@ -359,132 +571,152 @@ __device__ void scheduler(const Params& p, const SmemT& sm) {
     } while (u.kind != kNone && u.skip);
     st.units[s] = u;
     if (u.kind != kNone) {
-      int* rows = sm.rows + s * kN;
-      for (int n = 0; n < kN; ++n) {
-        const int nn = min(n, u.nrows - 1);
-        int r;
-        if (u.kind == kGateUp)
-          r = (__ldg(p.perm + u.off + nn) / p.k) * p.H;
-        else if (u.kind == kDown)
-          r = (u.off + nn) * p.I;
-        else
-          r = (u.tg * kN + nn) * u.d->cols;
-        rows[n] = r;
-      }
+      const BlockDesc& d = *u.d;
+      const long long first = (static_cast<long long>(u.strip) * (d.cols / pw::kTileCols) + u.st0 / 2) *
+                              (pw::kTileBytes / 4);
+      for (int q = 0; q < u.q; ++q) st.planes[s][q] = d.planes[q] + first;
     }
-    pw::mbar_arrive(unit_ready_bar(sm, s));
+    pw::mbar_arrive(bar(sm, kBarUReady + s));
     if (u.kind == kNone) return;
   }
 }
 
-// Wait (lane 0, then the whole warp) for unit i to be published.
-__device__ __forceinline__ void wait_unit(const SmemT& sm, uint32_t i, const Params& p, int& abort) {
-  if ((threadIdx.x & 31) == 0) {
-    if (!pw::mbar_wait(unit_ready_bar(sm, static_cast<int>(i & 1u)), (i >> 1) & 1u, 4 * p.wait_ns)) {
-      // the scheduler is stuck; stop after this unit
-      abort = 1;
+// Carve the dynamic shared memory: barriers and state, then the B ring and
+// the plane rings in the space around the 64 KB-aligned LUT region.
+__device__ __forceinline__ bool carve(Sm& sm, uint8_t* smem_raw) {
+  const uint32_t base = pw::smem_u32(smem_raw);
+  const uint32_t end = base + static_cast<uint32_t>(kSmemBytes);
+  const uint32_t small = (base + 1023u) & ~1023u;
+  sm.bar = small;
+  const uint32_t st_addr = small + kBarBytes;
+  sm.st = reinterpret_cast<DecState*>(smem_raw + (st_addr - base));
+  const uint32_t small_end = st_addr + static_cast<uint32_t>(sizeof(DecState));
+  sm.region = (small_end + 0xFFFFu) & ~0xFFFFu;
+  uint32_t a = (small_end + 1023u) & ~1023u, b = sm.region + static_cast<uint32_t>(pw::kLutRegionBytes);
+  auto take = [&](uint32_t size, uint32_t& out) {
+    if (a + size <= sm.region) {
+      out = a;
+      a += size;
+      return true;
     }
-  }
-  __syncwarp();
+    if (b + size <= end) {
+      out = b;
+      b += size;
+      return true;
+    }
+    return false;
+  };
+  bool ok = take(kBS * kBBytes, sm.bring);
+  for (int s = 0; s < kSets; ++s) ok = ok && take(kPRingBytes, sm.pring[s]);
+  return ok && sm.region + static_cast<uint32_t>(pw::kLutRegionBytes) <= end;
 }
 
-__global__ void __launch_bounds__(kThreads, 1) apl_decode_kernel(Params p) {
+__global__ void __launch_bounds__(kThreads, 1)
+    apl_decode_kernel(const Params p, const __grid_constant__ CUtensorMap map_gu,
+                      const __grid_constant__ CUtensorMap map_dn) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
-  const uint32_t base = pw::smem_u32(smem_raw);
-  const uint32_t pre = (base + 1023u) & ~1023u;
-  const uint32_t region = (pre + static_cast<uint32_t>(kPreBytes) + 0xFFFFu) & ~0xFFFFu;
-  const uint32_t post = region + static_cast<uint32_t>(pw::kLutRegionBytes);
-  if (post + static_cast<uint32_t>(kPostBytes) > base + static_cast<uint32_t>(kSmemBytes)) {
+  Sm sm;
+  if (!carve(sm, smem_raw)) {
     if (threadIdx.x == 0) report(p.status, PW_ERR_UNSUPPORTED);   // unexpected shared-window base
     return;
   }
-  auto at = [&](uint32_t addr) { return smem_raw + (addr - base); };
-  SmemT sm;
-  uint32_t cur = pre;
-  sm.b_ring = at(cur);
-  cur += kBRingBytes;
-  sm.bar = cur;
-  cur += kBarBytes;
-  sm.rows = reinterpret_cast<int*>(at(cur));
-  cur += kRowsBytes;
-  sm.st = reinterpret_cast<DecState*>(at((cur + 15u) & ~15u));
-  sm.lut_region = region;
-  sm.plane_ring = at(post);
-  sm.xch = reinterpret_cast<float*>(at(post + kG * kPlaneRing));
-
-  const int warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  DecState& st = *sm.st;
   if (threadIdx.x == 0) {
-    for (int g = 0; g < kG; ++g) {
-      const uint32_t g0 = group_bar(sm, g);
-      for (int i = 0; i < kF; ++i) {
-        pw::mbar_init(bar_full(g0, i), kDeqWarps);
-        pw::mbar_init(bar_free(g0, i), 1);
-      }
-      pw::mbar_init(bar_done(g0), 1);
+    for (int i = 0; i < kF; ++i) {
+      pw::mbar_init(bar(sm, kBarAFull + i), 4);
+      pw::mbar_init(bar(sm, kBarTFree + i), 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      pw::mbar_init(unit_ready_bar(sm, s), 1);
-      pw::mbar_init(unit_free_bar(sm, s), kG * kDeqWarps + kG);
+    for (int i = 0; i < kBS; ++i) pw::mbar_init(bar(sm, kBarBFull + i), 1);
+    for (int i = 0; i < 2; ++i) {
+      pw::mbar_init(bar(sm, kBarDone + i), kSets);
+      pw::mbar_init(bar(sm, kBarDFree + i), 4);
+      pw::mbar_init(bar(sm, kBarRegReady + i), 4);
+    }
+    pw::mbar_init(bar(sm, kBarEpiDone), 4);
+    pw::mbar_init(bar(sm, kBarEpiGo), 1);
+    for (int s = 0; s < kUS; ++s) {
+      pw::mbar_init(bar(sm, kBarUReady + s), 1);
+      pw::mbar_init(bar(sm, kBarUFree + s), kUnitFreeCount);
     }
     pw::mbar_init_fence();
-    sm.st->sched.abort = 0;
-    setup_schedule<kN>(p, sm.st->sched);
+    st.abort = 0;
+    st.deq_done = 0;
+    st.sched.abort = 0;
+    setup_schedule<kN>(p, st.sched);
   }
   if (warp == 0) {
-    pw::tmem_alloc(pw::smem_u32(&sm.st->sched.tmem), kTmemColsT);
+    pw::tmem_alloc(pw::smem_u32(&st.sched.tmem), kTmemCols);
     pw::tmem_relinquish();
   }
-  pw::tc_fence_before();
-  __syncthreads();
-  pw::tc_fence_after();
-  const uint32_t tmem = sm.st->sched.tmem;
-
-  int abort_local = 0;
-  if (warp == kSchedWarp) {
-    if ((threadIdx.x & 31) == 0) scheduler(p, sm);
-  } else if (warp >= kMmaWarp0) {
-    uint32_t tcnt = 0;
-    for (uint32_t i = 0;; ++i) {
-      wait_unit(sm, i, p, abort_local);
-      const Unit& u = sm.st->units[i & 1u];
-      if (u.kind == kNone || abort_local) break;
-      mma_unit(u, sm, tmem, tcnt, p, abort_local);
-      if ((threadIdx.x & 31) == 0) pw::mbar_arrive(unit_free_bar(sm, static_cast<int>(i & 1u)));
+  if (warp == kLoadWarp && lane == 0) {
+    pw::prefetch_tmap(&map_gu);
+    if (!p.linear) pw::prefetch_tmap(&map_dn);
+  }
+  // gate_up B rows: this CTA's share of x gathered into expert order
+  if (!p.linear) {
+    const int vrow = p.H / 8;
+    const long long nvec = static_cast<long long>(p.A) * vrow;
+    for (long long v = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; v < nvec;
+         v += static_cast<long long>(gridDim.x) * kThreads) {
+      const int a = static_cast<int>(v / vrow), c = static_cast<int>(v % vrow);
+      const int tok = __ldg(p.perm + a) / p.k;
+      const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<long long>(tok) * p.H) + c);
+      reinterpret_cast<uint4*>(p.xp + static_cast<long long>(a) * p.H)[c] = val;
     }
-  } else {
-    uint32_t tcnt = 0;
-    bool early = false;
-    for (uint32_t i = 0;; ++i) {
-      wait_unit(sm, i, p, abort_local);
-      const int s = static_cast<int>(i & 1u);
-      const Unit& u = sm.st->units[s];
-      if (u.kind == kNone || abort_local) break;
-      const int* urows = sm.rows + s * kN;
-      switch (u.q) {
-        case 2: early = dequant_unit<2>(p, u, sm, urows, tmem, tcnt, i, s, early, abort_local); break;
-        case 3: early = dequant_unit<3>(p, u, sm, urows, tmem, tcnt, i, s, early, abort_local); break;
-        case 4: early = dequant_unit<4>(p, u, sm, urows, tmem, tcnt, i, s, early, abort_local); break;
-        case 5: early = dequant_unit<5>(p, u, sm, urows, tmem, tcnt, i, s, early, abort_local); break;
-        case 6: early = dequant_unit<6>(p, u, sm, urows, tmem, tcnt, i, s, early, abort_local); break;
-        case 7: early = dequant_unit<7>(p, u, sm, urows, tmem, tcnt, i, s, early, abort_local); break;
-        default: early = dequant_unit<8>(p, u, sm, urows, tmem, tcnt, i, s, early, abort_local); break;
-      }
-      // every epilogue store of both groups is issued: publish the unit
-      named_sync_dequant();
-      if (threadIdx.x == 0) sm.st->combine = finish_unit(p, sm.st->sched, u, 0);
-      named_sync_dequant();
-      if (sm.st->combine >= 0) combine_strip(p, sm.st->combine, threadIdx.x, kDeqAll);
-      if (abort_local) {
-        report(p.status, PW_ERR_TIMEOUT);
-        sm.st->sched.abort = 1;
-      }
-      if ((threadIdx.x & 31) == 0) pw::mbar_arrive(unit_free_bar(sm, s));
-    }
+    pw::fence_proxy_async_global();
   }
   pw::tc_fence_before();
   __syncthreads();
   pw::tc_fence_after();
-  if (warp == 0) pw::tmem_dealloc(tmem, kTmemColsT);
+  if (!p.linear && threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(p.gather_ctr, 1u);
+  }
+  const uint32_t tmem = st.sched.tmem;
+
+  if (warp < kDeqWarpsAll) {
+    dequant_role(p, sm, tmem);
+  } else if (warp < kEpiWarp0) {
+    if (lane == 0) mma_role(p, sm, tmem, warp - kMmaWarp0);
+  } else if (warp < kLoadWarp) {
+    epilogue_role(p, sm, tmem);
+  } else if (warp == kLoadWarp) {
+    if (lane == 0) loader_role(p, sm, &map_gu, &map_dn);
+  } else if (lane == 0) {
+    scheduler_role(p, sm);
+  }
+  pw::tc_fence_before();
+  __syncthreads();
+  pw::tc_fence_after();
+  if (warp == 0) pw::tmem_dealloc(tmem, kTmemCols);
+}
+
+// Row-major fp16 [rows][cols] seen as a 2-D tensor with 64 x kN boxes in the
+// 128-byte swizzle (one B atom per box).
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+int encode_rows(CUtensorMap* m, const void* base, long long cols, long long rows) {
+  static EncodeTiled fn = nullptr;
+  if (!fn) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    PW_CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q));
+    if (!f || q != cudaDriverEntryPointSuccess)
+      return pw::set_error(PW_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    fn = reinterpret_cast<EncodeTiled>(f);
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+  const cuuint32_t box[2] = {64, kN};
+  const cuuint32_t es[2] = {1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return pw::set_error(PW_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+  return PW_OK;
 }
 
 }  // namespace
@@ -497,8 +729,16 @@ int launch_decode_kernel(const Params& p, cudaStream_t s) {
   }
   const int sms = sm_count_cached();
   if (sms < 1) return pw::set_error(PW_ERR_CUDA, "could not query the SM count");
+  CUtensorMap gu, dn;
+  if (p.linear) {
+    if (int e = encode_rows(&gu, p.x, p.lin.cols, p.M)) return e;
+    dn = gu;
+  } else {
+    if (int e = encode_rows(&gu, p.xp, p.H, p.A)) return e;
+    if (int e = encode_rows(&dn, p.h, p.I, p.A)) return e;
+  }
   // one CTA per SM: it owns all 512 TMEM columns
-  apl_decode_kernel<<<sms, kThreads, kSmemBytes, s>>>(p);
+  apl_decode_kernel<<<sms, kThreads, kSmemBytes, s>>>(p, gu, dn);
   PW_CUDA_TRY(cudaGetLastError());
   return PW_OK;
 }

@@ -179,7 +179,8 @@ size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k);
  * rounded to fp16, and y is rounded to fp16.  Experts with no tokens are not
  * read.  Blocks of expert e in `layer` are descriptor entries
  * (layer*E + e)*2 + {0: gate_up, 1: down} of d_desc (see _sync).
- *  d_x  fp16 [T][H];  d_y fp16 [T][H] (written);  routing arrays as produced by
+ *  d_x  fp16 [T][H], 16-byte aligned;  d_y fp16 [T][H] (written), 8-byte
+ *  aligned;  routing arrays as produced by
  *  pw_moe_route_topk (d_ids may be NULL: it is not read);
  *  d_ws workspace of pw_moe_apl_ffn_workspace() bytes, 256-byte aligned,
  *  contents need not be initialised;
@@ -187,7 +188,7 @@ size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k);
  *  untouched on success, so the caller zeroes it beforehand).
  * Shapes: H % 128 == 0, I % 128 == 0, committed bitwidths 2..8.
  * The call picks one of two tile shapes from the average number of tokens
- * per expert (T*k/E): up to 32 tokens per tile below 48, else 256 (both run on
+ * per expert (T*k/E): up to 16 tokens per tile below 48, else 256 (both run on
  * the tcgen05 tensor cores; pw_moe_apl_ffn_ex can force either). */
 int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
                    int E, int k, const int32_t* d_ids, const float* d_w,
@@ -204,7 +205,7 @@ int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, in
  * PW_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU that loads the library
  * holds until the process exits.  Calls whose workspace
  * (pw_moe_apl_ffn_workspace) exceeds it fail with PW_ERR_WORKSPACE before
- * anything is enqueued; for the Mixtral-8x7B shape that allows up to 117
+ * anything is enqueued; for the Mixtral-8x7B shape that allows up to 110
  * tokens per call at top-2.  This entry point allocates nothing itself (no
  * cudaMalloc/cudaFree, no allocating library routine).
  *  - The first call on a device looks up the array's device address (a one-off
@@ -223,7 +224,7 @@ int pw_moe_apl_ffn_noalloc(const void* d_desc, int layer, const uint16_t* d_x, i
 
 /* Options of pw_moe_apl_ffn_ex (zero-initialise, then set what you need). */
 #define PW_PATH_AUTO 0
-#define PW_PATH_DECODE 1   /* token tiles of up to 32 (decode batches) */
+#define PW_PATH_DECODE 1   /* token tiles of up to 16 (decode batches) */
 #define PW_PATH_PREFILL 2  /* token tiles of up to 256 (prefill batches) */
 #define PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL 1u  /* test hook: one gate_up unit never
                                                  signals completion, so the waits

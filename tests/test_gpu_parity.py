@@ -223,6 +223,34 @@ def test_ffn_tiny_workload():
     _assert_close(y_ref, y)
 
 
+@pytest.mark.parametrize("bits,T", [(4, 1), (3, 1), (8, 1), (5, 8), (6, 64), (8, 100)])
+def test_ffn_back_to_back_calls(bits, T):
+    """Thirty back-to-back calls of one 8x7B-shaped layer on the decode path:
+    every call completes (no wait runs out) and returns the same bits (the
+    combine order is fixed), and a sampled token matches the oracle."""
+    wl = synth.MIXTRAL_8X7B_SWEEP.with_(fixed_bits=bits, tokens=T)
+    li = synth.layer_inputs(wl, device=DEV)
+    sh = wl.shape
+    stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, wl.parent_bits, wl.seed_bits, DEV)
+    load_layer(stack, 0, li)
+    stack.sync()
+    call = MoECall(stack, T)
+    opts = pw.pw_ffn_options()
+    opts.path = pw.PW_PATH_DECODE
+    first = None
+    for _ in range(30):
+        y = call(0, li.x, li.logits, options=opts)
+        torch.cuda.synchronize()
+        assert int(call.status.item()) == 0
+        if first is None:
+            first = y.clone()
+        else:
+            assert torch.equal(y, first)
+    toks = _sample_tokens(li, 1, seed=bits * 100 + T)
+    y_ref, _ = _oracle_y(li, tokens=toks)
+    _assert_close(y_ref, first.float().cpu().numpy(), rows=toks)
+
+
 def test_ffn_is_deterministic():
     li = synth.layer_inputs(synth.TINY_LAYER.with_(tokens=40))
     y1, s1, call, stack = _run_gpu(li)
