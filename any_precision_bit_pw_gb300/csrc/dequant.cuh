@@ -22,6 +22,14 @@
 namespace pw {
 
 constexpr int kStageK = 64;                      // columns per pipeline stage
+
+// Shifts by a count known after unrolling (0 allowed).
+__device__ __forceinline__ uint32_t shl_mul(uint32_t x, int s) {
+  return x << s;
+}
+__device__ __forceinline__ uint32_t shr_mul(uint32_t x, int s) {
+  return x >> s;
+}
 constexpr int kLutRegionBytes = 65536;           // shared LUT region of a strip (q >= 5), 64 KB aligned
 
 // Nibble selector of 8 consecutive columns (sub-block js) from one word per
@@ -30,7 +38,11 @@ template <int P0, int P1>
 __device__ __forceinline__ uint32_t nibble_sel(const uint32_t* w, int js) {
   uint32_t s = 0u;
 #pragma unroll
-  for (int p = P0; p < P1; ++p) s |= ((w[p] >> js) & 0x11111111u) << (P1 - 1 - p);
+  for (int p = P0; p < P1; ++p) {
+    const int k = P1 - 1 - p, sh = js - k;   // bit js of each nibble -> bit k
+    const uint32_t t = sh >= 0 ? shr_mul(w[p], sh) : shl_mul(w[p], -sh);
+    s |= t & (0x11111111u << k);
+  }
   return s;
 }
 
@@ -130,24 +142,27 @@ struct RowDequant<Q, true> {
 // swaps, all four byte lanes at once): afterwards bit c of byte j of X[i]
 // holds what was bit i of byte j of X[c].
 __device__ __forceinline__ void transpose8x8(uint32_t (&X)[8]) {
+  // each exchange: the low part of a keeps its own bits and takes b's low
+  // part shifted up; b keeps its high part and takes a's high part shifted
+  // down (one shift and one three-input logic op per result)
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const uint32_t t = ((X[i] >> 4) ^ X[i + 4]) & 0x0F0F0F0Fu;
-    X[i + 4] ^= t;
-    X[i] ^= t << 4;
+    const uint32_t a = X[i], b = X[i + 4];
+    X[i] = (a & 0x0F0F0F0Fu) | (shl_mul(b, 4) & 0xF0F0F0F0u);
+    X[i + 4] = (shr_mul(a, 4) & 0x0F0F0F0Fu) | (b & 0xF0F0F0F0u);
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     if (i & 2) continue;
-    const uint32_t t = ((X[i] >> 2) ^ X[i + 2]) & 0x33333333u;
-    X[i + 2] ^= t;
-    X[i] ^= t << 2;
+    const uint32_t a = X[i], b = X[i + 2];
+    X[i] = (a & 0x33333333u) | (shl_mul(b, 2) & 0xCCCCCCCCu);
+    X[i + 2] = (shr_mul(a, 2) & 0x33333333u) | (b & 0xCCCCCCCCu);
   }
 #pragma unroll
   for (int i = 0; i < 8; i += 2) {
-    const uint32_t t = ((X[i] >> 1) ^ X[i + 1]) & 0x55555555u;
-    X[i + 1] ^= t;
-    X[i] ^= t << 1;
+    const uint32_t a = X[i], b = X[i + 1];
+    X[i] = (a & 0x55555555u) | (shl_mul(b, 1) & 0xAAAAAAAAu);
+    X[i + 1] = (shr_mul(a, 1) & 0x55555555u) | (b & 0xAAAAAAAAu);
   }
 }
 

@@ -286,9 +286,17 @@ inline int sm_count_cached() {
 
 // ---------------------------------------------------------------------------
 // Combine (whole CTA): y rows of one strip for every token, fixed order.
-// An item is one token and four consecutive rows (float4 partial sums); the
-// k x nsplit loads of an item are independent.
+// An item is one token and four consecutive rows (float4 partial sums).  For
+// each of the token's k slots, the partial sums of up to 8 K-splits are loaded
+// together (independent loads), then added in split order.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void add4(float4& a, const float4 v) {
+  a.x += v.x;
+  a.y += v.y;
+  a.z += v.z;
+  a.w += v.w;
+}
+
 __device__ inline void combine_strip(const Params& p, int strip, int tid, int nthreads) {
   const int n_items = p.T * 32;
   for (int it = tid; it < n_items; it += nthreads) {
@@ -299,14 +307,16 @@ __device__ inline void combine_strip(const Params& p, int strip, int tid, int nt
       const int slot = t * p.k + j;
       const int ps = __ldg(p.inv_perm + slot);
       const float wt = __ldg(p.w + slot);
+      const float4* base = reinterpret_cast<const float4*>(p.part + static_cast<long long>(ps) * p.H + row);
+      const long long sstride = static_cast<long long>(p.A) * p.H / 4;   // float4 per split
       float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int sp = 0; sp < p.nsplit; ++sp) {
-        const float4 v =
-            __ldcg(reinterpret_cast<const float4*>(p.part + (static_cast<long long>(sp) * p.A + ps) * p.H + row));
-        s.x += v.x;
-        s.y += v.y;
-        s.z += v.z;
-        s.w += v.w;
+      for (int sp0 = 0; sp0 < p.nsplit; sp0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          v[u] = sp0 + u < p.nsplit ? __ldcg(base + (sp0 + u) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) add4(s, v[u]);
       }
       acc.x += wt * s.x;
       acc.y += wt * s.y;

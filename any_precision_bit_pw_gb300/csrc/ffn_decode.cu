@@ -2,7 +2,7 @@
 // 128-row strip x 128-column tile of a block per pipeline step.  See
 // ffn_common.cuh for the work units and their scheduling.
 //
-// One CTA per SM (persistent), 26 warps in six roles:
+// One CTA per SM (persistent), 27 warps in seven roles:
 //   warps 0-15, dequant: four sets of four warps (one warp per TMEM lane
 //     quadrant, one thread per row of the strip); tile x of the CTA's tile
 //     stream goes to set x % 4.  A thread copies its row's 16 bytes of every
@@ -43,9 +43,10 @@ constexpr int kDeqWarpsAll = kSets * 4;           // warps 0-15
 constexpr int kMmaWarp0 = kDeqWarpsAll;           // warps 16-19: one MMA issuer per set
 constexpr int kEpiWarp0 = kMmaWarp0 + kSets;      // warps 20-23
 constexpr int kEpiThreads = 128;
-constexpr int kLoadWarp = kEpiWarp0 + 4;          // warp 24
+constexpr int kLoadWarp = kEpiWarp0 + 4;          // warp 24: plane chunks
 constexpr int kSchedWarp = kLoadWarp + 1;         // warp 25
-constexpr int kThreads = (kSchedWarp + 1) * 32;   // 832
+constexpr int kBLoadWarp = kSchedWarp + 1;        // warp 26: B operands
+constexpr int kThreads = (kBLoadWarp + 1) * 32;   // 864
 constexpr int kSA = 6;                            // TMEM A slots
 constexpr int kATileCols = 64;                    // TMEM columns per A tile (128 fp16 per row)
 constexpr int kDCol0 = kSA * kATileCols;          // accumulators: [buffer][set] x kN columns from here
@@ -55,22 +56,25 @@ constexpr int kUS = 4;                            // unit slots
 constexpr int kBS = 6;                            // B ring slots
 constexpr int kBAtom = kN * 128;                  // 16 rows x 64 fp16, 128-byte swizzle
 constexpr int kBBytes = 2 * kBAtom;               // B of one tile
-constexpr int kPSlots = 16;                       // plane ring: 2 x 8-byte slots per thread
-constexpr int kPRingBytes = kPSlots * pw::kTileBytes;   // per set
+constexpr int kPS = 4;                            // plane chunk slots
+constexpr int kPSlotBytes = 32768;                // one chunk: up to 4 tiles x 4 planes or 2 tiles x 8 planes
 constexpr int kSmemBytes = 232448;
 constexpr uint32_t kHintNs = 20000;
 static_assert(kDCol0 + 2 * kSets * kN <= kTmemCols, "TMEM columns");
 static_assert(kSA <= kF && 2 * kBS <= kF, "barrier reuse distances");
-static_assert(kPSlots >= 2 * PW_MAX_BITS, "two tiles of the widest bitwidth in flight");
+static_assert(4 * 4 * 2048 <= kPSlotBytes && 2 * 8 * 2048 <= kPSlotBytes, "chunk sizes");
 
 enum : int {
   kBarAFull = 0,                  // [kF]  A slot written (4 warps of a set)
   kBarTFree = kF,                 // [kF]  tile's MMAs done (tcgen05.commit)
   kBarBFull = 2 * kF,             // [kBS] B slot loaded (transaction bytes)
-  kBarDone = 2 * kF + kBS,        // [2]   unit's accumulators complete (one arrival per set issuer)
+  kBarPFull = 2 * kF + kBS,       // [kPS] plane chunk loaded (transaction bytes)
+  kBarPFree = kBarPFull + kPS,    // [kPS] plane chunk consumed (16 dequant warps)
+  kBarDone = kBarPFree + kPS,     // [2]   unit's accumulators complete (one arrival per set issuer)
   kBarDFree = kBarDone + 2,       // [2]   accumulator read (4 epilogue warps)
   kBarRegReady = kBarDFree + 2,   // [2]   region half written for the unit (4 epilogue warps)
-  kBarEpiDone = kBarRegReady + 2,
+  kBarQ8Fill = kBarRegReady + 2,  // q = 8 region written by the dequant warps themselves (16 warps)
+  kBarEpiDone = kBarQ8Fill + 1,
   kBarEpiGo = kBarEpiDone + 1,
   kBarUReady = kBarEpiGo + 1,     // [kUS]
   kBarUFree = kBarUReady + kUS,   // [kUS]
@@ -78,13 +82,15 @@ enum : int {
 };
 constexpr int kBarBytes = 512;
 static_assert(kNumBars * 8 <= kBarBytes, "barrier area");
-constexpr uint32_t kUnitFreeCount = kDeqWarpsAll + kSets + 4 + 1;
+constexpr uint32_t kUnitFreeCount = kDeqWarpsAll + kSets + 4 + 2;
 
 struct DecState {
   Shared sched;                              // ticket decoding state (scheduler thread)
   Unit units[kUS];                           // published units
   const uint32_t* planes[kUS][PW_MAX_BITS];  // each published unit's first tile, per plane
   uint32_t deq_done;                         // units finished, summed over the 16 dequant warps
+  uint32_t bring;                            // B ring (shared address)
+  uint32_t pslot[kPS];                       // plane chunk slots (shared addresses)
   int combine;
   int abort;                                 // CTA-wide: give up waiting
 };
@@ -92,12 +98,10 @@ struct DecState {
 struct Sm {
   uint32_t bar;              // first barrier (shared address)
   uint32_t region;           // 64 KB-aligned LUT region (q >= 5)
-  uint32_t bring;            // B ring
-  uint32_t pring[kSets];     // plane rings
-  DecState* st;
+  DecState* st;              // also holds the B ring and plane slot addresses
 };
 
-__device__ __forceinline__ uint32_t bar(const Sm& sm, int i) { return sm.bar + 8u * static_cast<uint32_t>(i); }
+__device__ __forceinline__ uint32_t bar(const Sm sm, int i) { return sm.bar + 8u * static_cast<uint32_t>(i); }
 
 __device__ __forceinline__ void fail(const Params& p, DecState& st) {
   st.abort = 1;
@@ -106,7 +110,7 @@ __device__ __forceinline__ void fail(const Params& p, DecState& st) {
 }
 
 // Bounded wait for phase `parity`; gives up early once the CTA aborts.
-__device__ __forceinline__ bool wait_bar(const Sm& sm, int i, uint32_t parity, const Params& p) {
+__device__ __forceinline__ bool wait_bar(const Sm sm, int i, uint32_t parity, const Params& p) {
   const uint32_t b = bar(sm, i);
   if (pw::mbar_try_wait_hint(b, parity, kHintNs)) return true;
   const uint64_t t0 = pw::global_ns();
@@ -123,14 +127,14 @@ __device__ __forceinline__ bool wait_bar(const Sm& sm, int i, uint32_t parity, c
 
 // Bounded wait that ignores the abort flag (copies and MMAs already issued
 // must land before the CTA exits).
-__device__ __forceinline__ void drain_bar(const Sm& sm, int i, uint32_t parity) {
+__device__ __forceinline__ void drain_bar(const Sm sm, int i, uint32_t parity) {
   const uint64_t t0 = pw::global_ns();
   while (!pw::mbar_try_wait_hint(bar(sm, i), parity, kHintNs))
     if (pw::global_ns() - t0 > 100000000ull) return;
 }
 
 // Bounded wait until a shared counter reaches `target`.
-__device__ __forceinline__ bool wait_count(const Sm& sm, const uint32_t* ctr, uint32_t target, const Params& p) {
+__device__ __forceinline__ bool wait_count(const Sm sm, const uint32_t* ctr, uint32_t target, const Params& p) {
   const volatile uint32_t* c = ctr;
   if (*c >= target) {
     __threadfence_block();
@@ -151,164 +155,127 @@ __device__ __forceinline__ bool wait_count(const Sm& sm, const uint32_t* ctr, ui
 }
 
 // Lane 0 waits for unit i to be published; the warp then reads it.
-__device__ __forceinline__ bool wait_unit(const Sm& sm, uint32_t i, const Params& p) {
+__device__ __forceinline__ bool wait_unit(const Sm sm, uint32_t i, const Params& p) {
   int ok = 1;
   if ((threadIdx.x & 31) == 0) ok = wait_bar(sm, kBarUReady + static_cast<int>(i % kUS), (i / kUS) & 1u, p);
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-__device__ __forceinline__ void cp_async_wait_dyn(int n) {
-  switch (n) {
-    case 0: pw::cp_async_wait<0>(); break;
-    case 1: pw::cp_async_wait<1>(); break;
-    case 2: pw::cp_async_wait<2>(); break;
-    case 3: pw::cp_async_wait<3>(); break;
-    case 4: pw::cp_async_wait<4>(); break;
-    case 5: pw::cp_async_wait<5>(); break;
-    case 6: pw::cp_async_wait<6>(); break;
-    default: pw::cp_async_wait<7>(); break;
-  }
-}
-
 // ---------------------------------------------------------------------------
 // dequant warps
 // ---------------------------------------------------------------------------
-// A thread's plane-copy cursor over its set's tiles, across units.
-struct PlaneLoads {
-  uint32_t head, tail;   // ring slots taken / given back
-  uint32_t li, lx0;      // unit being copied and its first tile in the CTA's stream
-  int lt;                // its next tile for this set (unit-relative)
-  int ahead;             // tiles copied (commit groups) not yet consumed
-  bool end;
-};
-
-// Copy the next tile of this set (all committed planes, this thread's row);
-// false when the ring is full, the next unit is not published yet (unless
-// `block`) or there are no more units.
-__device__ __forceinline__ bool issue_next(PlaneLoads& L, const Sm& sm, int set, int pos, uint32_t ring, bool block,
-                                           const Params& p) {
-  const DecState& st = *sm.st;
-  while (!L.end) {
-    const int us = static_cast<int>(L.li % kUS);
-    const uint32_t par = (L.li / kUS) & 1u;
-    if (!pw::mbar_test(bar(sm, kBarUReady + us), par)) {
-      if (!block) return false;
-      if (!wait_bar(sm, kBarUReady + us, par, p)) {
-        L.end = true;
-        return false;
-      }
-    }
-    const Unit& u = st.units[us];
-    if (u.kind == kNone) {
-      L.end = true;
-      return false;
-    }
-    const int nt = u.nst / 2;
-    if (L.lt >= nt) {
-      L.lx0 += static_cast<uint32_t>(nt);
-      ++L.li;
-      L.lt = static_cast<int>((static_cast<uint32_t>(set) - L.lx0) & 3u);
-      continue;
-    }
-    const int q = u.q;
-    if (L.head + static_cast<uint32_t>(q) - L.tail > static_cast<uint32_t>(kPSlots)) return false;
-    // slot layout: [half][pos][8 bytes] so that a warp reads 256 contiguous
-    // bytes per half
-    const long long off = static_cast<long long>(L.lt) * (pw::kTileBytes / 4) + pos * 4;
-    for (int pl = 0; pl < q; ++pl) {
-      const uint32_t dst = ring + ((L.head + pl) % kPSlots) * pw::kTileBytes + pos * 8;
-      const uint32_t* src = st.planes[us][pl] + off;
-      pw::cp_async_8(dst, src);
-      pw::cp_async_8(dst + pw::kTileBytes / 2, src + 2);
-    }
-    pw::cp_async_commit();
-    L.head += static_cast<uint32_t>(q);
-    ++L.ahead;
-    L.lt += kSets;
-    return true;
-  }
-  return false;
-}
+// Plane chunks: the loader copies a unit's tiles in chunks of consecutive
+// tiles (4 for q <= 4, 2 for q >= 5; at most 32 KB), one bulk copy per plane,
+// into kPS fixed slots.  Slot layout: [plane][tile of the chunk][row pos][16 B],
+// plane stride chunk_tiles * 2 KB.  Every dequant warp waits for each chunk
+// and signals it consumed, whether or not its set has a tile in it.
+__host__ __device__ constexpr int chunk_tiles(int q) { return q <= 4 ? 4 : 2; }
 
 template <int Q>
-__device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, const Sm& sm, uint32_t tmem, uint32_t x0,
-                                             uint32_t ui, PlaneLoads& L) {
+__device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, const Sm sm, uint32_t tmem, uint32_t x0,
+                                             uint32_t c0, uint32_t ui, uint32_t n8) {
+  constexpr int kCt = chunk_tiles(Q);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int set = warp >> 2, qd = warp & 3;
   const int pos = qd * 32 + lane;
-  const uint32_t ring = sm.pring[set];
   bool ok = true;
   pw::RowDequant<Q> dq;
+  // the unit's LUT is in region half ui & 1 (written one unit ahead)
+  ok = wait_bar(sm, kBarRegReady + static_cast<int>(ui & 1u), (ui >> 1) & 1u, p);
   if constexpr (Q <= 4) {
-    const BlockDesc& d = *u.d;
-    const int row = strip_pos_row(u.strip, pos, d.rows / 2);
-    dq.load(d.lut + static_cast<long long>(row) * (1 << Q), 0u, lane);
+    if (ok) dq.load_shared(sm.region + (ui & 1u) * 32768u + static_cast<uint32_t>(pos) * 32u);
   } else {
     dq.set_row(sm.region, qd, lane, static_cast<int>(ui & 1u));
-    ok = wait_bar(sm, kBarRegReady + static_cast<int>(ui & 1u), (ui >> 1) & 1u, p);
   }
-  const uint32_t nt = static_cast<uint32_t>(u.nst / 2);
-  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
-  for (uint32_t x = x0 + ((static_cast<uint32_t>(set) - x0) & 3u); ok && x < x0 + nt; x += kSets) {
-    if (L.ahead == 0 && !issue_next(L, sm, set, pos, ring, true, p)) break;
-    while (issue_next(L, sm, set, pos, ring, false, p)) {
-    }
-    cp_async_wait_dyn(L.ahead - 1);
-    const uint32_t slot0 = L.tail;
-    L.tail += Q;
-    --L.ahead;
-    const int fs = static_cast<int>(x % kF);
-    if (x >= kSA && !wait_bar(sm, kBarTFree + static_cast<int>((x - kSA) % kF), ((x - kSA) / kF) & 1u, p)) break;
-    pw::tc_fence_after();
-    const uint32_t acol = tl + (x % kSA) * kATileCols;
+  if constexpr (Q == 8) {
+    // a q = 8 table takes the whole region, so it cannot be written ahead:
+    // the LUT warps only confirmed that every unit before this one is done;
+    // the 16 dequant warps write it (this thread: 64 entries of its row)
+    if (ok) {
+      const BlockDesc& d = *u.d;
+      const int row = strip_pos_row(u.strip, pos, d.rows / 2);
+      const uint4* src = reinterpret_cast<const uint4*>(d.lut + (static_cast<long long>(row) << 8)) + set * 8;
+      uint4 a[8];
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      uint32_t w2[Q][2];
+      for (int j = 0; j < 8; ++j) a[j] = __ldg(src + j);
 #pragma unroll
-      for (int q = 0; q < Q; ++q)
-        pw::lds_v2(ring + ((slot0 + q) % kPSlots) * pw::kTileBytes + hh * (pw::kTileBytes / 2) + pos * 8, w2[q][0],
-                   w2[q][1]);
+      for (int j = 0; j < 8; ++j) {
+        const uint32_t av[4] = {a[j].x, a[j].y, a[j].z, a[j].w};
 #pragma unroll
-      for (int wd = 0; wd < 2; ++wd) {
-        uint32_t ww[Q];
-#pragma unroll
-        for (int q = 0; q < Q; ++q) ww[q] = w2[q][wd];
-        uint32_t out[16];
-        dq.word(ww, out);
-        pw::tmem_st_x16(acol + 16 * (2 * hh + wd), out);
+        for (int i = 0; i < 4; ++i) {
+          const uint32_t cc = static_cast<uint32_t>(set * 64 + j * 8 + 2 * i);
+          pw::sts_u16(dq.tblw + cc * 256u, av[i] & 0xFFFFu);
+          pw::sts_u16(dq.tblw + (cc + 1u) * 256u, av[i] >> 16);
+        }
       }
     }
-    pw::tmem_st_wait();
-    pw::tc_fence_before();
     __syncwarp();
-    if (lane == 0) pw::mbar_arrive(bar(sm, kBarAFull + fs));
+    if (lane == 0) pw::mbar_arrive(bar(sm, kBarQ8Fill));
+    ok = wait_bar(sm, kBarQ8Fill, n8 & 1u, p) && ok;
+  }
+  const int nt = u.nst / 2;
+  const int nch = (nt + kCt - 1) / kCt;
+  const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+  for (int k = 0; k < nch; ++k) {
+    const uint32_t c = c0 + static_cast<uint32_t>(k);
+    const int ps = static_cast<int>(c % kPS);
+    const int n_in = min(kCt, nt - k * kCt);
+    const uint32_t xs = x0 + static_cast<uint32_t>(k * kCt);
+    const int j = static_cast<int>((static_cast<uint32_t>(set) - xs) & 3u);   // this set's tile in the chunk
+    const bool has = ok && j < n_in;
+    if (ok) ok = wait_bar(sm, kBarPFull + ps, (c / kPS) & 1u, p);
+    if (has && ok) {
+      const uint32_t x = xs + static_cast<uint32_t>(j);
+      if (x >= kSA && !wait_bar(sm, kBarTFree + static_cast<int>((x - kSA) % kF), ((x - kSA) / kF) & 1u, p))
+        ok = false;
+      if (ok) {
+        pw::tc_fence_after();
+        const uint32_t acol = tl + (x % kSA) * kATileCols;
+        const uint32_t src = sm.st->pslot[ps] + static_cast<uint32_t>(j) * pw::kTileBytes + pos * 16;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t w2[Q][2];
+#pragma unroll
+          for (int q = 0; q < Q; ++q) pw::lds_v2(src + q * (kCt * pw::kTileBytes) + hh * 8, w2[q][0], w2[q][1]);
+#pragma unroll
+          for (int wd = 0; wd < 2; ++wd) {
+            uint32_t ww[Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) ww[q] = w2[q][wd];
+            uint32_t out[16];
+            dq.word(ww, out);
+            pw::tmem_st_x16(acol + 16 * (2 * hh + wd), out);
+          }
+        }
+        pw::tmem_st_wait();
+        pw::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) pw::mbar_arrive(bar(sm, kBarAFull + static_cast<int>(x % kF)));
+      }
+    }
+    __syncwarp();
+    if (lane == 0) pw::mbar_arrive(bar(sm, kBarPFree + ps));   // this warp is done with the chunk
   }
 }
 
-__device__ void dequant_role(const Params& p, const Sm& sm, uint32_t tmem) {
-  const int set = (threadIdx.x >> 5) >> 2;
-  PlaneLoads L;
-  L.head = L.tail = 0;
-  L.li = 0;
-  L.lx0 = 0;
-  L.lt = set;
-  L.ahead = 0;
-  L.end = false;
-  uint32_t x = 0;
+__device__ __forceinline__ void dequant_role(const Params& p, const Sm sm, uint32_t tmem) {
+  uint32_t x = 0, c = 0, n8 = 0;
   for (uint32_t i = 0;; ++i) {
     if (!wait_unit(sm, i, p)) break;
     const Unit& u = sm.st->units[i % kUS];
     if (u.kind == kNone) break;
     switch (u.q) {
-      case 2: dequant_unit<2>(p, u, sm, tmem, x, i, L); break;
-      case 3: dequant_unit<3>(p, u, sm, tmem, x, i, L); break;
-      case 4: dequant_unit<4>(p, u, sm, tmem, x, i, L); break;
-      case 5: dequant_unit<5>(p, u, sm, tmem, x, i, L); break;
-      case 6: dequant_unit<6>(p, u, sm, tmem, x, i, L); break;
-      case 7: dequant_unit<7>(p, u, sm, tmem, x, i, L); break;
-      default: dequant_unit<8>(p, u, sm, tmem, x, i, L); break;
+      case 2: dequant_unit<2>(p, u, sm, tmem, x, c, i, n8); break;
+      case 3: dequant_unit<3>(p, u, sm, tmem, x, c, i, n8); break;
+      case 4: dequant_unit<4>(p, u, sm, tmem, x, c, i, n8); break;
+      case 5: dequant_unit<5>(p, u, sm, tmem, x, c, i, n8); break;
+      case 6: dequant_unit<6>(p, u, sm, tmem, x, c, i, n8); break;
+      case 7: dequant_unit<7>(p, u, sm, tmem, x, c, i, n8); break;
+      default: dequant_unit<8>(p, u, sm, tmem, x, c, i, n8++); break;
     }
-    x += static_cast<uint32_t>(u.nst / 2);
+    const int nt = u.nst / 2, ct = chunk_tiles(u.q);
+    x += static_cast<uint32_t>(nt);
+    c += static_cast<uint32_t>((nt + ct - 1) / ct);
     __syncwarp();
     if ((threadIdx.x & 31) == 0) {
       // a monotonic count, not a barrier phase: the LUT writers may look at it
@@ -318,63 +285,107 @@ __device__ void dequant_role(const Params& p, const Sm& sm, uint32_t tmem) {
       pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(i % kUS)));
     }
   }
-  pw::cp_async_wait<0>();   // every plane copy lands before the CTA exits
 }
 
 // ---------------------------------------------------------------------------
-// loader (one thread): B operands and LUT prefetch
+// plane loader warp: plane chunks and LUT prefetch (lane 0 waits and signals;
+// lanes issue one bulk copy per plane)
 // ---------------------------------------------------------------------------
-__device__ void loader_role(const Params& p, const Sm& sm, const void* map_gu, const void* map_dn) {
+__device__ __forceinline__ void plane_loader_role(const Params& p, const Sm sm) {
+  const int lane = threadIdx.x & 31;
+  DecState& st = *sm.st;
+  uint32_t c = 0;
+  bool ok = true;
+  for (uint32_t u = 0; ok; ++u) {
+    if (!wait_unit(sm, u, p)) break;
+    const int us = static_cast<int>(u % kUS);
+    const Unit& un = st.units[us];
+    if (un.kind == kNone) break;
+    const BlockDesc& d = *un.d;
+    const int Q = un.q, ct = chunk_tiles(Q), nt = un.nst / 2;
+    if (lane < 2) {
+      // the unit's LUT rows (two runs of 64 rows) into L2 for the LUT writers
+      const long long rowb = static_cast<long long>(2) << Q;
+      const long long r0 = (lane == 0 ? 0ll : static_cast<long long>(d.rows / 2)) + un.strip * 64;
+      pw::prefetch_l2(reinterpret_cast<const char*>(d.lut) + r0 * rowb, static_cast<uint32_t>(64 * rowb));
+    }
+    const uint32_t* plane = lane < Q ? st.planes[us][lane] : nullptr;
+    for (int t0 = 0; t0 < nt; t0 += ct, ++c) {
+      const int n_in = min(ct, nt - t0);
+      const int ps = static_cast<int>(c % kPS);
+      const uint32_t fb = bar(sm, kBarPFull + ps);
+      int r = 1;
+      if (lane == 0) {
+        // the slot's previous chunk must be consumed by every dequant warp
+        if (c >= kPS) r = wait_bar(sm, kBarPFree + ps, ((c - kPS) / kPS) & 1u, p);
+        if (r) pw::mbar_arrive_expect_tx(fb, static_cast<uint32_t>(Q * n_in) * pw::kTileBytes);
+      }
+      if (!__shfl_sync(0xffffffffu, r, 0)) {
+        ok = false;
+        break;
+      }
+      if (lane < Q)
+        pw::bulk_g2s(st.pslot[ps] + static_cast<uint32_t>(lane * ct) * pw::kTileBytes,
+                     plane + static_cast<long long>(t0) * (pw::kTileBytes / 4),
+                     static_cast<uint32_t>(n_in) * pw::kTileBytes, fb);
+    }
+    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(u % kUS)));
+  }
+  // the last copies land before the CTA exits
+  if (lane == 0)
+    for (uint32_t y = c > static_cast<uint32_t>(kPS) ? c - kPS : 0u; y < c; ++y)
+      drain_bar(sm, kBarPFull + static_cast<int>(y % kPS), (y / kPS) & 1u);
+  __syncwarp();
+}
+
+// ---------------------------------------------------------------------------
+// B loader (one thread): each tile's 16 token rows, two tensor-map boxes
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void b_loader_role(const Params& p, const Sm sm, const void* map_gu, const void* map_dn) {
   DecState& st = *sm.st;
   bool gathered = p.linear != 0;
   uint32_t x = 0;
-  for (uint32_t u = 0;; ++u) {
+  bool ok = true;
+  for (uint32_t u = 0; ok; ++u) {
     if (!wait_bar(sm, kBarUReady + static_cast<int>(u % kUS), (u / kUS) & 1u, p)) break;
     const Unit& un = st.units[u % kUS];
     if (un.kind == kNone) break;
-    const BlockDesc& d = *un.d;
-    // the unit's LUT rows (two runs of 64 rows) into L2 for the LUT readers
-    const long long rowb = static_cast<long long>(2) << un.q;
-    const char* lut = reinterpret_cast<const char*>(d.lut);
-    pw::prefetch_l2(lut + un.strip * 64 * rowb, static_cast<uint32_t>(64 * rowb));
-    pw::prefetch_l2(lut + (static_cast<long long>(d.rows / 2) + un.strip * 64) * rowb, static_cast<uint32_t>(64 * rowb));
     if (un.kind == kGateUp && !gathered) {
       const uint64_t t0 = pw::global_ns();
-      bool g = true;
       while (pw::ld_acquire_gpu(p.gather_ctr) < gridDim.x) {
         if (st.abort || pw::global_ns() - t0 > p.wait_ns) {
           if (!st.abort) fail(p, st);
-          g = false;
+          ok = false;
           break;
         }
         __nanosleep(100);
       }
-      if (!g) break;
+      if (!ok) break;
       gathered = true;
     }
     if (un.kind != kLinear) pw::fence_proxy_async_global();   // x / h rows written by this kernel
     const void* map = un.kind == kDown ? map_dn : map_gu;
     const int brow = un.kind == kLinear ? un.tg * kN : un.off;
-    const int tile0 = un.st0 / 2, ntl = un.nst / 2;
-    bool ok = true;
-    for (int t = 0; t < ntl; ++t, ++x) {
+    const int tile0 = un.st0 / 2, nt = un.nst / 2;
+    for (int t = 0; t < nt; ++t, ++x) {
       const int b = static_cast<int>(x % kBS);
-      const uint32_t fb = bar(sm, kBarBFull + b);
+      const uint32_t bb = bar(sm, kBarBFull + b);
       // the slot's previous tile (x - kBS) must be consumed by its MMAs
       if (x >= kBS && !wait_bar(sm, kBarTFree + static_cast<int>((x - kBS) % kF), ((x - kBS) / kF) & 1u, p)) {
         ok = false;
         break;
       }
-      pw::mbar_arrive_expect_tx(fb, kBBytes);
-      const uint32_t dst = sm.bring + static_cast<uint32_t>(b) * kBBytes;
+      pw::mbar_arrive_expect_tx(bb, kBBytes);
+      const uint32_t dst = st.bring + static_cast<uint32_t>(b) * kBBytes;
       const int col = (tile0 + t) * pw::kTileCols;
-      pw::tma_load_2d(dst, map, col, brow, fb);
-      pw::tma_load_2d(dst + kBAtom, map, col + 64, brow, fb);
+      pw::tma_load_2d(dst, map, col, brow, bb);
+      pw::tma_load_2d(dst + kBAtom, map, col + 64, brow, bb);
     }
     if (!ok) break;
     pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(u % kUS)));
   }
-  // the last copies land before the CTA exits
   for (uint32_t y = x > static_cast<uint32_t>(kBS) ? x - kBS : 0u; y < x; ++y)
     drain_bar(sm, kBarBFull + static_cast<int>(y % kBS), (y / kBS) & 1u);
 }
@@ -382,7 +393,7 @@ __device__ void loader_role(const Params& p, const Sm& sm, const void* map_gu, c
 // ---------------------------------------------------------------------------
 // MMA issuers: one thread per set, its own accumulators
 // ---------------------------------------------------------------------------
-__device__ void mma_role(const Params& p, const Sm& sm, uint32_t tmem, int set) {
+__device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t tmem, int set) {
   DecState& st = *sm.st;
   const uint32_t idesc = pw::idesc_f16_f32(128, kN);
   uint32_t x0 = 0;
@@ -406,7 +417,7 @@ __device__ void mma_role(const Params& p, const Sm& sm, uint32_t tmem, int set) 
       }
       pw::tc_fence_after();
       const uint32_t a = tmem + (x % kSA) * kATileCols;
-      const uint32_t bsm = sm.bring + static_cast<uint32_t>(b) * kBBytes;
+      const uint32_t bsm = sm.st->bring + static_cast<uint32_t>(b) * kBBytes;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
         const uint64_t bdesc = pw::sdesc_kmajor_sw128(bsm + (j >> 2) * kBAtom) + 2ull * (j & 3);
@@ -437,7 +448,7 @@ __device__ void mma_role(const Params& p, const Sm& sm, uint32_t tmem, int set) 
 // half ready (also for q <= 4, which keeps the barrier phases one per unit).
 // Returns 1 when done, 0 when unit i is the end marker, and -1 without
 // waiting when `block` is false and unit i is not published yet.
-__device__ int lut_fill(const Params& p, const Sm& sm, uint32_t i, bool& prev_q8, bool block) {
+__device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i, bool& prev_q8, bool block) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (!block) {
     int pub = 0;
@@ -453,7 +464,28 @@ __device__ int lut_fill(const Params& p, const Sm& sm, uint32_t i, bool& prev_q8
   // i or i - 1 takes the whole region, are finished by every dequant warp
   const uint32_t need = static_cast<uint32_t>(kDeqWarpsAll) * ((u.q == 8 || prev_q8) ? i : (i >= 1 ? i - 1 : 0u));
   const bool ok = wait_count(sm, &sm.st->deq_done, need, p);
-  if (ok && u.q >= 5) {
+  if (ok && u.q <= 4) {
+    // q <= 4: the row's table (at most 32 bytes), row-major at the start of
+    // the half; the dequant threads load it into registers
+    const BlockDesc& d = *u.d;
+    const int row = strip_pos_row(u.strip, pos, d.rows / 2);
+    const uint4* src = reinterpret_cast<const uint4*>(d.lut + (static_cast<long long>(row) << u.q));
+    const uint32_t dst = sm.region + static_cast<uint32_t>(h) * 32768u + static_cast<uint32_t>(pos) * 32u;
+    if (u.q == 2) {
+      const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(v.x), "r"(v.y) : "memory");
+    } else {
+      const uint4 v = __ldg(src);
+      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                   : "memory");
+      if (u.q == 4) {
+        const uint4 v2 = __ldg(src + 1);
+        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16), "r"(v2.x), "r"(v2.y), "r"(v2.z),
+                     "r"(v2.w)
+                     : "memory");
+      }
+    }
+  } else if (ok && u.q < 8) {
     const BlockDesc& d = *u.d;
     const int row = strip_pos_row(u.strip, pos, d.rows / 2);
     const uint16_t* lut = d.lut + (static_cast<long long>(row) << u.q);
@@ -462,8 +494,7 @@ __device__ int lut_fill(const Params& p, const Sm& sm, uint32_t i, bool& prev_q8
     switch (u.q) {
       case 5: pw::region_fill<5>(tblw, lut, h); break;
       case 6: pw::region_fill<6>(tblw, lut, h); break;
-      case 7: pw::region_fill<7>(tblw, lut, h); break;
-      default: pw::region_fill<8>(tblw, lut, h); break;
+      default: pw::region_fill<7>(tblw, lut, h); break;
     }
   }
   prev_q8 = u.q == 8;
@@ -472,7 +503,7 @@ __device__ int lut_fill(const Params& p, const Sm& sm, uint32_t i, bool& prev_q8
   return 1;
 }
 
-__device__ void epilogue_unit(const Params& p, const Sm& sm, uint32_t tmem, uint32_t i, uint32_t x0) {
+__device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint32_t tmem, uint32_t i, uint32_t x0) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qd = warp & 3;
   const int pos = qd * 32 + lane;
@@ -541,12 +572,21 @@ __device__ void epilogue_unit(const Params& p, const Sm& sm, uint32_t tmem, uint
 // role never waits for a publication before finishing the current unit's
 // epilogue (the scheduler may be waiting, for a down unit, on exactly that
 // epilogue's gate_up completion).
-__device__ void epilogue_role(const Params& p, const Sm& sm, uint32_t tmem) {
+__device__ __forceinline__ void epilogue_role(const Params& p, const Sm sm, uint32_t tmem) {
   bool prev_q8 = false;
   int more = lut_fill(p, sm, 0, prev_q8, true);
   uint32_t x0 = 0;
   for (uint32_t i = 0; more == 1; ++i) {
+    // fill the next unit's table as soon as it is published, but do not wait
+    // for its publication past the moment this unit's accumulators are ready
     int next = lut_fill(p, sm, i + 1, prev_q8, false);
+    while (next < 0) {
+      int done = 0;
+      if ((threadIdx.x & 31) == 0) done = pw::mbar_test(bar(sm, kBarDone + static_cast<int>(i & 1u)), (i >> 1) & 1u);
+      if (__shfl_sync(0xffffffffu, done, 0) || sm.st->abort) break;
+      __nanosleep(128);
+      next = lut_fill(p, sm, i + 1, prev_q8, false);
+    }
     const uint32_t nt = static_cast<uint32_t>(sm.st->units[i % kUS].nst / 2);
     epilogue_unit(p, sm, tmem, i, x0);
     x0 += nt;
@@ -558,7 +598,7 @@ __device__ void epilogue_role(const Params& p, const Sm& sm, uint32_t tmem) {
 // ---------------------------------------------------------------------------
 // scheduler (one thread)
 // ---------------------------------------------------------------------------
-__device__ void scheduler_role(const Params& p, const Sm& sm) {
+__device__ __forceinline__ void scheduler_role(const Params& p, const Sm sm) {
   DecState& st = *sm.st;
   for (uint32_t i = 0;; ++i) {
     const int s = static_cast<int>(i % kUS);
@@ -606,13 +646,18 @@ __device__ __forceinline__ bool carve(Sm& sm, uint8_t* smem_raw) {
     }
     return false;
   };
-  bool ok = take(kBS * kBBytes, sm.bring);
-  for (int s = 0; s < kSets; ++s) ok = ok && take(kPRingBytes, sm.pring[s]);
+  uint32_t bring = 0, pslot[kPS] = {};
+  bool ok = take(kBS * kBBytes, bring);
+  for (int s = 0; s < kPS; ++s) ok = ok && take(kPSlotBytes, pslot[s]);
+  if (threadIdx.x == 0) {
+    sm.st->bring = bring;
+    for (int s = 0; s < kPS; ++s) sm.st->pslot[s] = pslot[s];
+  }
   return ok && sm.region + static_cast<uint32_t>(pw::kLutRegionBytes) <= end;
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    apl_decode_kernel(const Params p, const __grid_constant__ CUtensorMap map_gu,
+    apl_decode_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap map_gu,
                       const __grid_constant__ CUtensorMap map_dn) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   Sm sm;
@@ -628,11 +673,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       pw::mbar_init(bar(sm, kBarTFree + i), 1);
     }
     for (int i = 0; i < kBS; ++i) pw::mbar_init(bar(sm, kBarBFull + i), 1);
+    for (int i = 0; i < kPS; ++i) {
+      pw::mbar_init(bar(sm, kBarPFull + i), 1);
+      pw::mbar_init(bar(sm, kBarPFree + i), kDeqWarpsAll);
+    }
     for (int i = 0; i < 2; ++i) {
       pw::mbar_init(bar(sm, kBarDone + i), kSets);
       pw::mbar_init(bar(sm, kBarDFree + i), 4);
       pw::mbar_init(bar(sm, kBarRegReady + i), 4);
     }
+    pw::mbar_init(bar(sm, kBarQ8Fill), kDeqWarpsAll);
     pw::mbar_init(bar(sm, kBarEpiDone), 4);
     pw::mbar_init(bar(sm, kBarEpiGo), 1);
     for (int s = 0; s < kUS; ++s) {
@@ -649,7 +699,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     pw::tmem_alloc(pw::smem_u32(&st.sched.tmem), kTmemCols);
     pw::tmem_relinquish();
   }
-  if (warp == kLoadWarp && lane == 0) {
+  if (warp == kBLoadWarp && lane == 0) {
     pw::prefetch_tmap(&map_gu);
     if (!p.linear) pw::prefetch_tmap(&map_dn);
   }
@@ -682,9 +732,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp < kLoadWarp) {
     epilogue_role(p, sm, tmem);
   } else if (warp == kLoadWarp) {
-    if (lane == 0) loader_role(p, sm, &map_gu, &map_dn);
+    plane_loader_role(p, sm);
+  } else if (warp == kSchedWarp) {
+    if (lane == 0) scheduler_role(p, sm);
   } else if (lane == 0) {
-    scheduler_role(p, sm);
+    b_loader_role(p, sm, &map_gu, &map_dn);
   }
   pw::tc_fence_before();
   __syncthreads();

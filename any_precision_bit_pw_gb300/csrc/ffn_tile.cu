@@ -271,7 +271,7 @@ __device__ void producer_role(const Params& p, const Unit& u, const Smem& sm, ui
 }
 
 template <int NMAX, int G>
-__global__ void __launch_bounds__(Cfg<NMAX, G>::kThreads, 1) apl_tc_kernel(Params p) {
+__global__ void __launch_bounds__(Cfg<NMAX, G>::kThreads, 1) apl_tc_kernel(const __grid_constant__ Params p) {
   using C = Cfg<NMAX, G>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // carve up dynamic shared memory around a 64 KB-aligned LUT region

@@ -140,9 +140,12 @@ __device__ __forceinline__ void lds_v4u(uint32_t addr, uint32_t (&v)[4]) {
 __device__ __forceinline__ void lds_v2(uint32_t addr, uint32_t& a, uint32_t& b) {
   asm volatile("ld.shared.v2.u32 {%0, %1}, [%2];" : "=r"(a), "=r"(b) : "r"(addr));
 }
+// 16-bit shared load, zero-extended into a 32-bit register.  Not volatile: a
+// caller's address must depend on data read after the writes it needs (the
+// LUT lookups' addresses come from the plane words).
 __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr));
+  uint32_t v;
+  asm("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
 __device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v) {
