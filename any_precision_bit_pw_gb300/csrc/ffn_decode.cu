@@ -5,27 +5,30 @@
 // One CTA per SM (persistent), 27 warps in seven roles:
 //   warps 0-15, dequant: four sets of four warps (one warp per TMEM lane
 //     quadrant, one thread per row of the strip); tile x of the CTA's tile
-//     stream goes to set x % 4.  A thread copies its row's 16 bytes of every
-//     committed plane of its set's coming tiles into its own slots of the
-//     set's ring (cp.async; it is the only reader of those slots, so no
-//     barrier guards them), turns the row's 128 columns into fp16 through its
-//     LUT (dequant.cuh) and stores them as operand A in one of six TMEM slots;
-//   warp 16, loader: copies each tile's B operand (the 16 tokens' x or h
-//     columns: two 2-D tensor-map boxes in the 128-byte-swizzled layout the
-//     tensor core reads) into a six-slot ring, and prefetches each unit's LUT
-//     rows into L2;
-//   warp 17, MMA (one thread): per tile, eight tcgen05.mma (A from TMEM, B
-//     from the ring, fp32 accumulator in TMEM) committed to the tile's "free"
-//     barrier, which releases its TMEM slot and its B slot;
-//   warps 18-21, epilogue: write a unit's LUT (q >= 5) into a shared region
-//     one unit ahead (two halves used alternately for q <= 7), read the
-//     unit's accumulator (double-buffered in TMEM) and write h =
-//     silu(gate)*up, down-projection partial sums or the linear output; then
-//     publish the unit and run the deterministic combine of a finished strip;
-//   warp 22, scheduler (one thread): takes tickets and publishes units into
-//     four slots ahead of the other roles.
+//     stream goes to set x % 4.  A thread reads its row's 16 bytes of every
+//     committed plane of its tile from a shared chunk, turns the row's 128
+//     columns into fp16 through its LUT (dequant.cuh) and stores them as
+//     operand A in one of six TMEM slots (tcgen05.st);
+//   warps 16-19, MMA issuers (one thread each, one per set): per tile, eight
+//     tcgen05.mma (A from TMEM, B from shared memory, fp32 accumulator in the
+//     set's own double-buffered TMEM columns) committed to the tile's "free"
+//     barrier, which releases its TMEM slot and its B slot.  Several issuing
+//     warps are needed: one thread issues an N = 16 MMA only every ~45 ns;
+//   warps 20-23, epilogue: write each unit's LUT into a shared region one
+//     unit ahead (two halves used alternately), sum the sets' accumulators
+//     of a unit and write h = silu(gate)*up, down-projection partial sums or
+//     the linear output; then publish the unit and run the deterministic
+//     combine of a finished strip;
+//   warp 24, plane loader: per chunk of a unit's consecutive tiles, one bulk
+//     copy per plane (a run of tiles of one plane is contiguous) into one of
+//     four 32 KB slots;
+//   warp 25, scheduler (one thread): takes tickets and publishes units into
+//     four slots ahead of the other roles;
+//   warp 26, B loader (one thread): each tile's B operand (the 16 tokens' x or
+//     h columns: two 2-D tensor-map boxes in the 128-byte-swizzled layout the
+//     tensor core reads) into a six-slot ring.
 // Gate_up B rows are the routed tokens' x rows in expert order; every CTA
-// gathers a share of them into the workspace at the start and the loader
+// gathers a share of them into the workspace at the start and the B loader
 // waits for all shares before the first gate_up copy.
 // All waits are bounded (PW_ERR_TIMEOUT); no role waits without a time limit
 // on a barrier that a failed role could leave unfinished, every copy lands

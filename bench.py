@@ -66,6 +66,36 @@ def _tensor_peak():
         return 1700.0, "fallback sustained"
 
 
+def source_digest(paths) -> str:
+    """sha256 of the code in `paths` with comments and blank space removed (a
+    comment edit does not change the kernel the record was taken on)."""
+    import hashlib
+    import re
+    h = hashlib.sha256()
+    for path in paths:
+        with open(path) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        h.update("\n".join(line.strip() for line in text.splitlines() if line.strip()).encode())
+    return h.hexdigest()
+
+
+def measured_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
+    record (profiles/traffic.json), or None when there is no record or the
+    kernel's code changed since it was taken."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)[kernel]
+        if rec["workload"] != workload:
+            return None
+        paths = [os.path.join(ROOT, "any_precision_bit_pw_gb300", "csrc", n) for n in rec["source_files"]]
+        return float(rec["dram_bytes_per_launch"]) if source_digest(paths) == rec["source_sha256"] else None
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def algorithmic_flops(wl, offsets):
     """2 * A * (2I*H + H*I): the gate_up and down contractions of every assignment."""
     sh = wl.shape
@@ -263,11 +293,14 @@ def gpu_arm(args, rank, world, local_rank):
     ffn_avg_ms = float(np.mean(ffn_ms))
     achieved = mean_bytes / (ffn_avg_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
+    prefill = wl.tokens * sh.top_k >= 48 * sh.experts
     hbm_roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "apl_decode_kernel / apl_tc_kernel (pw_moe_apl_ffn)",
+                "traffic": None if prefill else measured_traffic("apl_decode_kernel", wl.name),
+                "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
+                "kernel": "apl_tc_kernel (pw_moe_apl_ffn, 256-token tiles)" if prefill else
+                          "apl_decode_kernel (pw_moe_apl_ffn, 16-token tiles)",
                 "algorithmic_bytes_per_launch": mean_bytes, "plane_bytes_per_launch": mean_planes,
                 "launch_ms": ffn_avg_ms, "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"}
-    prefill = wl.tokens * sh.top_k >= 48 * sh.experts
     roofline = hbm_roof
     if prefill:
         flops = float(np.mean([algorithmic_flops(wl, o) for o in offsets_per_batch]))
