@@ -23,6 +23,15 @@ namespace pw {
 
 constexpr int kStageK = 64;                      // columns per pipeline stage
 
+// Two zero-extended 16-bit values into one 32-bit pair (lo | hi << 16) as an
+// integer multiply-add, which issues on the multiply-add pipe rather than the
+// logic pipe that carries the masks and byte permutes.
+__device__ __forceinline__ uint32_t pack_mad(uint32_t lo, uint32_t hi) {
+  uint32_t r;
+  asm("mad.lo.u32 %0, %1, 65536, %2;" : "=r"(r) : "r"(hi), "r"(lo));
+  return r;
+}
+
 // Shifts by a count known after unrolling (0 allowed).
 __device__ __forceinline__ uint32_t shl_mul(uint32_t x, int s) {
   return x << s;
@@ -251,7 +260,7 @@ struct RowDequant<Q, false> {
         const uint32_t sel = 0x7604u | (static_cast<uint32_t>(j) << 4);
         const uint32_t v0 = lds_u16(prmt(X[js], tblw, sel));
         const uint32_t v1 = lds_u16(prmt(X[4 + js], tblw, sel));
-        out[4 * js + j] = prmt(v0, v1, 0x5410u);
+        out[4 * js + j] = pack_mad(v0, v1);
       }
     }
   }

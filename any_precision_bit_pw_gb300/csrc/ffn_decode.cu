@@ -182,10 +182,13 @@ __device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, con
   const int set = warp >> 2, qd = warp & 3;
   const int pos = qd * 32 + lane;
   bool ok = true;
-  pw::RowDequant<Q> dq;
+  // q <= 3: LUT in registers; q >= 4: LUT in the shared region (for four
+  // planes the transpose and shared lookups cost fewer logic ops than the
+  // two-level register lookup)
+  pw::RowDequant<Q, (Q <= 3)> dq;
   // the unit's LUT is in region half ui & 1 (written one unit ahead)
   ok = wait_bar(sm, kBarRegReady + static_cast<int>(ui & 1u), (ui >> 1) & 1u, p);
-  if constexpr (Q <= 4) {
+  if constexpr (Q <= 3) {
     if (ok) dq.load_shared(sm.region + (ui & 1u) * 32768u + static_cast<uint32_t>(pos) * 32u);
   } else {
     dq.set_row(sm.region, qd, lane, static_cast<int>(ui & 1u));
@@ -467,8 +470,8 @@ __device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i
   // i or i - 1 takes the whole region, are finished by every dequant warp
   const uint32_t need = static_cast<uint32_t>(kDeqWarpsAll) * ((u.q == 8 || prev_q8) ? i : (i >= 1 ? i - 1 : 0u));
   const bool ok = wait_count(sm, &sm.st->deq_done, need, p);
-  if (ok && u.q <= 4) {
-    // q <= 4: the row's table (at most 32 bytes), row-major at the start of
+  if (ok && u.q <= 3) {
+    // q <= 3: the row's table (at most 16 bytes), row-major at the start of
     // the half; the dequant threads load it into registers
     const BlockDesc& d = *u.d;
     const int row = strip_pos_row(u.strip, pos, d.rows / 2);
@@ -481,12 +484,6 @@ __device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i
       const uint4 v = __ldg(src);
       asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                    : "memory");
-      if (u.q == 4) {
-        const uint4 v2 = __ldg(src + 1);
-        asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst + 16), "r"(v2.x), "r"(v2.y), "r"(v2.z),
-                     "r"(v2.w)
-                     : "memory");
-      }
     }
   } else if (ok && u.q < 8) {
     const BlockDesc& d = *u.d;
@@ -495,6 +492,7 @@ __device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i
     const uint32_t tblw =
         sm.region | (static_cast<uint32_t>((qd & 1) * 32 + lane) * 4u + static_cast<uint32_t>(qd >> 1) * 2u);
     switch (u.q) {
+      case 4: pw::region_fill<4>(tblw, lut, h); break;
       case 5: pw::region_fill<5>(tblw, lut, h); break;
       case 6: pw::region_fill<6>(tblw, lut, h); break;
       default: pw::region_fill<7>(tblw, lut, h); break;
