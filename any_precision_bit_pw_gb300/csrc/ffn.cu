@@ -1,8 +1,8 @@
 // Host entry points of the fused mixed-precision MoE expert layer and of the
 // any-precision linear test export: argument checks, workspace layout, path
-// choice, launch.  The kernels are in ffn_decode.cu (token tiles of up to 16)
-// and ffn_tile.cu (token tiles of up to 256); ffn_common.cuh describes the work
-// units they share.
+// choice, launch.  The kernel body is ffn_stream.cuh, instantiated for token
+// tiles of 16 and 32 (decode path) and 64 (prefill path); ffn_common.cuh
+// describes the work units.
 //
 // "PagedWeight" arXiv text, §3.3 (Fused Mixed-Precision MoE Kernel).
 #include <mutex>
@@ -37,13 +37,17 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int path) {
   L.nsplit = (I + L.split_cols - 1) / L.split_cols;
   const size_t ctr_words = 2 + static_cast<size_t>(E) * L.nsplit + static_cast<size_t>(H) / 128;
   L.ctr = 0;
-  L.gather = ctr_words * 4;
-  L.h = align256(L.gather + 4);
+  L.gather = ctr_words * 4;   // [0] x-gather shares done, [1] CTAs done (prefill combine)
+  L.h = align256(L.gather + 8);
   L.part = L.h + align256(static_cast<size_t>(A) * I * 2);
   L.xp = L.part + align256(static_cast<size_t>(L.nsplit) * A * H * 4);
-  L.total = L.xp + (path == PW_PATH_PREFILL ? 0 : align256(static_cast<size_t>(A) * H * 2));
+  L.total = L.xp + align256(static_cast<size_t>(A) * H * 2);
   return L;
 }
+
+// Token-tile width of the decode path: 16 while experts average at most 16
+// tokens, else 32.
+int decode_width(int T, int E, int k) { return static_cast<long long>(T) * k <= 16ll * E ? 16 : 32; }
 
 // Workspace of the path pw_moe_apl_ffn picks by itself for this size.
 WsLayout ws_layout(int T, int H, int I, int E, int k) {
@@ -118,12 +122,14 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
   p.part = reinterpret_cast<float*>(ws + L.part);
   p.xp = reinterpret_cast<uint16_t*>(ws + L.xp);
   p.gather_ctr = reinterpret_cast<uint32_t*>(ws + L.gather);
+  p.grid_combine = path == PW_PATH_PREFILL;
   p.status = d_status;
   p.wait_ns = (o.wait_timeout_us ? o.wait_timeout_us : 2000000u) * 1000ull;
   p.flags = o.flags;
   p.linear = 0;
   PW_CUDA_TRY(cudaMemsetAsync(p.ctr, 0, L.h - L.ctr, s));
-  return path == PW_PATH_PREFILL ? pw_ffn::launch_tile_kernel(p, s, 256) : pw_ffn::launch_decode_kernel(p, s);
+  if (path == PW_PATH_PREFILL) return pw_ffn::launch_prefill_kernel(p, s);
+  return decode_width(T, E, k) == 16 ? pw_ffn::launch_decode_kernel(p, s) : pw_ffn::launch_decode32_kernel(p, s);
 }
 
 int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I, int E, int k,
@@ -160,7 +166,8 @@ int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,
   p.linear = 1;
   p.nsplit = 1;
   p.split_cols = d.cols;
-  return M > 16 ? pw_ffn::launch_tile_kernel(p, s, 256) : pw_ffn::launch_decode_kernel(p, s);
+  if (M <= 16) return pw_ffn::launch_decode_kernel(p, s);
+  return M <= 32 ? pw_ffn::launch_decode32_kernel(p, s) : pw_ffn::launch_prefill_kernel(p, s);
 }
 
 }  // extern "C"

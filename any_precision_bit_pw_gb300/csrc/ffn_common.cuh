@@ -62,7 +62,8 @@ struct Params {
   float* part;
   uint16_t* xp;            // decode path: x rows in expert order [A][H]
   uint32_t* ctr;           // [0] ticket, [1] abort, [2, 2+E*nsplit) gate_up done, then strip arrivals
-  uint32_t* gather_ctr;    // decode path: CTAs that finished their share of xp
+  uint32_t* gather_ctr;    // CTAs that finished their share of xp; [1]: CTAs done with all units
+  int grid_combine;        // 1: every CTA combines after the last unit (large batches)
   int32_t* status;
   uint64_t wait_ns;
   uint32_t flags;
@@ -263,7 +264,7 @@ __device__ __forceinline__ int finish_unit(const Params& p, const Shared& sh, co
       __threadfence();
       atomicAdd(p.ctr + 2 + u.e * p.nsplit + u.split, 1u);
     }
-  } else if (!u_skip && u.kind == kDown) {
+  } else if (!u_skip && u.kind == kDown && !p.grid_combine) {
     __threadfence();
     const uint32_t prev = atomicAdd(p.ctr + 2 + p.E * p.nsplit + u.strip, 1u);
     if (prev + 1 == static_cast<uint32_t>(sh.arrivals_per_strip)) {
@@ -297,42 +298,58 @@ __device__ __forceinline__ void add4(float4& a, const float4 v) {
   a.w += v.w;
 }
 
+// y[t][row..row+3] (fp16) from the token's k partial-sum vectors.
+__device__ __forceinline__ void combine_item(const Params& p, int t, int row) {
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int j = 0; j < p.k; ++j) {
+    const int slot = t * p.k + j;
+    const int ps = __ldg(p.inv_perm + slot);
+    const float wt = __ldg(p.w + slot);
+    const float4* base = reinterpret_cast<const float4*>(p.part + static_cast<long long>(ps) * p.H + row);
+    const long long sstride = static_cast<long long>(p.A) * p.H / 4;   // float4 per split
+    float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int sp0 = 0; sp0 < p.nsplit; sp0 += 8) {
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        v[u] = sp0 + u < p.nsplit ? __ldcg(base + (sp0 + u) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) add4(s, v[u]);
+    }
+    acc.x += wt * s.x;
+    acc.y += wt * s.y;
+    acc.z += wt * s.z;
+    acc.w += wt * s.w;
+  }
+  const uint32_t lo = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.x))) |
+                      (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.y))) << 16);
+  const uint32_t hi = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.z))) |
+                      (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.w))) << 16);
+  *reinterpret_cast<uint2*>(p.y + static_cast<long long>(t) * p.H + row) = make_uint2(lo, hi);
+}
+
+// One strip (128 rows) for every token, by the threads of one CTA.
 __device__ inline void combine_strip(const Params& p, int strip, int tid, int nthreads) {
   const int n_items = p.T * 32;
   for (int it = tid; it < n_items; it += nthreads) {
     const int t = it >> 5, r4 = (it & 31) * 4;
-    const int row = (r4 >> 6) * (p.H / 2) + strip * 64 + (r4 & 63);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < p.k; ++j) {
-      const int slot = t * p.k + j;
-      const int ps = __ldg(p.inv_perm + slot);
-      const float wt = __ldg(p.w + slot);
-      const float4* base = reinterpret_cast<const float4*>(p.part + static_cast<long long>(ps) * p.H + row);
-      const long long sstride = static_cast<long long>(p.A) * p.H / 4;   // float4 per split
-      float4 s = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int sp0 = 0; sp0 < p.nsplit; sp0 += 8) {
-        float4 v[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u)
-          v[u] = sp0 + u < p.nsplit ? __ldcg(base + (sp0 + u) * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int u = 0; u < 8; ++u) add4(s, v[u]);
-      }
-      acc.x += wt * s.x;
-      acc.y += wt * s.y;
-      acc.z += wt * s.z;
-      acc.w += wt * s.w;
-    }
-    const uint32_t lo = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.x))) |
-                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.y))) << 16);
-    const uint32_t hi = static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.z))) |
-                        (static_cast<uint32_t>(__half_as_ushort(__float2half_rn(acc.w))) << 16);
-    *reinterpret_cast<uint2*>(p.y + static_cast<long long>(t) * p.H + row) = make_uint2(lo, hi);
+    combine_item(p, t, (r4 >> 6) * (p.H / 2) + strip * 64 + (r4 & 63));
   }
 }
 
-// Kernel launchers (one translation unit each).
-int launch_tile_kernel(const Params& p, cudaStream_t s, int nmax);    // 256-token tiles (and linear M > 16)
-int launch_decode_kernel(const Params& p, cudaStream_t s);            // 16-token tiles, tile-sized stages
+// Every row of every token, spread over all threads of the grid (after the
+// last unit; the rows' partial sums are complete).
+__device__ inline void combine_all(const Params& p, long long tid, long long nthreads) {
+  const int q4 = p.H / 4;
+  const long long n_items = static_cast<long long>(p.T) * q4;
+  for (long long it = tid; it < n_items; it += nthreads)
+    combine_item(p, static_cast<int>(it / q4), static_cast<int>(it % q4) * 4);
+}
+
+// Kernel launchers (one translation unit each, ffn_stream.cuh instantiated
+// for 16-, 32- and 64-token tiles).
+int launch_decode_kernel(const Params& p, cudaStream_t s);     // 16-token tiles
+int launch_decode32_kernel(const Params& p, cudaStream_t s);   // 32-token tiles
+int launch_prefill_kernel(const Params& p, cudaStream_t s);    // 64-token tiles
 
 }  // namespace pw_ffn

@@ -96,6 +96,22 @@ def measured_traffic(kernel: str, workload: str):
         return None
 
 
+def ffn_kernel(tokens: int, top_k: int, experts: int) -> str:
+    """The fused-layer kernel pw_moe_apl_ffn picks for this size (token-tile
+    width from the average tokens per expert, as in the library)."""
+    A = tokens * top_k
+    if A >= 48 * experts:
+        return "apl_prefill_kernel"
+    return "apl_decode_kernel" if A <= 16 * experts else "apl_decode32_kernel"
+
+
+KERNEL_TILE = {"apl_decode_kernel": 16, "apl_decode32_kernel": 32, "apl_prefill_kernel": 64}
+
+
+def kernel_label(name: str) -> str:
+    return f"{name} (pw_moe_apl_ffn, {KERNEL_TILE[name]}-token tiles)"
+
+
 def algorithmic_flops(wl, offsets):
     """2 * A * (2I*H + H*I): the gate_up and down contractions of every assignment."""
     sh = wl.shape
@@ -293,12 +309,12 @@ def gpu_arm(args, rank, world, local_rank):
     ffn_avg_ms = float(np.mean(ffn_ms))
     achieved = mean_bytes / (ffn_avg_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
-    prefill = wl.tokens * sh.top_k >= 48 * sh.experts
+    kname = ffn_kernel(wl.tokens, sh.top_k, sh.experts)
+    prefill = kname == "apl_prefill_kernel"
     hbm_roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None if prefill else measured_traffic("apl_decode_kernel", wl.name),
+                "traffic": measured_traffic(kname, wl.name),
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
-                "kernel": "apl_tc_kernel (pw_moe_apl_ffn, 256-token tiles)" if prefill else
-                          "apl_decode_kernel (pw_moe_apl_ffn, 16-token tiles)",
+                "kernel": kernel_label(kname),
                 "algorithmic_bytes_per_launch": mean_bytes, "plane_bytes_per_launch": mean_planes,
                 "launch_ms": ffn_avg_ms, "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"}
     roofline = hbm_roof
@@ -307,7 +323,7 @@ def gpu_arm(args, rank, world, local_rank):
         tpk, tkind = _tensor_peak()
         ach_t = flops / (ffn_avg_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": ach_t, "peak": tpk, "unit": "TFLOP/s", "frac": ach_t / tpk,
-                    "traffic": None, "kernel": "apl_tc_kernel (pw_moe_apl_ffn, 256-token tiles)",
+                    "traffic": None, "kernel": kernel_label(kname),
                     "algorithmic_flops_per_launch": flops, "launch_ms": ffn_avg_ms, "peak_kind": tkind}
     clocks = clk.summary()
     value = job_throughput(wl.tokens, K, world, total_ms)
@@ -431,7 +447,7 @@ def stack_arm(args, rank, world, local_rank):
     peak, peak_kind = _peaks()
     achieved = float(nbytes.sum() / (ffn_ms.sum() * 1e-3) / 1e9)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": None, "kernel": "apl_decode_kernel (pw_moe_apl_ffn)",
+                "traffic": None, "kernel": kernel_label(ffn_kernel(T, sh.top_k, E)),
                 "algorithmic_bytes_per_launch": float(nbytes.mean()), "launch_ms": float(ffn_ms.mean()),
                 "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"}
     value = job_throughput(T, K, world, total_ms)

@@ -187,9 +187,11 @@ size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k);
  *  d_status int32, set to a PW_ERR_* code on a device-side failure (left
  *  untouched on success, so the caller zeroes it beforehand).
  * Shapes: H % 128 == 0, I % 128 == 0, committed bitwidths 2..8.
- * The call picks one of two tile shapes from the average number of tokens
- * per expert (T*k/E): up to 16 tokens per tile below 48, else 256 (both run on
- * the tcgen05 tensor cores; pw_moe_apl_ffn_ex can force either). */
+ * The call picks the token-tile width from the average number of tokens per
+ * expert (T*k/E): tiles of 16 tokens up to 16, of 32 below 48 (the decode
+ * path), else of 64 (the prefill path, whose combine runs over the whole grid
+ * after the last unit).  All run on the tcgen05 tensor cores;
+ * pw_moe_apl_ffn_ex can force either path. */
 int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
                    int E, int k, const int32_t* d_ids, const float* d_w,
                    const int32_t* d_offsets, const int32_t* d_perm, const int32_t* d_inv_perm,
@@ -224,8 +226,8 @@ int pw_moe_apl_ffn_noalloc(const void* d_desc, int layer, const uint16_t* d_x, i
 
 /* Options of pw_moe_apl_ffn_ex (zero-initialise, then set what you need). */
 #define PW_PATH_AUTO 0
-#define PW_PATH_DECODE 1   /* token tiles of up to 16 (decode batches) */
-#define PW_PATH_PREFILL 2  /* token tiles of up to 256 (prefill batches) */
+#define PW_PATH_DECODE 1   /* token tiles of 16 or 32 (decode batches) */
+#define PW_PATH_PREFILL 2  /* token tiles of 64 (prefill batches) */
 #define PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL 1u  /* test hook: one gate_up unit never
                                                  signals completion, so the waits
                                                  that depend on it run out */

@@ -374,7 +374,7 @@ def test_ffn_mixtral_8x7b_uniform_sweep_points(b, T):
 
 def test_ffn_mixtral_8x22b_prefill():
     """The 8x22B-shaped prefill layer: 4096 tokens, Zipf-skewed routing, hot
-    experts at 8 bits and the rest at 3-4 bits (256-token tiles)."""
+    experts at 8 bits and the rest at 3-4 bits (64-token tiles)."""
     wl = synth.MIXTRAL_8X22B_PREFILL
     li = synth.layer_inputs(wl, device=DEV)
     y, status, call, _ = _run_gpu(li)
