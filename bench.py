@@ -1,7 +1,7 @@
 """Benchmark of the fused mixed-precision Any-Precision MoE layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pw|reference]
-                    [--workload NAME] [--sweep PATH]
+                    [--workload NAME] [--tokens T] [--sweep PATH]
 
 One step = one pass of the hot path over one batch: top-k routing
 (pw_moe_route_topk) + the fused expert layer (pw_moe_apl_ffn: gather, gate_up
@@ -81,19 +81,25 @@ def source_digest(paths) -> str:
     return h.hexdigest()
 
 
-def measured_traffic(kernel: str, workload: str):
-    """DRAM bytes per launch of `kernel` on `workload` from the committed ncu
-    record (profiles/traffic.json), or None when there is no record or the
-    kernel's code changed since it was taken."""
+def measured_traffic(kernel: str, workload: str, tokens: int):
+    """DRAM bytes per launch of `kernel` on `workload` at `tokens` from the
+    committed ncu record (profiles/traffic.json), or None when there is no
+    record or the kernel's code changed since it was taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             rec = json.load(f)[kernel]
-        if rec["workload"] != workload:
+        if rec["workload"] != workload or int(rec["tokens"]) != tokens:
             return None
         paths = [os.path.join(ROOT, "any_precision_bit_pw_gb300", "csrc", n) for n in rec["source_files"]]
         return float(rec["dram_bytes_per_launch"]) if source_digest(paths) == rec["source_sha256"] else None
     except (OSError, KeyError, ValueError):
         return None
+
+
+def get_workload(name: str, tokens=None):
+    """A named workload, with its token count replaced when `tokens` is given."""
+    wl = synth.WORKLOADS[name]
+    return wl.with_(tokens=tokens) if tokens else wl
 
 
 def ffn_kernel(tokens: int, top_k: int, experts: int) -> str:
@@ -222,7 +228,7 @@ def gpu_arm(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     pw.lib()
-    wl = synth.WORKLOADS[args.workload]
+    wl = get_workload(args.workload, args.tokens)
     sh = wl.shape
     li = synth.layer_inputs(wl, device=dev)
     stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, wl.parent_bits, wl.seed_bits, dev)
@@ -312,7 +318,7 @@ def gpu_arm(args, rank, world, local_rank):
     kname = ffn_kernel(wl.tokens, sh.top_k, sh.experts)
     prefill = kname == "apl_prefill_kernel"
     hbm_roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                "traffic": measured_traffic(kname, wl.name),
+                "traffic": measured_traffic(kname, wl.name, wl.tokens),
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
                 "kernel": kernel_label(kname),
                 "algorithmic_bytes_per_launch": mean_bytes, "plane_bytes_per_launch": mean_planes,
@@ -323,7 +329,9 @@ def gpu_arm(args, rank, world, local_rank):
         tpk, tkind = _tensor_peak()
         ach_t = flops / (ffn_avg_ms * 1e-3) / 1e12
         roofline = {"bound": "tensor", "achieved": ach_t, "peak": tpk, "unit": "TFLOP/s", "frac": ach_t / tpk,
-                    "traffic": None, "kernel": kernel_label(kname),
+                    "traffic": measured_traffic(kname, wl.name, wl.tokens),
+                    "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
+                    "kernel": kernel_label(kname),
                     "algorithmic_flops_per_launch": flops, "launch_ms": ffn_avg_ms, "peak_kind": tkind}
     clocks = clk.summary()
     value = job_throughput(wl.tokens, K, world, total_ms)
@@ -357,7 +365,7 @@ def stack_arm(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     pw.lib()
-    wl = synth.WORKLOADS[args.workload]
+    wl = get_workload(args.workload, args.tokens)
     sh = wl.shape
     T, H, E, L = wl.tokens, sh.hidden, sh.experts, wl.layers
     run = StackRun(wl, dev, commit_every=synth.STACK_COMMIT_EVERY,
@@ -520,14 +528,14 @@ def sweep(args, dev, out_path):
 # ---------------------------------------------------------------------------
 # the reference arm / CPU baseline: the oracle on the host cores
 # ---------------------------------------------------------------------------
-def oracle_sample(workload: str, experts_in_sample: int = 1) -> dict:
+def oracle_sample(workload: str, experts_in_sample: int = 1, tokens=None) -> dict:
     """Time the oracle on a bounded sample of the workload: the layer output
     contribution of the first ``experts_in_sample`` active experts (their
     gate_up and down blocks read from the packed bit-planes at the committed
     bitwidths, for the tokens routed to them).  Scaled to the full layer by
     the number of active experts (every expert's blocks have the same shape)."""
     from oracle import apl
-    wl = synth.WORKLOADS[workload]
+    wl = get_workload(workload, tokens)
     sh = wl.shape
     x = synth.activations(wl).numpy()
     logits = synth.router_logits(wl).numpy()
@@ -558,11 +566,16 @@ def oracle_sample(workload: str, experts_in_sample: int = 1) -> dict:
                       + (f" and by {wl.layers} layers" if wl.layers > 1 else "")}
 
 
-def cpu_baseline(workload: str) -> dict:
+def _child_cmd(workload: str, tokens=None) -> list:
+    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", workload]
+    return cmd + ["--tokens", str(tokens)] if tokens else cmd
+
+
+def cpu_baseline(workload: str, tokens=None) -> dict:
     """Run the oracle sample in a fresh single-threaded child process."""
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                CUDA_VISIBLE_DEVICES="")
-    cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", workload]
+    cmd = _child_cmd(workload, tokens)
     r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
     if r.returncode != 0:
         return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
@@ -574,14 +587,14 @@ def cpu_baseline(workload: str) -> dict:
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
-    wl = synth.WORKLOADS[args.workload]
+    wl = get_workload(args.workload, args.tokens)
     times = []
     sample = ""
     for _ in range(args.warmup):
         pass  # the oracle has no warm-up state
     for _ in range(max(1, args.steps)):
         d = json.loads(subprocess.run(
-            [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", args.workload],
+            _child_cmd(args.workload, args.tokens),
             env=dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
                      CUDA_VISIBLE_DEVICES=""), capture_output=True, text=True, timeout=600
         ).stdout.strip().splitlines()[-1])
@@ -604,6 +617,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="pw", choices=["pw", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--tokens", type=int, default=None, help="replace the workload's token count")
     ap.add_argument("--sweep", default=None, help="also run the uniform-bitwidth sweep, JSON to this path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
@@ -612,7 +626,7 @@ def main():
         args.warmup = 3
 
     if args.cpu_baseline_child:
-        print(json.dumps(oracle_sample(args.workload)))
+        print(json.dumps(oracle_sample(args.workload, tokens=args.tokens)))
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -628,7 +642,7 @@ def main():
     # the CPU baseline runs in a child process started before this process touches the GPU
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.workload)
+        cpu = cpu_baseline(args.workload, args.tokens)
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     arm = stack_arm if synth.WORKLOADS[args.workload].layers > 1 else gpu_arm
