@@ -37,8 +37,8 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int path) {
   L.nsplit = (I + L.split_cols - 1) / L.split_cols;
   const size_t ctr_words = 2 + static_cast<size_t>(E) * L.nsplit + static_cast<size_t>(H) / 128;
   L.ctr = 0;
-  L.gather = ctr_words * 4;   // [0] x-gather shares done, [1] CTAs done (prefill combine)
-  L.h = align256(L.gather + 8);
+  L.gather = ctr_words * 4;   // [0] x-gather shares done, [1] CTAs done (prefill combine), [2] routed
+  L.h = align256(L.gather + 12);
   L.part = L.h + align256(static_cast<size_t>(A) * I * 2);
   L.xp = L.part + align256(static_cast<size_t>(L.nsplit) * A * H * 4);
   L.total = L.xp + align256(static_cast<size_t>(A) * H * 2);
@@ -79,14 +79,28 @@ size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k) {
   return a > b ? a : b;
 }
 
-int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I, int E, int k,
-                      const int32_t* d_ids, const float* d_w, const int32_t* d_offsets, const int32_t* d_perm,
-                      const int32_t* d_inv_perm, void* d_ws, size_t ws_bytes, uint16_t* d_y, int32_t* d_status,
-                      const pw_ffn_options* opts, void* stream) {
-  (void)d_ids;
+}  // extern "C"
+
+namespace {
+
+// Shared by the fused entry points: checks, workspace layout, path choice and
+// launch.  `routed`: the routing arrays are outputs, computed from d_logits in
+// the same launch on the decode path and by a routing launch just before on
+// the prefill path.
+int ffn_launch(bool routed, const void* d_desc, int layer, const uint16_t* d_x, const float* d_logits, int T, int H,
+               int I, int E, int k, int32_t* d_ids, const float* d_w, const int32_t* d_offsets,
+               const int32_t* d_perm, const int32_t* d_inv_perm, float* d_mass_accum, void* d_ws, size_t ws_bytes,
+               uint16_t* d_y, int32_t* d_status, const pw_ffn_options* opts, void* stream) {
   if (int e = validate_shape(T, H, I, E, k)) return e;
   if (layer < 0) return pw::set_error(PW_ERR_INVALID_ARG, "ffn: layer %d", layer);
-  if (T == 0) return PW_OK;
+  if (routed && T > 0 && !d_logits) return pw::set_error(PW_ERR_INVALID_ARG, "routed ffn: NULL logits");
+  if (routed && (!d_ids || !d_offsets))
+    return pw::set_error(PW_ERR_INVALID_ARG, "ffn: routed call needs ids and offsets");
+  if (T == 0)
+    return routed ? pw_moe_route_topk(d_logits, 0, E, k, d_ids, const_cast<float*>(d_w),
+                                      const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
+                                      const_cast<int32_t*>(d_inv_perm), d_mass_accum, stream)
+                  : PW_OK;
   if (!d_desc || !d_x || !d_w || !d_offsets || !d_perm || !d_inv_perm || !d_y || !d_status || !d_ws)
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: NULL argument");
   if ((reinterpret_cast<uintptr_t>(d_desc) & 15) || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
@@ -127,9 +141,50 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
   p.wait_ns = (o.wait_timeout_us ? o.wait_timeout_us : 2000000u) * 1000ull;
   p.flags = o.flags;
   p.linear = 0;
+  if (routed && path == PW_PATH_PREFILL) {
+    // large batches: one CTA would route while the grid waits; a separate
+    // routing launch comes first instead
+    if (int e = pw_moe_route_topk(d_logits, T, E, k, d_ids, const_cast<float*>(d_w),
+                                  const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
+                                  const_cast<int32_t*>(d_inv_perm), d_mass_accum, stream))
+      return e;
+  } else if (routed) {
+    p.logits = d_logits;
+    p.ids_out = d_ids;
+    p.mass_accum = d_mass_accum;
+  }
   PW_CUDA_TRY(cudaMemsetAsync(p.ctr, 0, L.h - L.ctr, s));
   if (path == PW_PATH_PREFILL) return pw_ffn::launch_prefill_kernel(p, s);
   return decode_width(T, E, k) == 16 ? pw_ffn::launch_decode_kernel(p, s) : pw_ffn::launch_decode32_kernel(p, s);
+}
+
+}  // namespace
+
+extern "C" {
+
+int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I, int E, int k,
+                      const int32_t* d_ids, const float* d_w, const int32_t* d_offsets, const int32_t* d_perm,
+                      const int32_t* d_inv_perm, void* d_ws, size_t ws_bytes, uint16_t* d_y, int32_t* d_status,
+                      const pw_ffn_options* opts, void* stream) {
+  (void)d_ids;
+  return ffn_launch(false, d_desc, layer, d_x, nullptr, T, H, I, E, k, nullptr, d_w, d_offsets, d_perm, d_inv_perm,
+                    nullptr, d_ws, ws_bytes, d_y, d_status, opts, stream);
+}
+
+int pw_moe_route_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, const float* d_logits, int T, int H,
+                            int I, int E, int k, int32_t* d_ids, float* d_w, int32_t* d_offsets, int32_t* d_perm,
+                            int32_t* d_inv_perm, float* d_mass_accum, void* d_ws, size_t ws_bytes, uint16_t* d_y,
+                            int32_t* d_status, const pw_ffn_options* opts, void* stream) {
+  return ffn_launch(true, d_desc, layer, d_x, d_logits, T, H, I, E, k, d_ids, d_w, d_offsets, d_perm, d_inv_perm,
+                    d_mass_accum, d_ws, ws_bytes, d_y, d_status, opts, stream);
+}
+
+int pw_moe_route_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, const float* d_logits, int T, int H,
+                         int I, int E, int k, int32_t* d_ids, float* d_w, int32_t* d_offsets, int32_t* d_perm,
+                         int32_t* d_inv_perm, float* d_mass_accum, void* d_ws, size_t ws_bytes, uint16_t* d_y,
+                         int32_t* d_status, void* stream) {
+  return pw_moe_route_apl_ffn_ex(d_desc, layer, d_x, d_logits, T, H, I, E, k, d_ids, d_w, d_offsets, d_perm,
+                                 d_inv_perm, d_mass_accum, d_ws, ws_bytes, d_y, d_status, nullptr, stream);
 }
 
 int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I, int E, int k,

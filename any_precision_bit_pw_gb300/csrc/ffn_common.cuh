@@ -62,8 +62,17 @@ struct Params {
   float* part;
   uint16_t* xp;            // decode path: x rows in expert order [A][H]
   uint32_t* ctr;           // [0] ticket, [1] abort, [2, 2+E*nsplit) gate_up done, then strip arrivals
-  uint32_t* gather_ctr;    // CTAs that finished their share of xp; [1]: CTAs done with all units
+  uint32_t* gather_ctr;    // CTAs that finished their share of xp; [1]: CTAs done with all units;
+                           // [2]: routing arrays written (routed call)
   int grid_combine;        // 1: every CTA combines after the last unit (large batches)
+  // Routed call (routing in the same launch): CTA 0 computes ids, w, offsets,
+  // perm and inv_perm from the logits and publishes them through
+  // gather_ctr[2]; NULL logits: the routing arrays are inputs.  The kernels
+  // read offsets, perm, inv_perm and w with ordinary (coherent) loads, not
+  // the read-only path, because a routed call writes them in the same launch.
+  const float* logits;
+  int32_t* ids_out;
+  float* mass_accum;
   int32_t* status;
   uint64_t wait_ns;
   uint32_t flags;
@@ -129,7 +138,7 @@ __device__ void setup_schedule(const Params& p, Shared& sh) {
   int n = 0, gu = 0, dn = 0, arr = 0;
   const int gu_strips = 2 * p.I / 128, dn_strips = p.H / 128;
   for (int e = 0; e < p.E; ++e) {
-    const int ne = __ldg(p.offsets + e + 1) - __ldg(p.offsets + e);
+    const int ne = p.offsets[e + 1] - p.offsets[e];
     if (ne <= 0) continue;
     const int g = (ne + NMAX - 1) / NMAX;
     sh.act[n] = e;
@@ -207,7 +216,7 @@ __device__ void next_unit(const Params& p, Shared& sh) {
     sh.u = u;
     return;
   }
-  const int off0 = __ldg(p.offsets + u.e), ne = __ldg(p.offsets + u.e + 1) - off0;
+  const int off0 = p.offsets[u.e], ne = p.offsets[u.e + 1] - off0;
   u.off = off0 + u.tg * NMAX;
   u.nrows = min(NMAX, ne - u.tg * NMAX);
   u.npad = ((u.nrows + 15) / 16) * 16;
@@ -303,8 +312,8 @@ __device__ __forceinline__ void combine_item(const Params& p, int t, int row) {
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
   for (int j = 0; j < p.k; ++j) {
     const int slot = t * p.k + j;
-    const int ps = __ldg(p.inv_perm + slot);
-    const float wt = __ldg(p.w + slot);
+    const int ps = p.inv_perm[slot];
+    const float wt = p.w[slot];
     const float4* base = reinterpret_cast<const float4*>(p.part + static_cast<long long>(ps) * p.H + row);
     const long long sstride = static_cast<long long>(p.A) * p.H / 4;   // float4 per split
     float4 s = make_float4(0.f, 0.f, 0.f, 0.f);

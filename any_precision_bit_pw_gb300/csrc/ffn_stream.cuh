@@ -38,6 +38,7 @@
 #include <cuda.h>
 
 #include "ffn_common.cuh"
+#include "route_block.cuh"
 
 namespace pw_ffn {
 namespace {
@@ -70,10 +71,16 @@ constexpr int kPS = kN <= 16 ? 4 : 3;             // plane chunk slots
 constexpr int kPSlotBytes = 32768;                // one chunk: up to 4 tiles x 4 planes or 2 tiles x 8 planes
 constexpr int kSmemBytes = 232448;
 constexpr uint32_t kHintNs = 20000;
+// Unroll of the two half-rows of a tile: the 16- and 32-token kernels run
+// faster with the smaller loop body (fewer instruction-fetch stalls), the
+// 64-token kernel with both halves unrolled (measured).
+constexpr int kHalfUnroll = kN <= 32 ? 1 : 2;
 static_assert(kDCol0 + 2 * kIssuers * kN <= kTmemCols, "TMEM columns");
 static_assert(kSA <= kF && 2 * kBS <= kF, "barrier reuse distances");
 static_assert(4 * 4 * 2048 <= kPSlotBytes && 2 * 8 * 2048 <= kPSlotBytes, "chunk sizes");
 static_assert(kSets % kIssuers == 0, "issuers share sets evenly");
+static_assert(pw_route::scratch_bytes(pw_route::kMaxE, kThreads / 32) <= pw::kLutRegionBytes,
+              "routing scratch fits the LUT region");
 
 enum : int {
   kBarAFull = 0,                  // [kF]  A slot written (4 warps of a set)
@@ -246,7 +253,7 @@ __device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, con
         pw::tc_fence_after();
         const uint32_t acol = tl + (x % kSA) * kATileCols;
         const uint32_t src = sm.st->pslot[ps] + static_cast<uint32_t>(j) * pw::kTileBytes + pos * 16;
-#pragma unroll
+#pragma unroll kHalfUnroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t w2[Q][2];
 #pragma unroll
@@ -696,6 +703,37 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   DecState& st = *sm.st;
+  // routed call: CTA 0 routes the batch (the LUT region is its scratch: the
+  // pipeline has not started) and publishes the routing arrays; every CTA
+  // waits for them before it schedules or gathers (all CTAs are resident:
+  // one per SM)
+  if (p.logits) {
+    if (blockIdx.x == 0) {
+      pw_route::route_block(p.logits, p.T, p.E, p.k, p.ids_out, const_cast<float*>(p.w),
+                            const_cast<int32_t*>(p.offsets), const_cast<int32_t*>(p.perm),
+                            const_cast<int32_t*>(p.inv_perm), p.mass_accum, smem_raw + (sm.region - pw::smem_u32(smem_raw)));
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        pw::st_release_gpu(p.gather_ctr + 2, 1u);
+      }
+    }
+    if (threadIdx.x == 0) {
+      int ok = 1;
+      const uint64_t t0 = pw::global_ns();
+      while (pw::ld_acquire_gpu(p.gather_ctr + 2) == 0u) {
+        if (pw::global_ns() - t0 > p.wait_ns) {
+          report(p.status, PW_ERR_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
+      }
+      st.abort = ok ? 0 : 1;
+    }
+    __syncthreads();
+    if (*reinterpret_cast<volatile int*>(&st.abort)) return;   // nothing allocated or issued yet
+  }
   if (threadIdx.x == 0) {
     for (int i = 0; i < kF; ++i) {
       pw::mbar_init(bar(sm, kBarAFull + i), 4);
@@ -739,7 +777,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long v = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; v < nvec;
          v += static_cast<long long>(gridDim.x) * kThreads) {
       const int a = static_cast<int>(v / vrow), c = static_cast<int>(v % vrow);
-      const int tok = __ldg(p.perm + a) / p.k;
+      const int tok = p.perm[a] / p.k;
       const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<long long>(tok) * p.H) + c);
       reinterpret_cast<uint4*>(p.xp + static_cast<long long>(a) * p.H)[c] = val;
     }

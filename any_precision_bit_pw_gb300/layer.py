@@ -122,13 +122,14 @@ class RouteBuffers:
 
 
 class MoECall:
-    """Preallocated buffers for one (T, shape) and the two-launch layer call:
-    pw_moe_route_topk then pw_moe_apl_ffn."""
+    """Preallocated buffers for one (T, shape) and the layer call: routing and
+    the fused expert layer in one launch (pw_moe_route_apl_ffn), or with
+    ``fused=False`` as two launches, pw_moe_route_topk then pw_moe_apl_ffn."""
 
-    def __init__(self, stack: APLMoEStack, tokens: int, device=None):
+    def __init__(self, stack: APLMoEStack, tokens: int, device=None, fused: bool = True):
         dev = stack.device if device is None else torch.device(device)
         T, E, k = tokens, stack.E, stack.k
-        self.stack, self.T = stack, T
+        self.stack, self.T, self.fused = stack, T, fused
         A = max(1, T * k)
         self.route = RouteBuffers(
             ids=torch.empty((max(T, 1), k), dtype=torch.int32, device=dev),
@@ -145,10 +146,14 @@ class MoECall:
     def __call__(self, layer: int, x: torch.Tensor, logits: torch.Tensor, options=None, stream=None,
                  accumulate_mass: bool = True) -> torch.Tensor:
         s, r = self.stack, self.route
-        pw.pw_moe_route_topk(logits, s.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm,
-                             self.mass[layer] if accumulate_mass else None, stream=stream)
-        pw.pw_moe_apl_ffn(s.desc, layer, x, s.I, s.E, s.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm,
-                          self.ws, self.y, self.status, options=options, stream=stream)
+        mass = self.mass[layer] if accumulate_mass else None
+        if self.fused:
+            pw.pw_moe_route_apl_ffn(s.desc, layer, x, logits, s.I, s.E, s.k, r.ids, r.w, r.offsets, r.perm,
+                                    r.inv_perm, mass, self.ws, self.y, self.status, options=options, stream=stream)
+        else:
+            pw.pw_moe_route_topk(logits, s.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm, mass, stream=stream)
+            pw.pw_moe_apl_ffn(s.desc, layer, x, s.I, s.E, s.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm,
+                              self.ws, self.y, self.status, options=options, stream=stream)
         return self.y[: self.T]
 
 

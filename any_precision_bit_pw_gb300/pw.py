@@ -37,6 +37,7 @@ EXPORTS = (
     "pw_page_table_set_desired", "pw_page_table_set_bits", "pw_page_table_get", "pw_page_table_bytes",
     "pw_page_table_resident_bytes", "pw_page_table_sync", "pw_moe_route_topk",
     "pw_moe_apl_ffn_workspace", "pw_moe_apl_ffn", "pw_moe_apl_ffn_ex", "pw_moe_apl_ffn_noalloc",
+    "pw_moe_route_apl_ffn", "pw_moe_route_apl_ffn_ex",
     "pw_unpack_indices",
     "pw_apl_linear",
 )
@@ -89,6 +90,10 @@ def lib() -> ctypes.CDLL:
             "pw_moe_apl_ffn_ex": (I32, [P, I32, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P, P,
                                         ctypes.POINTER(pw_ffn_options), P]),
             "pw_moe_apl_ffn_noalloc": (I32, [P, I32, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, P]),
+            "pw_moe_route_apl_ffn": (I32, [P, I32, P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, SZ, P, P,
+                                           P]),
+            "pw_moe_route_apl_ffn_ex": (I32, [P, I32, P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, SZ, P,
+                                              P, ctypes.POINTER(pw_ffn_options), P]),
             "pw_unpack_indices": (I32, [P, I32, I32, P, P]),
             "pw_apl_linear": (I32, [P, I32, P, I32, P, P]),
         }
@@ -220,6 +225,28 @@ def pw_moe_apl_ffn(d_desc: torch.Tensor, layer: int, x: torch.Tensor, I: int, E:
         _check(lib().pw_moe_apl_ffn(*args, _stream(stream)))
     else:
         _check(lib().pw_moe_apl_ffn_ex(*args, ctypes.byref(options), _stream(stream)))
+
+
+def pw_moe_route_apl_ffn(d_desc: torch.Tensor, layer: int, x: torch.Tensor, logits: torch.Tensor, I: int, E: int,
+                         k: int, ids: torch.Tensor, w: torch.Tensor, offsets: torch.Tensor, perm: torch.Tensor,
+                         inv_perm: torch.Tensor, mass_accum: Optional[torch.Tensor], ws: torch.Tensor,
+                         y: torch.Tensor, status: torch.Tensor, options: Optional[pw_ffn_options] = None,
+                         stream=None) -> None:
+    """Routing and the fused expert layer in one launch (the routing arrays
+    are outputs)."""
+    _dev(x, torch.float16, "x")
+    _dev(y, torch.float16, "y")
+    _dev(logits, torch.float32, "logits")
+    T, H = x.shape
+    if tuple(logits.shape) != (T, E):
+        raise ValueError(f"logits: need shape ({T}, {E}), got {tuple(logits.shape)}")
+    args = (_ptr(d_desc), layer, _ptr(x), _ptr(logits), T, H, I, E, k, _ptr(ids), _ptr(w), _ptr(offsets),
+            _ptr(perm), _ptr(inv_perm), _ptr(mass_accum), _ptr(ws), ws.numel() * ws.element_size(), _ptr(y),
+            _ptr(status))
+    if options is None:
+        _check(lib().pw_moe_route_apl_ffn(*args, _stream(stream)))
+    else:
+        _check(lib().pw_moe_route_apl_ffn_ex(*args, ctypes.byref(options), _stream(stream)))
 
 
 PW_NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -3,9 +3,12 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pw|reference]
                     [--workload NAME] [--tokens T] [--sweep PATH]
 
-One step = one pass of the hot path over one batch: top-k routing
-(pw_moe_route_topk) + the fused expert layer (pw_moe_apl_ffn: gather, gate_up
-at each block's committed bitwidth, SiLU*mul, down, top-k weighted combine).
+One step = one pass of the hot path over one batch: top-k routing and the
+fused expert layer (gather, gate_up at each block's committed bitwidth,
+SiLU*mul, down, top-k weighted combine).  On the decode path both run in one
+launch (pw_moe_route_apl_ffn); on the prefill path routing is its own launch
+(pw_moe_route_topk) before the fused layer (pw_moe_apl_ffn), so that the
+timed kernel is the fused layer alone.
 Weights are resident in HBM (bit-planes + LUTs, packed once before timing).
 The default workload is the Mixtral-8x7B-shaped decode layer (H 4096, I 14336,
 8 experts, top-2, 32 tokens, per-block bitwidths uniform on 3..8).
@@ -116,6 +119,23 @@ KERNEL_TILE = {"apl_decode_kernel": 16, "apl_decode32_kernel": 32, "apl_prefill_
 
 def kernel_label(name: str) -> str:
     return f"{name} (pw_moe_apl_ffn, {KERNEL_TILE[name]}-token tiles)"
+
+
+def layer_call(pw, stack, call, layer, x, logits, mass, ev, stream, routed: bool) -> None:
+    """One layer call of a timed step; `ev` (start, stop) brackets the fused
+    kernel's launch."""
+    r, sh = call.route, stack
+    if routed:
+        ev[0].record(stream)
+        pw.pw_moe_route_apl_ffn(stack.desc, layer, x, logits, sh.I, sh.E, sh.k, r.ids, r.w, r.offsets, r.perm,
+                                r.inv_perm, mass, call.ws, call.y, call.status)
+        ev[1].record(stream)
+    else:
+        pw.pw_moe_route_topk(logits, sh.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm, mass)
+        ev[0].record(stream)
+        pw.pw_moe_apl_ffn(stack.desc, layer, x, sh.I, sh.E, sh.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm,
+                          call.ws, call.y, call.status)
+        ev[1].record(stream)
 
 
 def algorithmic_flops(wl, offsets):
@@ -240,6 +260,8 @@ def gpu_arm(args, rank, world, local_rank):
     lgs = [synth.router_logits(wl, 0, s, dev) for s in range(n_batches)]
     call = MoECall(stack, wl.tokens)
     stream = torch.cuda.current_stream()
+    kname = ffn_kernel(wl.tokens, sh.top_k, sh.experts)
+    routed = kname != "apl_prefill_kernel"
 
     # routing of each batch (for the algorithmic byte count)
     bytes_per_batch = []
@@ -268,13 +290,7 @@ def gpu_arm(args, rank, world, local_rank):
         start.record(stream)
         for i in range(K):
             s = i % n_batches
-            pw.pw_moe_route_topk(lgs[s], sh.top_k, call.route.ids, call.route.w, call.route.offsets,
-                                 call.route.perm, call.route.inv_perm, call.mass[0])
-            ev[i][0].record(stream)
-            pw.pw_moe_apl_ffn(stack.desc, 0, xs[s], sh.intermediate, sh.experts, sh.top_k, call.route.ids,
-                              call.route.w, call.route.offsets, call.route.perm, call.route.inv_perm, call.ws,
-                              call.y, call.status)
-            ev[i][1].record(stream)
+            layer_call(pw, stack, call, 0, xs[s], lgs[s], call.mass[0], ev[i], stream, routed)
         stop.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -315,8 +331,7 @@ def gpu_arm(args, rank, world, local_rank):
     ffn_avg_ms = float(np.mean(ffn_ms))
     achieved = mean_bytes / (ffn_avg_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
-    kname = ffn_kernel(wl.tokens, sh.top_k, sh.experts)
-    prefill = kname == "apl_prefill_kernel"
+    prefill = not routed
     hbm_roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": measured_traffic(kname, wl.name, wl.tokens),
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
@@ -347,7 +362,7 @@ def gpu_arm(args, rank, world, local_rank):
         "roofline_hbm": hbm_roof if prefill else None,
         "e2e": {"value": wl.tokens / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": T * H * 2 + T * E * 4, "d2h_bytes_per_step": T * H * 2},
-        "gpu_launches": 2 * K,
+        "gpu_launches": (1 if routed else 2) * K,
         "clocks": clocks,
         "status": status,
     }
@@ -377,6 +392,7 @@ def stack_arm(args, rank, world, local_rank):
     lgs = [[synth.router_logits(wl, l, s, dev) for l in range(L)] for s in range(n_in)]
     call, stack = run.call, run.stack
     stream = torch.cuda.current_stream()
+    routed = ffn_kernel(T, sh.top_k, E) != "apl_prefill_kernel"
 
     # warm-up: the layer calls without step boundaries (no commits, no mass)
     for i in range(args.warmup):
@@ -405,11 +421,7 @@ def stack_arm(args, rank, world, local_rank):
             resident.append(stack.resident_bytes())
             s = i % n_in
             for l in range(L):
-                pw.pw_moe_route_topk(lgs[s][l], sh.top_k, r.ids, r.w, r.offsets, r.perm, r.inv_perm, call.mass[l])
-                ev[i][l][0].record(stream)
-                pw.pw_moe_apl_ffn(stack.desc, l, xs[s][l], sh.intermediate, E, sh.top_k, r.ids, r.w, r.offsets,
-                                  r.perm, r.inv_perm, call.ws, call.y, call.status)
-                ev[i][l][1].record(stream)
+                layer_call(pw, stack, call, l, xs[s][l], lgs[s][l], call.mass[l], ev[i][l], stream, routed)
             run.step_no += 1
             plan, released = run.boundary()
             released_total += released
@@ -473,7 +485,7 @@ def stack_arm(args, rank, world, local_rank):
         "roofline": roofline,
         "e2e": {"value": T / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": L * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": L * T * H * 2},
-        "gpu_launches": 2 * L * K,
+        "gpu_launches": (1 if routed else 2) * L * K,
         "clocks": clk.summary(),
         "status": status,
     }

@@ -244,6 +244,33 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
                       void* d_ws, size_t ws_bytes, uint16_t* d_y, int32_t* d_status,
                       const pw_ffn_options* opts, void* stream);
 
+/* Routing and the fused expert layer in one launch (§3.3: the kernel takes
+ * routing, the per-expert computation and the output accumulation together).
+ * Computes what pw_moe_route_topk followed by pw_moe_apl_ffn computes, with
+ * the same results bit for bit:
+ *  d_logits fp32 [T][E] router logits (input, finite values);
+ *  d_ids, d_w, d_offsets, d_perm, d_inv_perm: the routing arrays, OUTPUTS
+ *    here (layouts as in pw_moe_route_topk), none may be NULL when T > 0;
+ *  d_mass_accum fp32 [E] or NULL: the routing mass is added as in
+ *    pw_moe_route_topk.
+ * On the decode path (T*k < 48*E) one CTA of the fused kernel routes the
+ * batch at the start of the launch and the others wait for it (bounded; a
+ * timeout sets d_status to PW_ERR_TIMEOUT).  On the prefill path, where one
+ * CTA would route too slowly, a routing launch runs first on the same stream.
+ * T = 0 writes the offsets (all zero) and nothing else (d_logits may then be
+ * NULL).  Every other argument,
+ * limit and error is that of pw_moe_apl_ffn. */
+int pw_moe_route_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, const float* d_logits,
+                         int T, int H, int I, int E, int k, int32_t* d_ids, float* d_w,
+                         int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm,
+                         float* d_mass_accum, void* d_ws, size_t ws_bytes, uint16_t* d_y,
+                         int32_t* d_status, void* stream);
+int pw_moe_route_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, const float* d_logits,
+                            int T, int H, int I, int E, int k, int32_t* d_ids, float* d_w,
+                            int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm,
+                            float* d_mass_accum, void* d_ws, size_t ws_bytes, uint16_t* d_y,
+                            int32_t* d_status, const pw_ffn_options* opts, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Test exports: they run the same device dequant code as the fused layer.     */
 /* ------------------------------------------------------------------------ */

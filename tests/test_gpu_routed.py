@@ -1,0 +1,111 @@
+"""GPU: the routed layer call (routing and the fused expert layer in one
+launch, pw_moe_route_apl_ffn) against the two-launch call (pw_moe_route_topk,
+then pw_moe_apl_ffn) on the same inputs -- the routing arrays, the routing
+mass and y must agree bit for bit -- and against the CPU oracle."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import apl
+
+pytestmark = pytest.mark.gpu
+
+pw = pytest.importorskip("any_precision_bit_pw_gb300.pw")
+from any_precision_bit_pw_gb300 import synth  # noqa: E402
+from any_precision_bit_pw_gb300.layer import APLMoEStack, MoECall, load_layer  # noqa: E402
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    import os
+    if not os.path.exists(pw.LIB_PATH):
+        import __graft_entry__
+        __graft_entry__.build()
+    pw.lib()
+    torch.cuda.set_device(0)
+
+
+def _stack(li):
+    sh = li.wl.shape
+    st = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, li.wl.parent_bits, li.wl.seed_bits, DEV)
+    load_layer(st, 0, li)
+    st.sync()
+    return st
+
+
+def _routing(call):
+    r = call.route
+    return [t.cpu().numpy().copy() for t in (r.ids, r.w, r.offsets, r.perm, r.inv_perm)]
+
+
+# (workload, tokens): 16-token tiles, 32-token tiles, the prefill path (a
+# routing launch before the fused one), and a tiny shape
+CASES = [("tiny", 16), ("tiny", 40), ("8x7b", 32), ("8x7b", 100), ("8x7b", 256), ("8x7b", 3)]
+
+
+def _inputs(name, T):
+    wl = synth.TINY_LAYER if name == "tiny" else synth.MIXTRAL_8X7B_DECODE
+    return synth.layer_inputs(wl.with_(tokens=T), device=DEV)
+
+
+@pytest.mark.parametrize("name,T", CASES)
+def test_routed_call_equals_two_launch_call(name, T):
+    li = _inputs(name, T)
+    st = _stack(li)
+    fused, split = MoECall(st, T, fused=True), MoECall(st, T, fused=False)
+    for rep in range(3):   # the routing mass accumulates across calls
+        yf = fused(0, li.x, li.logits).clone()
+        ys = split(0, li.x, li.logits).clone()
+        torch.cuda.synchronize()
+        assert int(fused.status.item()) == 0 and int(split.status.item()) == 0
+        for a, b in zip(_routing(fused), _routing(split)):
+            assert np.array_equal(a, b)
+        assert torch.equal(yf, ys)
+        assert torch.equal(fused.mass, split.mass)
+    # and the routing is the oracle's
+    r = apl.route_topk(li.logits.cpu().numpy(), li.wl.shape.top_k)
+    ids, w, offsets, perm, inv_perm = _routing(fused)
+    assert np.array_equal(ids, r["ids"])
+    assert np.array_equal(offsets, r["offsets"])
+    assert np.array_equal(perm, r["perm"])
+    assert np.array_equal(inv_perm, r["inv_perm"])
+    np.testing.assert_allclose(w, r["w"], atol=1e-6, rtol=0)
+
+
+def test_routed_call_matches_oracle_8x7b_decode():
+    li = synth.layer_inputs(synth.MIXTRAL_8X7B_DECODE, device=DEV)
+    st = _stack(li)
+    call = MoECall(st, li.x.shape[0], fused=True)
+    y = call(0, li.x, li.logits).float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(call.status.item()) == 0
+    sh = li.wl.shape
+    toks = [0, 17]
+    r = apl.route_topk(li.logits.cpu().numpy(), sh.top_k)
+
+    def blocks(e, u):
+        idx = li.idx[(e, u)].cpu().numpy()
+        return apl.IndexBlock(idx, {b: t.cpu().numpy() for b, t in li.luts[(e, u)].items()}, li.bits[2 * e + u],
+                              li.wl.parent_bits)
+    y_ref = apl.moe_layer(li.x.cpu().numpy(), r["ids"], r["w"], sh.intermediate, blocks, tokens=toks)
+    m = apl.compare(y_ref[toks], y[toks])
+    assert m["rel_l2"] <= 2e-3 and m["max_abs_over_rms"] <= 1e-2, m
+
+
+def test_routed_call_zero_tokens():
+    li = _inputs("tiny", 16)
+    st = _stack(li)
+    call = MoECall(st, 0, fused=True)
+    sh = li.wl.shape
+    call.route.offsets.fill_(-1)
+    x = torch.empty((0, sh.hidden), dtype=torch.float16, device=DEV)
+    lg = torch.empty((0, sh.experts), dtype=torch.float32, device=DEV)
+    pw.pw_moe_route_apl_ffn(st.desc, 0, x, lg, sh.intermediate, sh.experts, sh.top_k, call.route.ids,
+                            call.route.w, call.route.offsets, call.route.perm, call.route.inv_perm, None, call.ws,
+                            call.y, call.status)
+    torch.cuda.synchronize()
+    assert call.route.offsets.cpu().tolist() == [0] * (sh.experts + 1)

@@ -155,3 +155,15 @@ def test_workspace_and_host_validation(L):
     rc = L.pw_moe_route_topk(None, 4, 8, 9, None, None, None, None, None, None, None)
     assert rc == pw.PW_ERR_UNSUPPORTED
     assert "k <=" in pw.pw_last_error()
+
+
+def test_routed_ffn_checks_arguments_before_any_launch(L):
+    """The routed layer call rejects missing logits and routing outputs on the
+    host (no device is touched)."""
+    rc = L.pw_moe_route_apl_ffn(None, 0, None, None, 4, 128, 128, 4, 2, None, None, None, None, None, None,
+                                None, 0, None, None, None)
+    assert rc == pw.PW_ERR_INVALID_ARG and "logits" in pw.pw_last_error()
+    fake = 0x7F0000000000
+    rc = L.pw_moe_route_apl_ffn(fake, 0, fake, fake, 4, 128, 128, 4, 2, None, fake, None, fake, fake, None,
+                                fake, 1 << 20, fake, fake, None)
+    assert rc == pw.PW_ERR_INVALID_ARG and "ids and offsets" in pw.pw_last_error()
