@@ -11,6 +11,14 @@
 // The table borrows device pointers; it never allocates device memory.  A page
 // is "attached" when the caller has handed its buffer to the table (the
 // GPU-resident state); detaching it on a lowering hands ownership back.
+//
+// §3.3 asynchronous page movement: a page can also hold a host copy (CPU
+// resident) and be in transfer.  Offload and reload are one cudaMemcpyAsync
+// each on the caller's copy stream, tracked by an event the table owns; the
+// table learns of completion only in pw_page_table_poll, so a reloaded page is
+// attached (and q_i can be raised) only after its copy has finished, and a
+// page above q_i whose offload copy is still in flight stays attached until
+// the copy has finished.
 #include <cstring>
 #include <vector>
 
@@ -18,12 +26,25 @@
 
 namespace {
 
+constexpr int kPages = 2 * PW_MAX_BITS + 1;   // page ids: plane p = p, LUT of bitwidth b = 8 + b
+enum : int { kXferNone = 0, kXferToCpu = 1, kXferToGpu = 2 };
+
+struct PageXfer {
+  void* host = nullptr;       // host copy (complete once `cpu`)
+  bool cpu = false;
+  int xfer = kXferNone;
+  void* pending = nullptr;    // reload destination, attached when the copy completes
+  cudaEvent_t ev = nullptr;
+};
+
 struct BlockState {
   pw_block_info info{};
   int q = 0;
   int d = 0;
   const uint32_t* planes[PW_MAX_BITS] = {};
   const uint16_t* luts[PW_MAX_BITS + 1] = {};
+  PageXfer pages[kPages];
+  uint64_t released_late = 0;   // pages above q detached by poll after their offload copy
 };
 
 bool bits_ok(const BlockState& b, int bits) {
@@ -44,6 +65,30 @@ int64_t block_bytes(const pw_block_info& in, int b) {
   int64_t bytes = static_cast<int64_t>(b) * in.rows * in.cols / 8;
   for (int k = in.seed_bits; k <= b; ++k) bytes += in.rows * (int64_t{1} << k) * 2;
   return bytes;
+}
+
+int64_t page_bytes(const BlockState& b, int page) {
+  if (page >= 0 && page < b.info.parent_bits) return b.info.rows * b.info.cols / 8;
+  const int k = page - PW_MAX_BITS;
+  if (page >= PW_MAX_BITS && page < kPages && bits_ok(b, k)) return b.info.rows * (int64_t{1} << k) * 2;
+  return -1;
+}
+
+const void* attached(const BlockState& b, int page) {
+  return page < PW_MAX_BITS ? static_cast<const void*>(b.planes[page])
+                            : static_cast<const void*>(b.luts[page - PW_MAX_BITS]);
+}
+
+void set_attached(BlockState& b, int page, const void* d) {
+  if (page < PW_MAX_BITS)
+    b.planes[page] = static_cast<const uint32_t*>(d);
+  else
+    b.luts[page - PW_MAX_BITS] = static_cast<const uint16_t*>(d);
+}
+
+// Referenced by the committed bitwidth (planes 0..q-1, LUTs seed..q).
+bool referenced(const BlockState& b, int page) {
+  return page < PW_MAX_BITS ? page < b.q : (page - PW_MAX_BITS) <= b.q;
 }
 
 }  // namespace
@@ -91,6 +136,14 @@ int pw_page_table_create(pw_page_table** out, int n_blocks, const pw_block_info*
 }
 
 int pw_page_table_destroy(pw_page_table* t) {
+  if (!t) return PW_OK;
+  // transfers still in flight finish before their events go away
+  for (BlockState& b : t->blocks)
+    for (PageXfer& x : b.pages)
+      if (x.ev) {
+        if (x.xfer != kXferNone) cudaEventSynchronize(x.ev);
+        cudaEventDestroy(x.ev);
+      }
   delete t;
   return PW_OK;
 }
@@ -102,6 +155,8 @@ int pw_page_table_attach_plane(pw_page_table* t, int block, int plane, const uin
     return pw::set_error(PW_ERR_INVALID_ARG, "plane %d outside [0, %d)", plane, b.info.parent_bits);
   if (!d_plane || (reinterpret_cast<uintptr_t>(d_plane) & 15))
     return pw::set_error(PW_ERR_INVALID_ARG, "plane pointer must be non-NULL and 16-byte aligned");
+  if (b.pages[plane].xfer != kXferNone)
+    return pw::set_error(PW_ERR_BUSY, "block %d: plane %d has a transfer in flight", block, plane);
   b.planes[plane] = d_plane;
   return PW_OK;
 }
@@ -114,6 +169,8 @@ int pw_page_table_attach_lut(pw_page_table* t, int block, int bits, const uint16
                          b.info.parent_bits);
   if (!d_lut || (reinterpret_cast<uintptr_t>(d_lut) & 15))
     return pw::set_error(PW_ERR_INVALID_ARG, "LUT pointer must be non-NULL and 16-byte aligned");
+  if (b.pages[PW_MAX_BITS + bits].xfer != kXferNone)
+    return pw::set_error(PW_ERR_BUSY, "block %d: LUT %d has a transfer in flight", block, bits);
   b.luts[bits] = d_lut;
   return PW_OK;
 }
@@ -147,15 +204,17 @@ int pw_page_table_set_bits(pw_page_table* t, int block, int q, uint64_t* release
     return PW_OK;
   }
   // lowering (or recommitting): commit first, then retire every page above q
+  // (a page whose offload copy is still in flight is retired by the poll that
+  // sees the copy finish)
   b.q = q;
   uint64_t mask = 0;
   for (int p = q; p < PW_MAX_BITS; ++p)
-    if (b.planes[p]) {
+    if (b.planes[p] && b.pages[p].xfer != kXferToCpu) {
       mask |= 1ull << p;
       b.planes[p] = nullptr;
     }
   for (int k = q + 1; k <= PW_MAX_BITS; ++k)
-    if (b.luts[k]) {
+    if (b.luts[k] && b.pages[PW_MAX_BITS + k].xfer != kXferToCpu) {
       mask |= 1ull << (8 + k);
       b.luts[k] = nullptr;
     }
@@ -208,6 +267,112 @@ int pw_page_table_sync(pw_page_table* t, void* d_desc, size_t desc_bytes, void* 
   // The staging vector is pageable host memory: cudaMemcpyAsync copies it to
   // a driver staging buffer before returning, so it may be reused right away.
   PW_CUDA_TRY(cudaMemcpyAsync(d_desc, t->staging.data(), need, cudaMemcpyHostToDevice, pw::as_stream(stream)));
+  return PW_OK;
+}
+
+int64_t pw_page_bytes(const pw_page_table* t, int block, int page) {
+  if (check_block(t, block)) return -1;
+  return page_bytes(t->blocks[block], page);
+}
+
+int pw_page_offload(pw_page_table* t, int block, int page, void* h_dst, void* copy_stream) {
+  if (int e = check_block(t, block)) return e;
+  BlockState& b = t->blocks[block];
+  const int64_t bytes = page_bytes(b, page);
+  if (bytes < 0) return pw::set_error(PW_ERR_INVALID_ARG, "block %d: no page %d", block, page);
+  if (!h_dst) return pw::set_error(PW_ERR_INVALID_ARG, "offload: NULL host buffer");
+  PageXfer& x = b.pages[page];
+  if (x.xfer != kXferNone) return pw::set_error(PW_ERR_BUSY, "block %d: page %d has a transfer in flight", block, page);
+  const void* d = attached(b, page);
+  if (!d) return pw::set_error(PW_ERR_NOT_RESIDENT, "block %d: page %d is not GPU-resident", block, page);
+  if (!x.ev) PW_CUDA_TRY(cudaEventCreateWithFlags(&x.ev, cudaEventDisableTiming));
+  cudaStream_t s = pw::as_stream(copy_stream);
+  PW_CUDA_TRY(cudaMemcpyAsync(h_dst, d, static_cast<size_t>(bytes), cudaMemcpyDeviceToHost, s));
+  PW_CUDA_TRY(cudaEventRecord(x.ev, s));
+  x.host = h_dst;
+  x.cpu = false;
+  x.xfer = kXferToCpu;
+  return PW_OK;
+}
+
+int pw_page_reload(pw_page_table* t, int block, int page, const void* h_src, void* d_dst, void* copy_stream) {
+  if (int e = check_block(t, block)) return e;
+  BlockState& b = t->blocks[block];
+  const int64_t bytes = page_bytes(b, page);
+  if (bytes < 0) return pw::set_error(PW_ERR_INVALID_ARG, "block %d: no page %d", block, page);
+  if (!d_dst || (reinterpret_cast<uintptr_t>(d_dst) & 15))
+    return pw::set_error(PW_ERR_INVALID_ARG, "reload: device buffer must be non-NULL and 16-byte aligned");
+  PageXfer& x = b.pages[page];
+  if (x.xfer != kXferNone) return pw::set_error(PW_ERR_BUSY, "block %d: page %d has a transfer in flight", block, page);
+  if (attached(b, page)) return pw::set_error(PW_ERR_INVALID_ARG, "block %d: page %d is already GPU-resident", block, page);
+  const void* src = h_src ? h_src : (x.cpu ? x.host : nullptr);
+  if (!src) return pw::set_error(PW_ERR_NOT_RESIDENT, "block %d: page %d has no host copy", block, page);
+  if (!x.ev) PW_CUDA_TRY(cudaEventCreateWithFlags(&x.ev, cudaEventDisableTiming));
+  cudaStream_t s = pw::as_stream(copy_stream);
+  PW_CUDA_TRY(cudaMemcpyAsync(d_dst, src, static_cast<size_t>(bytes), cudaMemcpyHostToDevice, s));
+  PW_CUDA_TRY(cudaEventRecord(x.ev, s));
+  x.pending = d_dst;
+  x.xfer = kXferToGpu;
+  return PW_OK;
+}
+
+int pw_page_table_poll(pw_page_table* t, int* in_flight) {
+  if (in_flight) *in_flight = 0;
+  if (!t) return pw::set_error(PW_ERR_INVALID_ARG, "page table is NULL");
+  int pending = 0;
+  for (size_t bi = 0; bi < t->blocks.size(); ++bi) {
+    BlockState& b = t->blocks[bi];
+    for (int page = 0; page < kPages; ++page) {
+      PageXfer& x = b.pages[page];
+      if (x.xfer == kXferNone) continue;
+      const cudaError_t r = cudaEventQuery(x.ev);
+      if (r == cudaErrorNotReady) {
+        ++pending;
+        continue;
+      }
+      if (r != cudaSuccess) return pw::cuda_error(r, "cudaEventQuery (page transfer)");
+      if (x.xfer == kXferToCpu) {
+        x.cpu = true;
+        if (!referenced(b, page) && attached(b, page)) {
+          set_attached(b, page, nullptr);
+          b.released_late |= 1ull << page;
+        }
+      } else {
+        set_attached(b, page, x.pending);
+        x.pending = nullptr;
+      }
+      x.xfer = kXferNone;
+    }
+  }
+  if (in_flight) *in_flight = pending;
+  return PW_OK;
+}
+
+int pw_page_table_take_released(pw_page_table* t, int block, uint64_t* released_mask) {
+  if (released_mask) *released_mask = 0;
+  if (int e = check_block(t, block)) return e;
+  BlockState& b = t->blocks[block];
+  if (released_mask) *released_mask = b.released_late;
+  b.released_late = 0;
+  return PW_OK;
+}
+
+int pw_page_state(const pw_page_table* t, int block, int page, int* state, const void** d_ptr, void** h_ptr) {
+  if (state) *state = 0;
+  if (d_ptr) *d_ptr = nullptr;
+  if (h_ptr) *h_ptr = nullptr;
+  if (int e = check_block(t, block)) return e;
+  const BlockState& b = t->blocks[block];
+  if (page_bytes(b, page) < 0) return pw::set_error(PW_ERR_INVALID_ARG, "block %d: no page %d", block, page);
+  const PageXfer& x = b.pages[page];
+  int st = 0;
+  if (attached(b, page)) st |= PW_PAGE_GPU;
+  if (x.cpu) st |= PW_PAGE_CPU;
+  if (x.xfer == kXferToCpu) st |= PW_PAGE_TO_CPU;
+  if (x.xfer == kXferToGpu) st |= PW_PAGE_TO_GPU;
+  if (state) *state = st;
+  if (d_ptr) *d_ptr = attached(b, page);
+  if (h_ptr) *h_ptr = x.host;
   return PW_OK;
 }
 

@@ -39,6 +39,10 @@ class APLMoEStack:
         self.table = pw.pw_page_table_create(infos)
         self.planes: Dict[int, List[Optional[torch.Tensor]]] = {}
         self.luts: Dict[int, Dict[int, torch.Tensor]] = {}
+        self.host: Dict[tuple, torch.Tensor] = {}   # (block, page) -> pinned host copy
+        self.host_bytes = 0                          # bytes of host copies started
+        self.host_alloc = lambda n: torch.empty(n, dtype=torch.uint8, pin_memory=True)
+        self._moving = set()                         # blocks with transfers started since the last poll
         nbytes = pw.pw_desc_bytes(self.n_blocks)
         self.desc = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
 
@@ -93,6 +97,79 @@ class APLMoEStack:
             if mask >> (8 + b) & 1:
                 self.luts[block].pop(b, None)
         return before - self.resident_bytes_of(block)
+
+    # -- asynchronous page movement (§3.3, Figure 4) -------------------------
+    def pages_between(self, block: int, lo: int, hi: int) -> List[int]:
+        """Page ids a block holds at bitwidth hi but not at lo: planes lo..hi-1
+        and the LUTs of bitwidths lo+1..hi."""
+        return list(range(lo, hi)) + [pw.PW_PAGE_LUT(b) for b in range(max(lo + 1, self.S), hi + 1)]
+
+    def offload(self, block: int, q: int, copy_stream: torch.cuda.Stream) -> int:
+        """Lower a block to q keeping host copies of the pages above q: start
+        copying each of them to pinned host memory on `copy_stream`, then commit
+        q.  Pages whose copy is still running stay on the GPU until a later
+        poll() sees the copy finish.  Returns the bytes the commit releases
+        (Eq. 3)."""
+        cur = self.committed_bits(block)
+        copy_stream.wait_stream(torch.cuda.current_stream(self.device))
+        for page in self.pages_between(block, q, cur):
+            st, _, _ = pw.pw_page_state(self.table, block, page)
+            if not st & pw.PW_PAGE_GPU or st & pw.PW_PAGE_CPU:
+                continue
+            host = self.host.get((block, page))
+            if host is None:
+                host = self.host_alloc(pw.pw_page_bytes(self.table, block, page))
+                self.host[(block, page)] = host
+            pw.pw_page_offload(self.table, block, page, host, stream=copy_stream)
+            self.host_bytes += pw.pw_page_bytes(self.table, block, page)
+            self._moving.add(block)
+        return self.commit(block, q)
+
+    def reload(self, block: int, q: int, copy_stream: torch.cuda.Stream) -> None:
+        """Start restoring a block's pages up to bitwidth q from their host
+        copies into new device buffers on `copy_stream`; raise_to(q) succeeds
+        once poll() has seen every copy finish."""
+        cur = self.committed_bits(block)
+        for page in self.pages_between(block, cur, q):
+            st, _, _ = pw.pw_page_state(self.table, block, page)
+            if st & (pw.PW_PAGE_GPU | pw.PW_PAGE_TO_GPU):
+                continue
+            dev = torch.empty(pw.pw_page_bytes(self.table, block, page), dtype=torch.uint8, device=self.device)
+            dev.record_stream(copy_stream)
+            pw.pw_page_reload(self.table, block, page, None, dev, stream=copy_stream)
+            self._moving.add(block)
+            if page < pw.PW_MAX_BITS:
+                self.planes[block][page] = dev
+            else:
+                self.luts[block][page - pw.PW_MAX_BITS] = dev
+
+    def poll(self) -> int:
+        """Advance finished page transfers and drop the device buffers of pages
+        the table retired after their offload copy; returns the transfers
+        still running."""
+        n = pw.pw_page_table_poll(self.table)
+        for block in sorted(self._moving):
+            m = pw.pw_page_table_take_released(self.table, block)
+            for p in range(self.P):
+                if m >> p & 1:
+                    self.planes[block][p] = None
+            for b in range(self.S, self.P + 1):
+                if m >> (8 + b) & 1:
+                    self.luts[block].pop(b, None)
+        if n == 0:
+            self._moving.clear()
+        return n
+
+    def raise_to(self, block: int, q: int) -> bool:
+        """Commit a higher bitwidth if its pages are GPU-resident (after
+        reload() and a poll() that saw the copies finish); False otherwise."""
+        try:
+            self.commit(block, q)
+            return True
+        except pw.PwError as e:
+            if e.code == pw.PW_ERR_NOT_RESIDENT:
+                return False
+            raise
 
     def block_bytes_at(self, block: int, q: int) -> int:
         """M_i^q of Eq. 3 for a block (page-table arithmetic)."""

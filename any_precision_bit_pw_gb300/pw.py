@@ -23,19 +23,28 @@ PW_ERR_NOT_RESIDENT = -3
 PW_ERR_CUDA = -4
 PW_ERR_TIMEOUT = -5
 PW_ERR_WORKSPACE = -6
+PW_ERR_BUSY = -7
+PW_PAGE_GPU, PW_PAGE_CPU, PW_PAGE_TO_CPU, PW_PAGE_TO_GPU = 1, 2, 4, 8
+
+
+def PW_PAGE_LUT(b: int) -> int:
+    return 8 + b
+
 PW_LAYOUT_TILED = 1
 PW_MAX_BITS = 8
 PW_PATH_AUTO, PW_PATH_DECODE, PW_PATH_PREFILL = 0, 1, 2
 PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL = 1
 
 ERR_NAMES = {0: "PW_OK", -1: "PW_ERR_INVALID_ARG", -2: "PW_ERR_UNSUPPORTED", -3: "PW_ERR_NOT_RESIDENT",
-             -4: "PW_ERR_CUDA", -5: "PW_ERR_TIMEOUT", -6: "PW_ERR_WORKSPACE"}
+             -4: "PW_ERR_CUDA", -5: "PW_ERR_TIMEOUT", -6: "PW_ERR_WORKSPACE", -7: "PW_ERR_BUSY"}
 
 EXPORTS = (
     "pw_last_error", "pw_plane_bytes", "pw_pack_bitplanes", "pw_desc_bytes", "pw_page_table_create",
     "pw_page_table_destroy", "pw_page_table_attach_plane", "pw_page_table_attach_lut",
     "pw_page_table_set_desired", "pw_page_table_set_bits", "pw_page_table_get", "pw_page_table_bytes",
     "pw_page_table_resident_bytes", "pw_page_table_sync", "pw_moe_route_topk",
+    "pw_page_bytes", "pw_page_offload", "pw_page_reload", "pw_page_table_poll", "pw_page_table_take_released",
+    "pw_page_state",
     "pw_moe_apl_ffn_workspace", "pw_moe_apl_ffn", "pw_moe_apl_ffn_ex", "pw_moe_apl_ffn_noalloc",
     "pw_moe_route_apl_ffn", "pw_moe_route_apl_ffn_ex",
     "pw_unpack_indices",
@@ -84,6 +93,12 @@ def lib() -> ctypes.CDLL:
             "pw_page_table_bytes": (I64, [P, I32, I32]),
             "pw_page_table_resident_bytes": (I64, [P]),
             "pw_page_table_sync": (I32, [P, P, SZ, P]),
+            "pw_page_bytes": (I64, [P, I32, I32]),
+            "pw_page_offload": (I32, [P, I32, I32, P, P]),
+            "pw_page_reload": (I32, [P, I32, I32, P, P, P]),
+            "pw_page_table_poll": (I32, [P, ctypes.POINTER(I32)]),
+            "pw_page_table_take_released": (I32, [P, I32, ctypes.POINTER(U64)]),
+            "pw_page_state": (I32, [P, I32, I32, ctypes.POINTER(I32), ctypes.POINTER(P), ctypes.POINTER(P)]),
             "pw_moe_route_topk": (I32, [P, I32, I32, I32, P, P, P, P, P, P, P]),
             "pw_moe_apl_ffn_workspace": (SZ, [I32, I32, I32, I32, I32]),
             "pw_moe_apl_ffn": (I32, [P, I32, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P, P, P]),
@@ -197,6 +212,44 @@ def pw_page_table_resident_bytes(t) -> int:
 
 def pw_page_table_sync(t, d_desc: torch.Tensor, stream=None) -> None:
     _check(lib().pw_page_table_sync(t, _ptr(d_desc), d_desc.numel() * d_desc.element_size(), _stream(stream)))
+
+
+def pw_page_bytes(t, block: int, page: int) -> int:
+    return int(lib().pw_page_bytes(t, block, page))
+
+
+def pw_page_offload(t, block: int, page: int, host: torch.Tensor, stream=None) -> None:
+    """Start copying a GPU-resident page into `host` (pinned, >= pw_page_bytes bytes)."""
+    if host.is_cuda or host.numel() * host.element_size() < pw_page_bytes(t, block, page):
+        raise ValueError("offload: need a host tensor of at least the page's bytes")
+    _check(lib().pw_page_offload(t, block, page, _ptr(host), _stream(stream)))
+
+
+def pw_page_reload(t, block: int, page: int, host: Optional[torch.Tensor], dev: torch.Tensor, stream=None) -> None:
+    """Start copying a page from `host` (None: the page's own host copy) into `dev`."""
+    if not dev.is_cuda or dev.numel() * dev.element_size() < pw_page_bytes(t, block, page):
+        raise ValueError("reload: need a device tensor of at least the page's bytes")
+    _check(lib().pw_page_reload(t, block, page, _ptr(host), _ptr(dev), _stream(stream)))
+
+
+def pw_page_table_poll(t) -> int:
+    """Advance finished transfers; returns the number still in flight."""
+    n = I32(0)
+    _check(lib().pw_page_table_poll(t, ctypes.byref(n)))
+    return int(n.value)
+
+
+def pw_page_table_take_released(t, block: int) -> int:
+    m = U64(0)
+    _check(lib().pw_page_table_take_released(t, block, ctypes.byref(m)))
+    return int(m.value)
+
+
+def pw_page_state(t, block: int, page: int):
+    """(state bits, attached device address or 0, host address or 0)."""
+    st, d, h = I32(0), P(), P()
+    _check(lib().pw_page_state(t, block, page, ctypes.byref(st), ctypes.byref(d), ctypes.byref(h)))
+    return int(st.value), int(d.value or 0), int(h.value or 0)
 
 
 def pw_moe_route_topk(logits: torch.Tensor, k: int, ids: torch.Tensor, w: torch.Tensor, offsets: torch.Tensor,

@@ -96,10 +96,17 @@ class StackRun:
     """L independent MoE layers on one GPU, stepped with fresh seeded inputs;
     every ``commit_every`` steps the schedule lowers blocks and the released
     plane/LUT tensors are dropped (their memory returns to the caching
-    allocator for later allocations on the stream)."""
+    allocator for later allocations on the stream).
+
+    With ``offload=True`` lowering follows §3.3's offload instead: the pages
+    above the new bitwidth are first copied to pinned host memory on a copy
+    stream (overlapping the next layer calls), q_i drops at once, and each
+    page's GPU buffer is dropped by the first step boundary whose poll sees its
+    copy finish.  Host buffers are slices of one pinned arena sized for every
+    page the schedule can lower (allocated up front, outside any timing)."""
 
     def __init__(self, wl, device, layers=None, commit_every: int = 8, n_commits: int = 7,
-                 final_fraction: float = 0.4):
+                 final_fraction: float = 0.4, offload: bool = False):
         from . import synth
         from .layer import APLMoEStack, MoECall, load_layer
         import torch
@@ -121,6 +128,15 @@ class StackRun:
         self.schedule = StackSchedule(self.L, sh.experts, wl.seed_bits, wl.parent_bits, block_bytes,
                                       commit_every, n_commits, final_fraction)
         self.step_no = 0
+        self.offload = offload
+        self.offloaded_bytes = 0
+        if offload:
+            st = self.stack
+            arena = sum(st.block_bytes_at(b, st.P) - st.block_bytes_at(b, st.S) for b in range(st.n_blocks))
+            self.arena = torch.empty(arena + 256 * 2 * st.P * st.n_blocks, dtype=torch.uint8, pin_memory=True)
+            self.arena_used = 0
+            self.copy_stream = torch.cuda.Stream(device=st.device)
+            st.host_alloc = self._host_slice
 
     def inputs(self, layer: int, step: int):
         dev = self.stack.device
@@ -140,16 +156,41 @@ class StackRun:
         self.step_no += 1
         return self.boundary()
 
+    def _host_slice(self, nbytes: int):
+        start = (self.arena_used + 255) & ~255
+        if start + nbytes > self.arena.numel():
+            raise RuntimeError("stack offload: host arena exhausted")
+        self.arena_used = start + nbytes
+        return self.arena[start:start + nbytes]
+
     def boundary(self):
         """Commit the schedule's lowering at a step boundary; returns the
         (block, q_old, q_new) steps committed and the bytes released."""
+        if self.offload:
+            self.stack.poll()      # drop GPU pages whose offload copy has finished
         if self.step_no % self.schedule.commit_every:
             return [], 0
         mass = self.call.mass.float().cpu().tolist()    # routing-mass numerators (Eq. 1)
         plan = self.schedule.at_boundary(self.step_no, mass)
         released = 0
         for (layer, e, u), _, new in plan:
-            released += self.stack.commit(self.stack.block_id(layer, e, u), new)
+            b = self.stack.block_id(layer, e, u)
+            if self.offload:
+                before = self.stack.host_bytes
+                released += self.stack.offload(b, new, self.copy_stream)
+                self.offloaded_bytes += self.stack.host_bytes - before
+            else:
+                released += self.stack.commit(b, new)
         if plan:
             self.stack.sync()
         return plan, released
+
+    def finish_offloads(self, limit_s: float = 60.0) -> None:
+        """Wait (host side) until every offload copy finished and its GPU pages
+        were dropped."""
+        import time
+        t0 = time.time()
+        while self.stack.poll() > 0:
+            if time.time() - t0 > limit_s:
+                raise RuntimeError("page copies did not finish")
+            time.sleep(0.001)

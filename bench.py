@@ -1,7 +1,7 @@
 """Benchmark of the fused mixed-precision Any-Precision MoE layer on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl pw|reference]
-                    [--workload NAME] [--tokens T] [--sweep PATH]
+                    [--workload NAME] [--tokens T] [--offload] [--sweep PATH]
 
 One step = one pass of the hot path over one batch: top-k routing and the
 fused expert layer (gather, gate_up at each block's committed bitwidth,
@@ -384,7 +384,7 @@ def stack_arm(args, rank, world, local_rank):
     sh = wl.shape
     T, H, E, L = wl.tokens, sh.hidden, sh.experts, wl.layers
     run = StackRun(wl, dev, commit_every=synth.STACK_COMMIT_EVERY,
-                   n_commits=synth.STACK_STEPS // synth.STACK_COMMIT_EVERY - 1)
+                   n_commits=synth.STACK_STEPS // synth.STACK_COMMIT_EVERY - 1, offload=args.offload)
     f8 = run.schedule.f8
     K = args.steps
     n_in = min(K, 16)
@@ -426,6 +426,8 @@ def stack_arm(args, rank, world, local_rank):
             plan, released = run.boundary()
             released_total += released
             commits += bool(plan)
+        if args.offload:
+            stream.wait_stream(run.copy_stream)   # copies that did not overlap count against the steps
         stop.record(stream)
         torch.cuda.synchronize()
     if world > 1:
@@ -480,6 +482,8 @@ def stack_arm(args, rank, world, local_rank):
                    "top_k": sh.top_k, "tokens": T, "parent_bits": wl.parent_bits, "seed_bits": wl.seed_bits,
                    "commit_every": synth.STACK_COMMIT_EVERY, "commits_in_timed_region": commits,
                    "released_bytes": released_total, "resident_bytes_first_last": [resident[0], resident[-1]],
+                   "offload": ({"d2h_bytes": run.offloaded_bytes, "pinned_arena_bytes": int(run.arena.numel()),
+                                "copy_stream": "separate; the stop event waits for it"} if args.offload else None),
                    "f8_bytes": f8, "parallelism": f"replicas x{world}",
                    "l2": "no flush: the planes read per step (%.1f GB) exceed the 129 MB L2" % (nbytes.sum() / K / 1e9)},
         "roofline": roofline,
@@ -630,6 +634,8 @@ def main():
     ap.add_argument("--impl", default="pw", choices=["pw", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--tokens", type=int, default=None, help="replace the workload's token count")
+    ap.add_argument("--offload", action="store_true",
+                    help="stack workload: lowering copies the released pages to pinned host memory first (§3.3)")
     ap.add_argument("--sweep", default=None, help="also run the uniform-bitwidth sweep, JSON to this path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)

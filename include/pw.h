@@ -40,6 +40,7 @@ extern "C" {
 #define PW_ERR_CUDA (-4)          /* a CUDA runtime call failed; see pw_last_error() */
 #define PW_ERR_TIMEOUT (-5)       /* a bounded in-kernel wait ran out (device status only) */
 #define PW_ERR_WORKSPACE (-6)     /* workspace too small or misaligned */
+#define PW_ERR_BUSY (-7)          /* a transfer of this page is still in flight */
 
 #define PW_MAX_BITS 8
 #define PW_LAYOUT_TILED 1
@@ -118,8 +119,10 @@ int pw_page_table_set_desired(pw_page_table* t, int block, int d);
  *  Lowering (q < q_i): commits q at once; planes q..P-1 and LUTs q+1..P become
  *  unreferenced, are detached, and are reported in *released_mask (bit p for
  *  plane p, bit 8+b for the LUT of bitwidth b) so the caller can free them
- *  once the stream has passed every launch that used them.  The planes below
- *  q are not touched.
+ *  once the stream has passed every launch that used them -- except pages
+ *  whose offload copy is still in flight, which stay attached until
+ *  pw_page_table_poll sees the copy finish (see pw_page_offload).  The planes
+ *  below q are not touched.
  *  Raising (q > q_i): only allowed once planes 0..q-1 and the LUTs seed..q are
  *  attached (reload first, then raise); otherwise PW_ERR_NOT_RESIDENT and
  *  nothing changes.  q must be in B_i.  released_mask may be NULL. */
@@ -142,6 +145,65 @@ int64_t pw_page_table_resident_bytes(const pw_page_table* t);
  * with an asynchronous copy on `stream`.  The fused kernels read only this
  * array, so a commit becomes visible to launches enqueued after the sync. */
 int pw_page_table_sync(pw_page_table* t, void* d_desc, size_t desc_bytes, void* stream);
+
+/* ------------------------------------------------------------------------ */
+/* Asynchronous page movement (§3.1 page states; §3.3 and Figure 4)          */
+/* ------------------------------------------------------------------------ */
+/* A weight page is one bit-plane or the LUT of one bitwidth of a block.  Page
+ * ids: plane p (0 = MSB) is page p; the LUT of bitwidth b is page 8 + b.  A
+ * page is GPU-resident (attached), may also hold a complete host copy
+ * (CPU-resident), and may be in transfer.  Transfers are one cudaMemcpyAsync
+ * each on the caller's copy stream (normally not the compute stream, so the
+ * copies overlap the fused layer), tracked by an event the table owns; the
+ * table notices that a transfer finished only in pw_page_table_poll.
+ *
+ * Offload (§3.3): pw_page_offload copies a GPU-resident page to host memory;
+ * the caller then lowers q_i with pw_page_table_set_bits, which retires pages
+ * above q_i at once unless their offload copy is still in flight -- those
+ * stay attached until the poll that sees the copy finish detaches them and
+ * reports them through pw_page_table_take_released.  Reload (§3.1 ordering):
+ * pw_page_reload copies the host copy into a caller device buffer; the page
+ * is attached only by the poll that sees the copy finish, so raising q_i
+ * before then fails with PW_ERR_NOT_RESIDENT.  Buffers stay caller-owned; the
+ * host buffers should be pinned for the copies to run asynchronously. */
+#define PW_PAGE_LUT(b) (8 + (b))
+#define PW_PAGE_GPU 1      /* attached: usable by the kernels when committed */
+#define PW_PAGE_CPU 2      /* a complete host copy exists */
+#define PW_PAGE_TO_CPU 4   /* offload copy in flight */
+#define PW_PAGE_TO_GPU 8   /* reload copy in flight */
+
+/* Bytes of a page (rows*cols/8 for a plane, rows*2^b*2 for LUT b); -1 if the
+ * block or page does not exist. */
+int64_t pw_page_bytes(const pw_page_table* t, int block, int page);
+
+/* Start copying a GPU-resident page to h_dst (pw_page_bytes bytes) on
+ * copy_stream.  PW_ERR_NOT_RESIDENT if the page is not attached, PW_ERR_BUSY
+ * if a transfer of it is in flight.  The copy reads the attached buffer, so
+ * the caller orders copy_stream after whatever wrote it. */
+int pw_page_offload(pw_page_table* t, int block, int page, void* h_dst, void* copy_stream);
+
+/* Start copying a page from host memory (h_src, or when h_src is NULL the
+ * page's own completed host copy) into d_dst (16-byte aligned, pw_page_bytes
+ * bytes) on copy_stream.  The page must not be attached (PW_ERR_INVALID_ARG)
+ * and must have no transfer in flight (PW_ERR_BUSY); PW_ERR_NOT_RESIDENT if
+ * h_src is NULL and no host copy exists. */
+int pw_page_reload(pw_page_table* t, int block, int page, const void* h_src, void* d_dst, void* copy_stream);
+
+/* Advance every finished transfer: an offload marks the host copy complete
+ * and detaches the page if it is above q_i; a reload attaches its buffer.
+ * *in_flight (may be NULL) gets the number of transfers still running.
+ * Host only: never waits. */
+int pw_page_table_poll(pw_page_table* t, int* in_flight);
+
+/* Pages of a block that a poll detached after their offload copy finished
+ * (bit p plane p, bit 8+b LUT b), cleared by the call; the caller frees those
+ * device buffers once the compute stream is past the launches that used
+ * them. */
+int pw_page_table_take_released(pw_page_table* t, int block, uint64_t* released_mask);
+
+/* State bits (PW_PAGE_*) of a page, its attached device buffer and its host
+ * buffer; any out pointer may be NULL. */
+int pw_page_state(const pw_page_table* t, int block, int page, int* state, const void** d_ptr, void** h_ptr);
 
 /* ------------------------------------------------------------------------ */
 /* Routing (§2.1: top-K experts per token; Eq. 1: routing mass)                */

@@ -84,3 +84,63 @@ def test_stack_commits_release_pages_and_keep_parity():
                 assert run.stack.committed_bits(run.stack.block_id(l, e, u)) <= n
     assert commits == 2
     assert run.stack.resident_bytes() <= 0.55 * f8
+
+
+def test_stack_offload_keeps_host_copies_and_parity():
+    """The stack driver in offload mode (§3.3) on a three-layer tiny stack:
+    lowering copies the released pages to pinned host memory first; once the
+    copies finished, every page above its block's committed bitwidth is
+    CPU-resident only and its host bytes are the oracle's packed plane (or the
+    LUT); layer outputs follow the committed bitwidths; reloading every
+    lowered block and raising it back restores the 4-bit outputs."""
+    wl = synth.TINY_LAYER.with_(name="tiny_stack", tokens=24, bits_mode="fixed", fixed_bits=4,
+                                logits_mode="biased", layers=3)
+    run = StackRun(wl, DEV, commit_every=2, n_commits=2, final_fraction=0.6, offload=True)
+    st = run.stack
+    P, S = wl.parent_bits, wl.seed_bits
+    for _ in range(4):
+        run.step()            # runs the step boundary (commits at steps 2 and 4)
+        run.finish_offloads()
+    torch.cuda.synchronize()
+    assert run.offloaded_bytes > 0
+    assert st.resident_bytes() == run.schedule.resident_bytes()
+    lowered = []
+    for (layer, e, u), q in run.schedule.bits.items():
+        b = st.block_id(layer, e, u)
+        assert st.committed_bits(b) == q
+        if q == P:
+            continue
+        lowered.append((b, layer, e, u, q))
+        idx = synth.parent_indices(wl, layer, e, u, DEV).cpu().numpy()
+        ref_planes = apl.pack_bitplanes(idx, P)
+        for page in st.pages_between(b, q, P):
+            state, d, h = pw.pw_page_state(st.table, b, page)
+            assert state == pw.PW_PAGE_CPU and d == 0 and h != 0
+            host = st.host[(b, page)].numpy()
+            if page < pw.PW_MAX_BITS:
+                assert np.array_equal(host, np.ascontiguousarray(ref_planes[page]).view(np.uint8).reshape(-1))
+            else:
+                lut = synth.lut(wl, layer, e, u, page - pw.PW_MAX_BITS, DEV).cpu().numpy()
+                assert np.array_equal(host, lut.view(np.uint8).reshape(-1))
+    assert lowered
+    # outputs at the committed bitwidths
+    for layer in range(run.L):
+        x, lg = run.inputs(layer, 0)
+        y = run.call(layer, x, lg).float().cpu().numpy()
+        torch.cuda.synchronize()
+        bits = {(e, u): st.committed_bits(st.block_id(layer, e, u)) for e in range(wl.shape.experts) for u in (0, 1)}
+        _check_layer(run, layer, 0, y, bits)
+    # reload every lowered block and raise it back to the parent bitwidth
+    for b, *_ in lowered:
+        st.reload(b, P, run.copy_stream)
+        assert not st.raise_to(b, P)
+    run.finish_offloads()
+    for b, *_ in lowered:
+        assert st.raise_to(b, P)
+    st.sync()
+    assert st.resident_bytes() == run.schedule.f8
+    for layer in range(run.L):
+        x, lg = run.inputs(layer, 0)
+        y = run.call(layer, x, lg).float().cpu().numpy()
+        torch.cuda.synchronize()
+        _check_layer(run, layer, 0, y, {(e, u): P for e in range(wl.shape.experts) for u in (0, 1)})

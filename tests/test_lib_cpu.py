@@ -167,3 +167,36 @@ def test_routed_ffn_checks_arguments_before_any_launch(L):
     rc = L.pw_moe_route_apl_ffn(fake, 0, fake, fake, 4, 128, 128, 4, 2, None, fake, None, fake, fake, None,
                                 fake, 1 << 20, fake, fake, None)
     assert rc == pw.PW_ERR_INVALID_ARG and "ids and offsets" in pw.pw_last_error()
+
+
+def test_page_movement_host_checks(L):
+    """Page ids, sizes and the checks pw_page_offload / pw_page_reload make
+    before any copy is enqueued (§3.1 page states)."""
+    import ctypes
+    t = _table(blocks=1, rows=128, cols=512, P=8, S=3)
+    try:
+        assert pw.pw_page_bytes(t, 0, 0) == 128 * 512 // 8
+        assert pw.pw_page_bytes(t, 0, 7) == 128 * 512 // 8
+        assert pw.pw_page_bytes(t, 0, pw.PW_PAGE_LUT(3)) == 128 * 8 * 2
+        assert pw.pw_page_bytes(t, 0, pw.PW_PAGE_LUT(8)) == 128 * 256 * 2
+        for bad in (-1, 8 + 2, 17):
+            assert pw.pw_page_bytes(t, 0, bad) == -1
+        assert pw.pw_page_state(t, 0, 2) == (0, 0, 0)
+        # offload of a page that is not GPU-resident
+        rc = L.pw_page_offload(t, 0, 2, ctypes.c_void_p(FAKE), None)
+        assert rc == pw.PW_ERR_NOT_RESIDENT
+        # reload without a host copy, and into a misaligned buffer
+        rc = L.pw_page_reload(t, 0, 2, None, ctypes.c_void_p(FAKE), None)
+        assert rc == pw.PW_ERR_NOT_RESIDENT
+        rc = L.pw_page_reload(t, 0, 2, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4), None)
+        assert rc == pw.PW_ERR_INVALID_ARG
+        # an attached page is GPU-resident; reloading into it is refused
+        pw.pw_page_table_attach_plane(t, 0, 2, FAKE)
+        assert pw.pw_page_state(t, 0, 2) == (pw.PW_PAGE_GPU, FAKE, 0)
+        rc = L.pw_page_reload(t, 0, 2, ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE), None)
+        assert rc == pw.PW_ERR_INVALID_ARG
+        # nothing in flight: poll touches no device and reports 0
+        assert pw.pw_page_table_poll(t) == 0
+        assert pw.pw_page_table_take_released(t, 0) == 0
+    finally:
+        pw.pw_page_table_destroy(t)
