@@ -55,7 +55,7 @@ WsLayout ws_layout(int T, int H, int I, int E, int k) {
 }
 
 int validate_shape(int T, int H, int I, int E, int k) {
-  if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxE || k < 1 || k > 8 || k > E)
+  if (T < 0 || H <= 0 || I <= 0 || E < 1 || E > kMaxE || k < 1 || k > 16 || k > E)
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: bad sizes T=%d H=%d I=%d E=%d k=%d", T, H, I, E, k);
   if (H % 128 || I % 128)
     return pw::set_error(PW_ERR_UNSUPPORTED, "ffn: H and I must be multiples of 128 (H=%d I=%d)", H, I);
@@ -91,15 +91,23 @@ int ffn_launch(bool routed, const void* d_desc, int layer, const uint16_t* d_x, 
                int I, int E, int k, int32_t* d_ids, const float* d_w, const int32_t* d_offsets,
                const int32_t* d_perm, const int32_t* d_inv_perm, float* d_mass_accum, void* d_ws, size_t ws_bytes,
                uint16_t* d_y, int32_t* d_status, const pw_ffn_options* opts, void* stream) {
+  // routed call: E and k count routed experts; the options add S shared
+  // experts (ids E .. E+S-1, one slot per token each, weight 1), so the layer
+  // runs over E + S experts and k + S slots per token
+  const int S = (routed && opts) ? opts->shared_experts : 0;
+  if (S < 0) return pw::set_error(PW_ERR_INVALID_ARG, "ffn: shared_experts %d", S);
+  const int ER = E, kR = k;
+  E += S;
+  k += S;
   if (int e = validate_shape(T, H, I, E, k)) return e;
   if (layer < 0) return pw::set_error(PW_ERR_INVALID_ARG, "ffn: layer %d", layer);
   if (routed && T > 0 && !d_logits) return pw::set_error(PW_ERR_INVALID_ARG, "routed ffn: NULL logits");
   if (routed && (!d_ids || !d_offsets))
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: routed call needs ids and offsets");
   if (T == 0)
-    return routed ? pw_moe_route_topk(d_logits, 0, E, k, d_ids, const_cast<float*>(d_w),
-                                      const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
-                                      const_cast<int32_t*>(d_inv_perm), d_mass_accum, stream)
+    return routed ? pw_moe_route_topk_shared(d_logits, 0, ER, kR, S, d_ids, const_cast<float*>(d_w),
+                                             const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
+                                             const_cast<int32_t*>(d_inv_perm), d_mass_accum, stream)
                   : PW_OK;
   if (!d_desc || !d_x || !d_w || !d_offsets || !d_perm || !d_inv_perm || !d_y || !d_status || !d_ws)
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: NULL argument");
@@ -144,12 +152,13 @@ int ffn_launch(bool routed, const void* d_desc, int layer, const uint16_t* d_x, 
   if (routed && path == PW_PATH_PREFILL) {
     // large batches: one CTA would route while the grid waits; a separate
     // routing launch comes first instead
-    if (int e = pw_moe_route_topk(d_logits, T, E, k, d_ids, const_cast<float*>(d_w),
-                                  const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
-                                  const_cast<int32_t*>(d_inv_perm), d_mass_accum, stream))
+    if (int e = pw_moe_route_topk_shared(d_logits, T, ER, kR, S, d_ids, const_cast<float*>(d_w),
+                                         const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
+                                         const_cast<int32_t*>(d_inv_perm), d_mass_accum, stream))
       return e;
   } else if (routed) {
     p.logits = d_logits;
+    p.route_shared = S;
     p.ids_out = d_ids;
     p.mass_accum = d_mass_accum;
   }

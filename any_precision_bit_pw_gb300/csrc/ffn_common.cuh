@@ -73,6 +73,7 @@ struct Params {
   const float* logits;
   int32_t* ids_out;
   float* mass_accum;
+  int route_shared;        // shared experts: the last route_shared of E, the last of k slots
   int32_t* status;
   uint64_t wait_ns;
   uint32_t flags;

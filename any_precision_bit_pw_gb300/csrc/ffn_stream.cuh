@@ -547,7 +547,9 @@ __device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint
   const int row = strip_pos_row(u.strip, pos, d.rows / 2);
   // 16 token columns at a time: the sum of the accumulators of the issuers
   // that hold a tile of the unit (issuer k holds x0 <= x < x0 + nt with
-  // x % kIssuers == k)
+  // x % kIssuers == k, i.e. the unit's tiles t with t = k - x0 mod kIssuers).
+  // The partial sums are added in the order of that residue, not of the
+  // issuer, so the result does not depend on which CTA took the unit.
 #pragma unroll 1
   for (int c16 = 0; c16 < kN / 16; ++c16) {
     float acc[16];
@@ -555,8 +557,9 @@ __device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint
     for (int n = 0; n < 16; ++n) acc[n] = 0.f;
     if (ok) {
       pw::tc_fence_after();
-      for (int k2 = 0; k2 < kIssuers; ++k2) {
-        if ((static_cast<uint32_t>(k2) - x0) % kIssuers >= nt) continue;
+      for (int r = 0; r < kIssuers; ++r) {
+        if (static_cast<uint32_t>(r) >= nt) continue;
+        const int k2 = static_cast<int>((static_cast<uint32_t>(r) + x0) % kIssuers);
         uint32_t v[16];
         pw::tmem_ld_x16(tmem + acc_col(db, k2) + 16u * c16 + (static_cast<uint32_t>(32 * qd) << 16), v);
         pw::tmem_ld_wait();
@@ -709,7 +712,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // one per SM)
   if (p.logits) {
     if (blockIdx.x == 0) {
-      pw_route::route_block(p.logits, p.T, p.E, p.k, p.ids_out, const_cast<float*>(p.w),
+      pw_route::route_block(p.logits, p.T, p.E - p.route_shared, p.k - p.route_shared, p.route_shared, p.ids_out,
+                            const_cast<float*>(p.w),
                             const_cast<int32_t*>(p.offsets), const_cast<int32_t*>(p.perm),
                             const_cast<int32_t*>(p.inv_perm), p.mass_accum, smem_raw + (sm.region - pw::smem_u32(smem_raw)));
       __syncthreads();

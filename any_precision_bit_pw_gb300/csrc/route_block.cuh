@@ -13,8 +13,8 @@
 
 namespace pw_route {
 
-constexpr int kMaxE = 256;
-constexpr int kMaxK = 8;
+constexpr int kMaxE = 256;   // routed + shared experts
+constexpr int kMaxK = 16;    // slots per token: routed top-k + shared experts
 
 // Shared-memory scratch of route_block: 3*E ints plus nwarps*E ints.
 __host__ __device__ constexpr size_t scratch_bytes(int E, int nwarps) {
@@ -22,21 +22,26 @@ __host__ __device__ constexpr size_t scratch_bytes(int E, int nwarps) {
 }
 
 // Every thread of the CTA calls this (it synchronises the CTA).  blockDim.x is
-// a multiple of 32; `scratch` is shared memory of scratch_bytes(E, warps).
-// Writes ids, w, offsets, perm and inv_perm (global); adds the routing mass of
-// the batch to mass_accum when it is not NULL, summed in a fixed order so that
+// a multiple of 32; `scratch` is shared memory of scratch_bytes(E + S, warps).
+// logits are [T][E] (routed experts).  Each token gets K = k + S slots: its
+// top-k routed experts, then the S shared experts E .. E+S-1 with weight 1
+// (experts every token passes through, added to the routed output).  Writes
+// ids [T][K], w [T][K], offsets [E+S+1], perm [T*K] and inv_perm [T*K]
+// (global); adds the routing mass of the batch (per expert, shared experts
+// included) to mass_accum when it is not NULL, summed in a fixed order so that
 // every result is the same from run to run.  The arrays are read back by this
 // CTA, so they must not alias the logits.
-__device__ inline void route_block(const float* __restrict__ logits, int T, int E, int k, int32_t* ids, float* w,
-                                   int32_t* offsets, int32_t* perm, int32_t* inv_perm, float* mass_accum,
-                                   uint8_t* scratch) {
+__device__ inline void route_block(const float* __restrict__ logits, int T, int E, int k, int S, int32_t* ids,
+                                   float* w, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
+                                   float* mass_accum, uint8_t* scratch) {
+  const int K = k + S, ET = E + S;
   const int nthreads = static_cast<int>(blockDim.x), nwarps = nthreads >> 5;
   const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, warp = tid >> 5;
   int* s_cnt = reinterpret_cast<int*>(scratch);
-  int* s_base = s_cnt + E;
-  int* s_chunk = s_base + E;
-  int* s_wcnt = s_chunk + E;   // [nwarps][E]
-  for (int e = tid; e < E; e += nthreads) s_cnt[e] = 0;
+  int* s_base = s_cnt + ET;
+  int* s_chunk = s_base + ET;
+  int* s_wcnt = s_chunk + ET;   // [nwarps][E + S]
+  for (int e = tid; e < ET; e += nthreads) s_cnt[e] = 0;
   __syncthreads();
 
   // 1) top-k per token: largest logit first, ties to the lower expert index;
@@ -99,12 +104,14 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
       if (j < k) den += expf(lsel[j] - lsel[0]);
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
-      if (j >= k) break;
-      const float wj = expf(lsel[j] - lsel[0]) / den;
-      ids[static_cast<long long>(t) * k + j] = sel[j];
-      w[static_cast<long long>(t) * k + j] = wj;
-      atomicAdd(&s_cnt[sel[j]], 1);
-      keep[j] = sel[j];
+      if (j >= K) break;
+      const bool routed = j < k;
+      const int e = routed ? sel[j] : E + (j - k);
+      const float wj = routed ? expf(lsel[j] - lsel[0]) / den : 1.0f;
+      ids[static_cast<long long>(t) * K + j] = e;
+      w[static_cast<long long>(t) * K + j] = wj;
+      atomicAdd(&s_cnt[e], 1);
+      keep[j] = e;
     }
   }
   __syncthreads();
@@ -112,12 +119,12 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
   // 2) expert offsets (exclusive scan of the counts)
   if (tid == 0) {
     int run = 0;
-    for (int e = 0; e < E; ++e) {
+    for (int e = 0; e < ET; ++e) {
       offsets[e] = run;
       s_base[e] = run;
       run += s_cnt[e];
     }
-    offsets[E] = run;
+    offsets[ET] = run;
   }
   __syncthreads();
 
@@ -130,25 +137,25 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
     int rank[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
-      my[j] = (valid && j < k) ? (one_pass ? keep[j] : ids[static_cast<long long>(t) * k + j]) : -1;
+      my[j] = (valid && j < K) ? (one_pass ? keep[j] : ids[static_cast<long long>(t) * K + j]) : -1;
       rank[j] = 0;
     }
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int e = 0; e < E; ++e) {
+    for (int e = 0; e < ET; ++e) {
       int jj = -1;
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j)
         if (my[j] == e) jj = j;
       const unsigned ball = __ballot_sync(0xffffffffu, jj >= 0);
       if (jj >= 0) rank[jj] = __popc(ball & lt_mask);
-      if (lane == 0) s_wcnt[warp * E + e] = __popc(ball);
+      if (lane == 0) s_wcnt[warp * ET + e] = __popc(ball);
     }
     __syncthreads();
-    for (int e = tid; e < E; e += nthreads) {
+    for (int e = tid; e < ET; e += nthreads) {
       int run = 0;
       for (int wi = 0; wi < nwarps; ++wi) {
-        const int v = s_wcnt[wi * E + e];
-        s_wcnt[wi * E + e] = run;
+        const int v = s_wcnt[wi * ET + e];
+        s_wcnt[wi * ET + e] = run;
         run += v;
       }
       s_chunk[e] = run;
@@ -157,16 +164,16 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
     if (valid) {
 #pragma unroll
       for (int j = 0; j < kMaxK; ++j) {
-        if (j >= k) break;
+        if (j >= K) break;
         const int e = my[j];
-        const int pos = s_base[e] + s_wcnt[warp * E + e] + rank[j];
-        const int slot = t * k + j;
+        const int pos = s_base[e] + s_wcnt[warp * ET + e] + rank[j];
+        const int slot = t * K + j;
         perm[pos] = slot;
         inv_perm[slot] = pos;
       }
     }
     __syncthreads();
-    for (int e = tid; e < E; e += nthreads) s_base[e] += s_chunk[e];
+    for (int e = tid; e < ET; e += nthreads) s_base[e] += s_chunk[e];
     __syncthreads();
   }
 
@@ -174,7 +181,7 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
   //    routing weights in expert order (lane-strided, then a fixed shuffle
   //    tree), one addition per expert per call
   if (mass_accum) {
-    for (int e = warp; e < E; e += nwarps) {
+    for (int e = warp; e < ET; e += nwarps) {
       float acc = 0.f;
       for (int pos = offsets[e] + lane; pos < offsets[e + 1]; pos += 32) acc += w[perm[pos]];
 #pragma unroll

@@ -15,6 +15,7 @@ arXiv text).
 """
 from __future__ import annotations
 
+import ctypes
 from dataclasses import dataclass
 from typing import Dict, List, Optional
 
@@ -27,11 +28,15 @@ GATE_UP, DOWN = 0, 1
 
 class APLMoEStack:
     def __init__(self, hidden: int, intermediate: int, experts: int, top_k: int, layers: int = 1,
-                 parent_bits: int = 8, seed_bits: int = 3, device="cuda"):
-        self.H, self.I, self.E, self.k, self.L = hidden, intermediate, experts, top_k, layers
+                 parent_bits: int = 8, seed_bits: int = 3, device="cuda", shared: int = 0):
+        # E counts every expert with blocks (routed, then `shared` shared
+        # experts that every token passes through with weight 1); k is the
+        # routed top-k
+        self.H, self.I, self.E, self.k, self.L = hidden, intermediate, experts + shared, top_k, layers
+        self.routed, self.shared = experts, shared
         self.P, self.S = parent_bits, seed_bits
         self.device = torch.device(device)
-        self.n_blocks = layers * experts * 2
+        self.n_blocks = layers * self.E * 2
         infos = []
         for b in range(self.n_blocks):
             rows, cols = self.block_shape(b % 2)
@@ -205,7 +210,7 @@ class MoECall:
 
     def __init__(self, stack: APLMoEStack, tokens: int, device=None, fused: bool = True):
         dev = stack.device if device is None else torch.device(device)
-        T, E, k = tokens, stack.E, stack.k
+        T, E, k = tokens, stack.E, stack.k + stack.shared   # all experts, slots per token
         self.stack, self.T, self.fused = stack, T, fused
         A = max(1, T * k)
         self.route = RouteBuffers(
@@ -225,12 +230,19 @@ class MoECall:
         s, r = self.stack, self.route
         mass = self.mass[layer] if accumulate_mass else None
         if self.fused:
-            pw.pw_moe_route_apl_ffn(s.desc, layer, x, logits, s.I, s.E, s.k, r.ids, r.w, r.offsets, r.perm,
+            if s.shared:
+                opts = pw.pw_ffn_options()
+                if options is not None:
+                    ctypes.memmove(ctypes.addressof(opts), ctypes.addressof(options), ctypes.sizeof(opts))
+                opts.shared_experts = s.shared
+                options = opts
+            pw.pw_moe_route_apl_ffn(s.desc, layer, x, logits, s.I, s.routed, s.k, r.ids, r.w, r.offsets, r.perm,
                                     r.inv_perm, mass, self.ws, self.y, self.status, options=options, stream=stream)
         else:
-            pw.pw_moe_route_topk(logits, s.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm, mass, stream=stream)
-            pw.pw_moe_apl_ffn(s.desc, layer, x, s.I, s.E, s.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm,
-                              self.ws, self.y, self.status, options=options, stream=stream)
+            pw.pw_moe_route_topk_shared(logits, s.k, s.shared, r.ids, r.w, r.offsets, r.perm, r.inv_perm, mass,
+                                        stream=stream)
+            pw.pw_moe_apl_ffn(s.desc, layer, x, s.I, s.E, s.k + s.shared, r.ids, r.w, r.offsets, r.perm,
+                              r.inv_perm, self.ws, self.y, self.status, options=options, stream=stream)
         return self.y[: self.T]
 
 

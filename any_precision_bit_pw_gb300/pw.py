@@ -42,7 +42,7 @@ EXPORTS = (
     "pw_last_error", "pw_plane_bytes", "pw_pack_bitplanes", "pw_desc_bytes", "pw_page_table_create",
     "pw_page_table_destroy", "pw_page_table_attach_plane", "pw_page_table_attach_lut",
     "pw_page_table_set_desired", "pw_page_table_set_bits", "pw_page_table_get", "pw_page_table_bytes",
-    "pw_page_table_resident_bytes", "pw_page_table_sync", "pw_moe_route_topk",
+    "pw_page_table_resident_bytes", "pw_page_table_sync", "pw_moe_route_topk", "pw_moe_route_topk_shared",
     "pw_page_bytes", "pw_page_offload", "pw_page_reload", "pw_page_table_poll", "pw_page_table_take_released",
     "pw_page_state",
     "pw_moe_apl_ffn_workspace", "pw_moe_apl_ffn", "pw_moe_apl_ffn_ex", "pw_moe_apl_ffn_noalloc",
@@ -65,7 +65,7 @@ class pw_block_info(ctypes.Structure):
 
 class pw_ffn_options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32),
-                ("reserved", ctypes.c_int32 * 5)]
+                ("shared_experts", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
 
 
 _lib: Optional[ctypes.CDLL] = None
@@ -100,6 +100,7 @@ def lib() -> ctypes.CDLL:
             "pw_page_table_take_released": (I32, [P, I32, ctypes.POINTER(U64)]),
             "pw_page_state": (I32, [P, I32, I32, ctypes.POINTER(I32), ctypes.POINTER(P), ctypes.POINTER(P)]),
             "pw_moe_route_topk": (I32, [P, I32, I32, I32, P, P, P, P, P, P, P]),
+            "pw_moe_route_topk_shared": (I32, [P, I32, I32, I32, I32, P, P, P, P, P, P, P]),
             "pw_moe_apl_ffn_workspace": (SZ, [I32, I32, I32, I32, I32]),
             "pw_moe_apl_ffn": (I32, [P, I32, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P, P, P]),
             "pw_moe_apl_ffn_ex": (I32, [P, I32, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, SZ, P, P,
@@ -259,6 +260,16 @@ def pw_moe_route_topk(logits: torch.Tensor, k: int, ids: torch.Tensor, w: torch.
     T, E = logits.shape
     _check(lib().pw_moe_route_topk(_ptr(logits), T, E, k, _ptr(ids), _ptr(w), _ptr(offsets), _ptr(perm),
                                    _ptr(inv_perm), _ptr(mass_accum), _stream(stream)))
+
+
+def pw_moe_route_topk_shared(logits: torch.Tensor, k: int, shared: int, ids: torch.Tensor, w: torch.Tensor,
+                             offsets: torch.Tensor, perm: torch.Tensor, inv_perm: torch.Tensor,
+                             mass_accum: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Top-k routing plus `shared` always-on experts (ids E..E+S-1, weight 1)."""
+    _dev(logits, torch.float32, "logits")
+    T, E = logits.shape
+    _check(lib().pw_moe_route_topk_shared(_ptr(logits), T, E, k, shared, _ptr(ids), _ptr(w), _ptr(offsets),
+                                          _ptr(perm), _ptr(inv_perm), _ptr(mass_accum), _stream(stream)))
 
 
 def pw_moe_apl_ffn_workspace(T: int, H: int, I: int, E: int, k: int) -> int:

@@ -37,8 +37,13 @@ DOWN = 1
 class MoEShape:
     hidden: int          # H
     intermediate: int    # I
-    experts: int         # E
+    experts: int         # E routed experts
     top_k: int           # k
+    shared: int = 0      # S shared experts (every token, weight 1): expert ids E .. E+S-1
+
+    @property
+    def total_experts(self) -> int:
+        return self.experts + self.shared
 
     def block_shape(self, u: int) -> Tuple[int, int]:
         """(rows, cols) of a linear-block: gate_up is 2I x H, down is H x I."""
@@ -50,6 +55,11 @@ class MoEShape:
 TINY = MoEShape(hidden=256, intermediate=512, experts=4, top_k=2)
 MIXTRAL_8X7B = MoEShape(hidden=4096, intermediate=14336, experts=8, top_k=2)
 MIXTRAL_8X22B = MoEShape(hidden=6144, intermediate=16384, experts=8, top_k=2)
+# The pages' Table 1 gives these two models' expert counts and top-k only; the
+# hidden and expert sizes below are this build's choice (Qwen1.5-MoE-like
+# 2048 x 1408, and a many-small-experts 2048 x 768).
+QWEN15_MOE = MoEShape(hidden=2048, intermediate=1408, experts=60, top_k=4, shared=4)
+GEMMA4_LIKE = MoEShape(hidden=2048, intermediate=768, experts=128, top_k=8, shared=1)
 
 
 @dataclass(frozen=True)
@@ -113,8 +123,13 @@ MIXTRAL_8X7B_STACK = Workload("mixtral8x7b_stack32_decode", MIXTRAL_8X7B, tokens
 STACK_STEPS = 64
 STACK_COMMIT_EVERY = 8
 
+QWEN15_DECODE = Workload("qwen15moe_decode_mixed", QWEN15_MOE, tokens=32, parent_bits=8, seed_bits=3, seed=5,
+                         bits_mode="uniform_choice", bits_choices=(3, 4, 5, 6, 7, 8))
+GEMMA4_DECODE = Workload("gemma4like_decode_mixed", GEMMA4_LIKE, tokens=32, parent_bits=8, seed_bits=3, seed=6,
+                         bits_mode="uniform_choice", bits_choices=(3, 4, 5, 6, 7, 8))
+
 WORKLOADS = {w.name: w for w in (TINY_LAYER, MIXTRAL_8X7B_DECODE, MIXTRAL_8X7B_SWEEP,
-                                 MIXTRAL_8X22B_PREFILL, MIXTRAL_8X7B_STACK)}
+                                 MIXTRAL_8X22B_PREFILL, MIXTRAL_8X7B_STACK, QWEN15_DECODE, GEMMA4_DECODE)}
 
 
 # ----------------------------------------------------------------------------
@@ -161,8 +176,9 @@ def zipf_ranks(wl: Workload, layer: int = 0) -> torch.Tensor:
 
 
 def committed_bits(wl: Workload, layer: int = 0) -> List[int]:
-    """q_i for the 2E blocks of one layer, ordered (expert, u) with u=0 gate_up."""
-    E = wl.shape.experts
+    """q_i for the 2(E+S) blocks of one layer (routed then shared experts),
+    ordered (expert, u) with u=0 gate_up."""
+    E = wl.shape.total_experts
     if wl.bits_mode == "fixed":
         return [wl.fixed_bits] * (2 * E)
     g = _gen(wl.seed, "cpu", "bits", layer)
@@ -237,7 +253,7 @@ def layer_inputs(wl: Workload, layer: int = 0, step: int = 0, device="cpu",
                  lut_bits: Optional[Sequence[int]] = None) -> LayerInputs:
     """Draw one layer.  ``experts`` limits which experts' weights are drawn;
     ``lut_bits`` limits which LUT bitwidths are drawn (default: all of S..P)."""
-    E = wl.shape.experts
+    E = wl.shape.total_experts
     ex = range(E) if experts is None else experts
     lb = wl.supported_bits if lut_bits is None else tuple(lut_bits)
     idx, luts = {}, {}

@@ -125,16 +125,20 @@ def layer_call(pw, stack, call, layer, x, logits, mass, ev, stream, routed: bool
     """One layer call of a timed step; `ev` (start, stop) brackets the fused
     kernel's launch."""
     r, sh = call.route, stack
+    opts = None
+    if sh.shared:
+        opts = pw.pw_ffn_options()
+        opts.shared_experts = sh.shared
     if routed:
         ev[0].record(stream)
-        pw.pw_moe_route_apl_ffn(stack.desc, layer, x, logits, sh.I, sh.E, sh.k, r.ids, r.w, r.offsets, r.perm,
-                                r.inv_perm, mass, call.ws, call.y, call.status)
+        pw.pw_moe_route_apl_ffn(stack.desc, layer, x, logits, sh.I, sh.routed, sh.k, r.ids, r.w, r.offsets, r.perm,
+                                r.inv_perm, mass, call.ws, call.y, call.status, options=opts)
         ev[1].record(stream)
     else:
-        pw.pw_moe_route_topk(logits, sh.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm, mass)
+        pw.pw_moe_route_topk_shared(logits, sh.k, sh.shared, r.ids, r.w, r.offsets, r.perm, r.inv_perm, mass)
         ev[0].record(stream)
-        pw.pw_moe_apl_ffn(stack.desc, layer, x, sh.I, sh.E, sh.k, r.ids, r.w, r.offsets, r.perm, r.inv_perm,
-                          call.ws, call.y, call.status)
+        pw.pw_moe_apl_ffn(stack.desc, layer, x, sh.I, sh.E, sh.k + sh.shared, r.ids, r.w, r.offsets, r.perm,
+                          r.inv_perm, call.ws, call.y, call.status)
         ev[1].record(stream)
 
 
@@ -228,7 +232,7 @@ def algorithmic_bytes(wl, bits, offsets):
     """Bytes one fused-layer launch must move: the committed planes and LUT_q
     of every block of every active expert, x, y and the h write + read."""
     sh = wl.shape
-    H, I, E, k = sh.hidden, sh.intermediate, sh.experts, sh.top_k
+    H, I, E, k = sh.hidden, sh.intermediate, sh.total_experts, sh.top_k + sh.shared   # all experts, slots
     T = int(offsets[-1]) // k
     planes = luts = 0
     for e in range(E):
@@ -251,7 +255,8 @@ def gpu_arm(args, rank, world, local_rank):
     wl = get_workload(args.workload, args.tokens)
     sh = wl.shape
     li = synth.layer_inputs(wl, device=dev)
-    stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, wl.parent_bits, wl.seed_bits, dev)
+    stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, wl.parent_bits, wl.seed_bits, dev,
+                        shared=sh.shared)
     load_layer(stack, 0, li)
     stack.sync()
     del li.idx
@@ -260,7 +265,7 @@ def gpu_arm(args, rank, world, local_rank):
     lgs = [synth.router_logits(wl, 0, s, dev) for s in range(n_batches)]
     call = MoECall(stack, wl.tokens)
     stream = torch.cuda.current_stream()
-    kname = ffn_kernel(wl.tokens, sh.top_k, sh.experts)
+    kname = ffn_kernel(wl.tokens, sh.top_k + sh.shared, sh.total_experts)
     routed = kname != "apl_prefill_kernel"
 
     # routing of each batch (for the algorithmic byte count)
@@ -355,7 +360,8 @@ def gpu_arm(args, rank, world, local_rank):
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic (seeded; bit-plane indices uniform, LUTs sorted N(0,0.02), x N(0,1))",
         "config": {"workload": wl.name, "hidden": H, "intermediate": sh.intermediate, "experts": E,
-                   "top_k": sh.top_k, "tokens": T, "parent_bits": wl.parent_bits, "seed_bits": wl.seed_bits,
+                   "shared_experts": sh.shared, "top_k": sh.top_k, "tokens": T, "parent_bits": wl.parent_bits,
+                   "seed_bits": wl.seed_bits,
                    "committed_bits": li.bits, "parallelism": f"replicas x{world}",
                    "l2": "no flush: the planes read per step (%.0f MB) exceed the 129 MB L2" % (mean_planes / 1e6)},
         "roofline": roofline,
@@ -555,8 +561,8 @@ def oracle_sample(workload: str, experts_in_sample: int = 1, tokens=None) -> dic
     sh = wl.shape
     x = synth.activations(wl).numpy()
     logits = synth.router_logits(wl).numpy()
-    r = apl.route_topk(logits, sh.top_k)
-    active = [e for e in range(sh.experts) if r["offsets"][e + 1] > r["offsets"][e]]
+    r = apl.route_topk_shared(logits, sh.top_k, sh.shared)
+    active = [e for e in range(sh.total_experts) if r["offsets"][e + 1] > r["offsets"][e]]
     sample = active[:experts_in_sample]
     li = synth.layer_inputs(wl, experts=sample)
     blocks = {}

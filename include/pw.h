@@ -219,11 +219,26 @@ int pw_page_state(const pw_page_table* t, int block, int page, int* state, const
  *  d_inv_perm int32 [T*k]   inverse of perm
  *  d_mass_accum fp32 [E] or NULL: adds sum_t sum_j w[t][j]*[ids[t][j] == e]
  *                           (the numerator of Eq. 1; the denominator is T)
- * Limits: 1 <= k <= E <= 256, k <= 8, 0 <= T <= 2^20.  T = 0 writes the
+ * Limits: 1 <= k <= E <= 256, k <= 16, 0 <= T <= 2^20.  T = 0 writes the
  * offsets (all zero) and nothing else. */
 int pw_moe_route_topk(const float* d_logits, int T, int E, int k, int32_t* d_ids, float* d_w,
                       int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm,
                       float* d_mass_accum, void* stream);
+
+/* Routing with S shared experts (Table 1: Qwen1.5-MoE-A2.7B has 60 routed
+ * plus 4 shared experts, Gemma-4-26B-A4B 128 plus 1): experts every token
+ * passes through, added to the routed output.  The pages give no gate for
+ * them; here each has weight 1.  Every token gets K = k + S slots: its top-k
+ * routed experts (as pw_moe_route_topk over the E routed logits) followed by
+ * the shared experts E .. E+S-1 with w = 1.  Outputs are over E + S experts
+ * and K slots: ids and w [T][K], offsets [E+S+1], perm and inv_perm [T*K],
+ * mass [E+S] (shared experts receive T per call); the permutation stays
+ * stable by (expert, token, slot).  pw_moe_apl_ffn then runs with E + S
+ * experts and K for k.  Limits: 1 <= k <= E, S >= 0, E + S <= 256,
+ * k + S <= 16. */
+int pw_moe_route_topk_shared(const float* d_logits, int T, int E, int k, int S, int32_t* d_ids,
+                             float* d_w, int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm,
+                             float* d_mass_accum, void* stream);
 
 /* ------------------------------------------------------------------------ */
 /* Fused mixed-precision MoE expert layer (§3.3, "Fused Mixed-Precision MoE Kernel") */
@@ -297,7 +312,8 @@ typedef struct pw_ffn_options {
   int32_t path;              /* PW_PATH_* */
   uint32_t flags;            /* PW_FFN_FLAG_* */
   uint32_t wait_timeout_us;  /* bound of each in-kernel wait; 0 = 2 s */
-  int32_t reserved[5];
+  int32_t shared_experts;    /* routed call only: S shared experts (see pw_moe_route_topk_shared) */
+  int32_t reserved[4];
 } pw_ffn_options;
 
 int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
@@ -320,8 +336,12 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
  * timeout sets d_status to PW_ERR_TIMEOUT).  On the prefill path, where one
  * CTA would route too slowly, a routing launch runs first on the same stream.
  * T = 0 writes the offsets (all zero) and nothing else (d_logits may then be
- * NULL).  Every other argument,
- * limit and error is that of pw_moe_apl_ffn. */
+ * NULL).  E and k count the routed experts (the logits' width and top-k);
+ * with options->shared_experts = S (the _ex form) routing is that of
+ * pw_moe_route_topk_shared and the layer runs over E + S experts (descriptor
+ * entries of the layer: E + S experts) and k + S slots, so the routing arrays
+ * are sized for them.  Every other argument, limit and error is that of
+ * pw_moe_apl_ffn. */
 int pw_moe_route_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, const float* d_logits,
                          int T, int H, int I, int E, int k, int32_t* d_ids, float* d_w,
                          int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm,

@@ -200,6 +200,39 @@ def route_topk(logits: np.ndarray, k: int) -> Dict[str, np.ndarray]:
                 probs=p)
 
 
+def route_topk_shared(logits: np.ndarray, k: int, S: int) -> Dict[str, np.ndarray]:
+    """Top-k routing plus S shared experts.
+
+    The pages' Table 1 lists models with shared experts (60 routed + 4 shared,
+    top-4; 128 routed + 1 shared, top-8) and gives them no gate; the reading
+    here: every token also passes through the shared experts E .. E+S-1 with
+    weight 1, added to its routed output.  Each token has K = k + S slots
+    (its routed picks, as route_topk, then the shared experts); slots
+    s = t*K + j are ordered by (expert, token, j) over E + S experts; mass is
+    Eq. 1 over all E + S experts.
+    """
+    lg = np.asarray(logits, dtype=np.float32)
+    T, E = lg.shape
+    if S < 0:
+        raise ValueError("need S >= 0")
+    r = route_topk(lg, k)
+    K = k + S
+    ids = np.concatenate([r["ids"], np.tile(E + np.arange(S, dtype=np.int32), (T, 1))], axis=1).astype(np.int32)
+    w = np.concatenate([r["w"], np.ones((T, S), dtype=np.float64)], axis=1)
+    expert_of_slot = ids.reshape(-1).astype(np.int64)              # slot order is (token, j)
+    perm = np.argsort(expert_of_slot, kind="stable").astype(np.int32)
+    inv_perm = np.empty(T * K, dtype=np.int32)
+    inv_perm[perm] = np.arange(T * K, dtype=np.int32)
+    counts = np.bincount(expert_of_slot, minlength=E + S)
+    offsets = np.concatenate([[0], np.cumsum(counts)]).astype(np.int32)
+    mass = np.zeros(E + S, dtype=np.float64)
+    np.add.at(mass, expert_of_slot, w.reshape(-1))
+    total = w.sum()
+    if total > 0:
+        mass /= total
+    return dict(ids=ids, w=w, offsets=offsets, perm=perm, inv_perm=inv_perm, mass=mass)
+
+
 # ----------------------------------------------------------------------------
 # The MoE layer (§3.3: routing, expert activation, down projection, output accumulation)
 # ----------------------------------------------------------------------------

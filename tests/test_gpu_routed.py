@@ -31,7 +31,8 @@ def _gpu():
 
 def _stack(li):
     sh = li.wl.shape
-    st = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, li.wl.parent_bits, li.wl.seed_bits, DEV)
+    st = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, li.wl.parent_bits, li.wl.seed_bits, DEV,
+                     shared=sh.shared)
     load_layer(st, 0, li)
     st.sync()
     return st
@@ -109,3 +110,57 @@ def test_routed_call_zero_tokens():
                             call.y, call.status)
     torch.cuda.synchronize()
     assert call.route.offsets.cpu().tolist() == [0] * (sh.experts + 1)
+
+
+# ---------------------------------------------------------------------------
+# shared experts (Table 1: 60 routed + 4 shared top-4; 128 routed + 1 shared top-8)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("T,E,k,S", [(32, 60, 4, 4), (32, 128, 8, 1), (300, 60, 4, 4), (5, 8, 2, 3)])
+def test_route_shared_matches_oracle(T, E, k, S):
+    g = torch.Generator().manual_seed(T + E + k + S)
+    logits = torch.randn((T, E), generator=g)
+    K = k + S
+    ids = torch.empty((T, K), dtype=torch.int32, device=DEV)
+    w = torch.empty((T, K), dtype=torch.float32, device=DEV)
+    off = torch.empty((E + S + 1,), dtype=torch.int32, device=DEV)
+    perm = torch.empty((T * K,), dtype=torch.int32, device=DEV)
+    inv = torch.empty((T * K,), dtype=torch.int32, device=DEV)
+    mass = torch.zeros((E + S,), dtype=torch.float32, device=DEV)
+    pw.pw_moe_route_topk_shared(logits.to(DEV).contiguous(), k, S, ids, w, off, perm, inv, mass)
+    torch.cuda.synchronize()
+    ref = apl.route_topk_shared(logits.numpy(), k, S)
+    assert np.array_equal(ids.cpu().numpy(), ref["ids"])
+    assert np.array_equal(off.cpu().numpy(), ref["offsets"])
+    assert np.array_equal(perm.cpu().numpy(), ref["perm"])
+    assert np.array_equal(inv.cpu().numpy(), ref["inv_perm"])
+    np.testing.assert_allclose(w.cpu().numpy(), ref["w"], atol=1e-6, rtol=0)
+    np.testing.assert_allclose(mass.cpu().numpy() / (T * (1 + S)), ref["mass"], atol=1e-5, rtol=0)
+
+
+@pytest.mark.parametrize("name", ["qwen15moe_decode_mixed", "gemma4like_decode_mixed"])
+def test_shared_expert_layers(name):
+    """The Qwen- and Gemma-shaped decode layers: routed call == two-launch call
+    bit for bit, and sampled tokens against the oracle."""
+    wl = synth.WORKLOADS[name]
+    li = synth.layer_inputs(wl, device=DEV)
+    st = _stack(li)
+    sh = wl.shape
+    fused, split = MoECall(st, wl.tokens, fused=True), MoECall(st, wl.tokens, fused=False)
+    yf = fused(0, li.x, li.logits).clone()
+    ys = split(0, li.x, li.logits).clone()
+    torch.cuda.synchronize()
+    assert int(fused.status.item()) == 0 and int(split.status.item()) == 0
+    for a, b in zip(_routing(fused), _routing(split)):
+        assert np.array_equal(a, b)
+    assert torch.equal(yf, ys)
+    r = apl.route_topk_shared(li.logits.cpu().numpy(), sh.top_k, sh.shared)
+    assert np.array_equal(_routing(fused)[0], r["ids"])
+    toks = [1, 22]
+
+    def blocks(e, u):
+        idx = li.idx[(e, u)].cpu().numpy()
+        return apl.IndexBlock(idx, {b: t.cpu().numpy() for b, t in li.luts[(e, u)].items()}, li.bits[2 * e + u],
+                              wl.parent_bits)
+    y_ref = apl.moe_layer(li.x.cpu().numpy(), r["ids"], r["w"], sh.intermediate, blocks, tokens=toks)
+    m = apl.compare(y_ref[toks], yf.float().cpu().numpy()[toks])
+    assert m["rel_l2"] <= 2e-3 and m["max_abs_over_rms"] <= 1e-2, m
