@@ -24,6 +24,12 @@ semantics but not the memory layout; this is the library's documented
     tile  = j // 128;    jj = j % 128;   word = jj // 32;  t = jj % 32
     bit   = 4*(t % 8) + t // 8                (bit of a little-endian uint32)
     byte offset of that uint32 = (strip * (K/128) + tile) * 2048 + 16*pos + 4*word
+
+  The LUT of bitwidth b (fp16 [N][2^b], one row of centroids per output row,
+  Figure 3 caption) is stored "tiled" too: with strip, w and i of row n as
+  above, entry c of row n sits at byte
+    (strip * 2^b + c) * 256 + 4*((w % 2)*32 + i) + 2*(w // 2)
+  so the table of a 128-row strip is one contiguous run of 2^b * 256 bytes.
 """
 from __future__ import annotations
 
@@ -75,6 +81,36 @@ def bit_address(n, j, N: int, K: int):
     word_byte = (strip * (K // TILE_COLS) + tile) * TILE_BYTES + 16 * pos + 4 * word
     # little-endian uint32: bit b of the word is bit b % 8 of byte b // 8
     return 8 * word_byte + bit
+
+
+def lut_tiled_offset(n, c, N: int, b: int):
+    """Byte offset of LUT entry c of row n in the tiled LUT layout (module
+    docstring); n and c broadcast like numpy arrays."""
+    n = np.asarray(n, dtype=np.int64)
+    c = np.asarray(c, dtype=np.int64)
+    half_rows = N // 2
+    half = n // half_rows
+    r = n % half_rows
+    strip = r // 64
+    rr = r % 64
+    w = rr // 16
+    i = rr % 16 + 16 * half
+    return (strip * (1 << b) + c) * 256 + 4 * ((w % 2) * 32 + i) + 2 * (w // 2)
+
+
+def pack_lut_tiled(lut: np.ndarray) -> np.ndarray:
+    """fp16 [N][2^b] row-major LUT -> uint8 bytes in the tiled LUT layout."""
+    lut = np.asarray(lut, dtype=np.float16)
+    N, C = lut.shape
+    b = C.bit_length() - 1
+    if C != 1 << b or N % TILE_ROWS:
+        raise ValueError("LUT must be [N][2^b] with N % 128 == 0")
+    out = np.zeros(N * C * 2, dtype=np.uint8)
+    off = lut_tiled_offset(np.arange(N)[:, None], np.arange(C)[None, :], N, b).ravel()
+    raw = lut.view(np.uint8).reshape(N * C, 2)
+    out[off] = raw[:, 0]
+    out[off + 1] = raw[:, 1]
+    return out
 
 
 def pack_bitplanes(idx: np.ndarray, parent_bits: int) -> List[np.ndarray]:

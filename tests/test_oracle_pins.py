@@ -318,3 +318,44 @@ def test_index_block_equals_plane_block():
         a = apl.Block(planes, luts, q, N, K).linear(x)
         b = apl.IndexBlock(idx, luts, q, P).linear(x)
         assert np.array_equal(a, b)
+
+
+# ---------------------------------------------------------------------------
+# Tiled LUT layout (the library's documented storage of LUT pages)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("N,b,n,c,byte", [
+    (256, 3, 0, 0, 0),            # strip 0, w 0, i 0, line 0
+    (256, 3, 1, 0, 4),            # i 1 -> next word
+    (256, 3, 16, 0, 128),         # w 1 -> words 32.. (odd w)
+    (256, 3, 32, 0, 2),           # w 2 -> high half-word of word 0
+    (256, 3, 48, 5, 5 * 256 + 128 + 2),   # w 3, line 5
+    (256, 3, 128, 0, 64),         # second half of the rows: i = 16
+    (256, 3, 64, 0, 8 * 256),     # strip 1 starts after 2^b lines
+    (256, 4, 64 + 17, 9, (16 + 9) * 256 + 4 * (32 + 1)),
+])
+def test_lut_layout_hand_derived_points(N, b, n, c, byte):
+    assert int(apl.lut_tiled_offset(n, c, N, b)) == byte
+
+
+@pytest.mark.parametrize("N,b", [(128, 2), (256, 3), (384, 8), (1024, 5)])
+def test_lut_layout_is_a_bijection_onto_even_bytes(N, b):
+    off = apl.lut_tiled_offset(np.arange(N)[:, None], np.arange(1 << b)[None, :], N, b).ravel()
+    assert np.array_equal(np.sort(off), np.arange(0, N * (2 << b), 2))
+    # a strip's table is one contiguous run of 2^b * 256 bytes
+    strips = (np.arange(N) % (N // 2)) // 64
+    for s in range(N // 128):
+        rows = np.nonzero(strips == s)[0]
+        o = apl.lut_tiled_offset(rows[:, None], np.arange(1 << b)[None, :], N, b)
+        assert o.min() == s * (256 << b) and o.max() == (s + 1) * (256 << b) - 2
+
+
+def test_pack_lut_tiled_places_every_entry():
+    rng = np.random.default_rng(5)
+    N, b = 256, 4
+    lut = rng.standard_normal((N, 1 << b)).astype(np.float16)
+    buf = apl.pack_lut_tiled(lut)
+    assert buf.size == N * (2 << b)
+    for n in (0, 1, 63, 64, 127, 128, 200, 255):
+        for c in (0, 7, 15):
+            o = int(apl.lut_tiled_offset(n, c, N, b))
+            assert buf[o:o + 2].view(np.float16)[0] == lut[n, c]
