@@ -9,12 +9,17 @@
 //  * plane words use the "nibble" bit order of the tiled layout: within a
 //    32-column word, column 8*js + e sits at bit 4*e + js, so one shift and
 //    mask per plane yields the indices of 8 consecutive columns as nibbles;
-//  * q <= 4: the LUT lives in registers as a low-byte and a high-byte table
-//    and one prmt looks up four 8-bit halves at once (q = 4 selects between
-//    two 8-entry halves with a byte mask built from the index MSB);
-//  * q >= 5: an 8x8 bit transpose of the plane words yields byte indices;
-//    the LUT lives in a 64 KB-aligned shared region with one bank per lane,
-//    so one prmt forms each lookup address and lookups never conflict.
+//  * every unit's LUT arrives in a 64 KB-aligned shared region by one bulk
+//    copy of its strip's table (LUT pages are stored in that order, see
+//    pw_pack_lut): entry c of a row is on the 256-byte line c, at the row's
+//    own bank;
+//  * q <= 3 (4 for the register form): the thread reads its row's entries
+//    into registers as a low-byte and a high-byte table, and one prmt looks
+//    up four 8-bit halves at once (q = 4 selects between two 8-entry halves
+//    with a byte mask built from the index MSB);
+//  * q >= 4 in the kernels: an 8x8 bit transpose of the plane words yields
+//    byte indices, one prmt forms each lookup address in the region, and
+//    lookups never conflict.
 #pragma once
 
 #include "tc_ptx.cuh"
@@ -64,53 +69,28 @@ struct RowDequant<Q, true> {
   static constexpr int kT = (Q == 4) ? 4 : 2;
   uint32_t lo[kT], hi[kT];
 
-  __device__ __forceinline__ void load(const uint16_t* __restrict__ lut_row, uint32_t, int) {
+  // The same tables from this row's LUT in the shared LUT region (the tiled
+  // LUT order: entry c at `base + c*256`, base = the region half plus this
+  // row's byte within a line).
+  __device__ __forceinline__ void load_region(uint32_t base) {
+    constexpr int kE = 1 << Q;
+    uint32_t v[kE / 2];
+#pragma unroll
+    for (int j = 0; j < kE / 2; ++j)
+      v[j] = lds_u16_ordered(base + (2 * j) * 256u) | (lds_u16_ordered(base + (2 * j + 1) * 256u) << 16);
     if (Q == 2) {
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(lut_row));
-      lo[0] = lo[1] = prmt(v.x, v.y, 0x6420u);
-      hi[0] = hi[1] = prmt(v.x, v.y, 0x7531u);
-    } else if (Q == 3) {
-      const uint4 v = __ldg(reinterpret_cast<const uint4*>(lut_row));
-      lo[0] = prmt(v.x, v.y, 0x6420u);
-      lo[1] = prmt(v.z, v.w, 0x6420u);
-      hi[0] = prmt(v.x, v.y, 0x7531u);
-      hi[1] = prmt(v.z, v.w, 0x7531u);
+      lo[0] = lo[1] = prmt(v[0], v[1], 0x6420u);
+      hi[0] = hi[1] = prmt(v[0], v[1], 0x7531u);
     } else {
-      const uint4 v0 = __ldg(reinterpret_cast<const uint4*>(lut_row));
-      const uint4 v1 = __ldg(reinterpret_cast<const uint4*>(lut_row) + 1);
-      lo[0] = prmt(v0.x, v0.y, 0x6420u);
-      lo[1] = prmt(v0.z, v0.w, 0x6420u);
-      hi[0] = prmt(v0.x, v0.y, 0x7531u);
-      hi[1] = prmt(v0.z, v0.w, 0x7531u);
-      if (kT == 4) {
-        lo[kT - 2] = prmt(v1.x, v1.y, 0x6420u);
-        lo[kT - 1] = prmt(v1.z, v1.w, 0x6420u);
-        hi[kT - 2] = prmt(v1.x, v1.y, 0x7531u);
-        hi[kT - 1] = prmt(v1.z, v1.w, 0x7531u);
-      }
-    }
-  }
-
-  // The same tables from this row's LUT in shared memory (2^Q fp16 at `saddr`).
-  __device__ __forceinline__ void load_shared(uint32_t saddr) {
-    if (Q == 2) {
-      uint32_t a, b;
-      lds_v2(saddr, a, b);
-      lo[0] = lo[1] = prmt(a, b, 0x6420u);
-      hi[0] = hi[1] = prmt(a, b, 0x7531u);
-    } else {
-      uint32_t v[4];
-      lds_v4u(saddr, v);
       lo[0] = prmt(v[0], v[1], 0x6420u);
       lo[1] = prmt(v[2], v[3], 0x6420u);
       hi[0] = prmt(v[0], v[1], 0x7531u);
       hi[1] = prmt(v[2], v[3], 0x7531u);
       if (kT == 4) {
-        lds_v4u(saddr + 16, v);
-        lo[kT - 2] = prmt(v[0], v[1], 0x6420u);
-        lo[kT - 1] = prmt(v[2], v[3], 0x6420u);
-        hi[kT - 2] = prmt(v[0], v[1], 0x7531u);
-        hi[kT - 1] = prmt(v[2], v[3], 0x7531u);
+        lo[kT - 2] = prmt(v[4 % (kE / 2)], v[5 % (kE / 2)], 0x6420u);
+        lo[kT - 1] = prmt(v[6 % (kE / 2)], v[7 % (kE / 2)], 0x6420u);
+        hi[kT - 2] = prmt(v[4 % (kE / 2)], v[5 % (kE / 2)], 0x7531u);
+        hi[kT - 1] = prmt(v[6 % (kE / 2)], v[7 % (kE / 2)], 0x7531u);
       }
     }
   }
@@ -197,54 +177,6 @@ struct RowDequant<Q, false> {
     hi7 = (Q < 8 && half) ? 0xFFFFFFFFu : 0u;
   }
 
-  // Write part `part` of `nparts` of this row's LUT (2^Q fp16) into its
-  // column of the region; all loads of the part are issued before any store.
-  template <int kParts = 1>
-  __device__ __forceinline__ void load(const uint16_t* __restrict__ lut_row, int part = 0) const {
-    constexpr int kVec = (1 << Q) / 8 / kParts;    // uint4 (8 entries) per part
-    const uint4* src = reinterpret_cast<const uint4*>(lut_row) + part * kVec;
-    uint4 a[kVec];
-#pragma unroll
-    for (int c8 = 0; c8 < kVec; ++c8) a[c8] = __ldg(src + c8);
-#pragma unroll
-    for (int c8 = 0; c8 < kVec; ++c8) {
-      const uint32_t av[4] = {a[c8].x, a[c8].y, a[c8].z, a[c8].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t c = static_cast<uint32_t>((part * kVec + c8) * 8 + 2 * i);
-        sts_u16(tblw + c * 256u, av[i] & 0xFFFFu);
-        sts_u16(tblw + (c + 1u) * 256u, av[i] >> 16);
-      }
-    }
-  }
-
-  // Copy this row's LUT from a row-major copy in shared memory (2^Q fp16 at
-  // `srow`) into its column of the region.  kSets threads share the row; the
-  // thread of set `set` writes 8-entry chunks set, set + kSets, ...  rotated by
-  // the lane so that the lanes of a warp read different bank groups.
-  template <int kSets>
-  __device__ __forceinline__ void fill(uint32_t srow, int set, int lane) const {
-    constexpr int kCh = (1 << Q) / 8;
-    static_assert(kCh % kSets == 0, "chunks per set");
-    constexpr int kPer = kCh / kSets;
-    uint32_t v[kPer][4];
-    int ch[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      ch[j] = (set + kSets * j + lane) & (kCh - 1);
-      lds_v4u(srow + ch[j] * 16, v[j]);
-    }
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t c = static_cast<uint32_t>(ch[j] * 8 + 2 * i);
-        sts_u16(tblw + c * 256u, v[j][i] & 0xFFFFu);
-        sts_u16(tblw + (c + 1u) * 256u, v[j][i] >> 16);
-      }
-    }
-  }
-
   // ww[p]: one 32-column word of plane p -> 16 fp16 pairs (columns in order).
   __device__ __forceinline__ void word(const uint32_t (&ww)[Q], uint32_t (&out)[16]) const {
     // row i of the bit matrix = index bit i = plane Q-1-i; missing bits are 0
@@ -265,32 +197,5 @@ struct RowDequant<Q, false> {
     }
   }
 };
-
-// Write one row's LUT (2^Q fp16 at `lut_row`, global) into its column of the
-// region: entry c at line c + 128*half (Q < 8) or line c (Q = 8).  `tblw` is
-// the row's set_row() address.  Loads go out in batches of up to 8 x 16 bytes.
-template <int Q>
-__device__ __forceinline__ void region_fill(uint32_t tblw, const uint16_t* __restrict__ lut_row, int half) {
-  constexpr int kCh = (1 << Q) / 8;
-  constexpr int kB = kCh < 8 ? kCh : 8;
-  const uint32_t base = tblw + ((Q < 8 && half) ? 128u * 256u : 0u);
-  const uint4* src = reinterpret_cast<const uint4*>(lut_row);
-#pragma unroll
-  for (int c0 = 0; c0 < kCh; c0 += kB) {
-    uint4 a[kB];
-#pragma unroll
-    for (int j = 0; j < kB; ++j) a[j] = __ldg(src + c0 + j);
-#pragma unroll
-    for (int j = 0; j < kB; ++j) {
-      const uint32_t av[4] = {a[j].x, a[j].y, a[j].z, a[j].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const uint32_t c = static_cast<uint32_t>((c0 + j) * 8 + 2 * i);
-        sts_u16(base + c * 256u, av[i] & 0xFFFFu);
-        sts_u16(base + (c + 1u) * 256u, av[i] >> 16);
-      }
-    }
-  }
-}
 
 }  // namespace pw

@@ -90,9 +90,8 @@ enum : int {
   kBarPFree = kBarPFull + kPS,    // [kPS] plane chunk consumed (16 dequant warps)
   kBarDone = kBarPFree + kPS,     // [2]   unit's accumulators complete (one arrival per issuer)
   kBarDFree = kBarDone + 2,       // [2]   accumulator read (4 epilogue warps)
-  kBarRegReady = kBarDFree + 2,   // [2]   region half written for the unit (4 epilogue warps)
-  kBarQ8Fill = kBarRegReady + 2,  // q = 8 region written by the dequant warps themselves (16 warps)
-  kBarEpiDone = kBarQ8Fill + 1,
+  kBarRegReady = kBarDFree + 2,   // [2]   the unit's LUT landed in its region half (bulk copy bytes)
+  kBarEpiDone = kBarRegReady + 2,
   kBarEpiGo = kBarEpiDone + 1,
   kBarUReady = kBarEpiGo + 1,     // [kUS]
   kBarUFree = kBarUReady + kUS,   // [kUS]
@@ -191,7 +190,7 @@ __host__ __device__ constexpr int chunk_tiles(int q) { return q <= 4 ? 4 : 2; }
 
 template <int Q>
 __device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, const Sm sm, uint32_t tmem, uint32_t x0,
-                                             uint32_t c0, uint32_t ui, uint32_t n8) {
+                                             uint32_t c0, uint32_t ui) {
   constexpr int kCt = chunk_tiles(Q);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int set = warp >> 2, qd = warp & 3;
@@ -201,38 +200,14 @@ __device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, con
   // planes the transpose and shared lookups cost fewer logic ops than the
   // two-level register lookup)
   pw::RowDequant<Q, (Q <= 3)> dq;
-  // the unit's LUT is in region half ui & 1 (written one unit ahead)
+  // the unit's LUT has landed in region half ui & 1 (one bulk copy of the
+  // strip's table, issued one unit ahead; a q = 8 table fills the region)
   ok = wait_bar(sm, kBarRegReady + static_cast<int>(ui & 1u), (ui >> 1) & 1u, p);
   if constexpr (Q <= 3) {
-    if (ok) dq.load_shared(sm.region + (ui & 1u) * 32768u + static_cast<uint32_t>(pos) * 32u);
+    const uint32_t rowoff = static_cast<uint32_t>((qd & 1) * 32 + lane) * 4u + static_cast<uint32_t>(qd >> 1) * 2u;
+    if (ok) dq.load_region(sm.region + (ui & 1u) * 32768u + rowoff);
   } else {
     dq.set_row(sm.region, qd, lane, static_cast<int>(ui & 1u));
-  }
-  if constexpr (Q == 8) {
-    // a q = 8 table takes the whole region, so it cannot be written ahead:
-    // the LUT warps only confirmed that every unit before this one is done;
-    // the 16 dequant warps write it (this thread: 64 entries of its row)
-    if (ok) {
-      const BlockDesc& d = *u.d;
-      const int row = strip_pos_row(u.strip, pos, d.rows / 2);
-      const uint4* src = reinterpret_cast<const uint4*>(d.lut + (static_cast<long long>(row) << 8)) + set * 8;
-      uint4 a[8];
-#pragma unroll
-      for (int j = 0; j < 8; ++j) a[j] = __ldg(src + j);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const uint32_t av[4] = {a[j].x, a[j].y, a[j].z, a[j].w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const uint32_t cc = static_cast<uint32_t>(set * 64 + j * 8 + 2 * i);
-          pw::sts_u16(dq.tblw + cc * 256u, av[i] & 0xFFFFu);
-          pw::sts_u16(dq.tblw + (cc + 1u) * 256u, av[i] >> 16);
-        }
-      }
-    }
-    __syncwarp();
-    if (lane == 0) pw::mbar_arrive(bar(sm, kBarQ8Fill));
-    ok = wait_bar(sm, kBarQ8Fill, n8 & 1u, p) && ok;
   }
   const int nt = u.nst / 2;
   const int nch = (nt + kCt - 1) / kCt;
@@ -280,19 +255,19 @@ __device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, con
 }
 
 __device__ __forceinline__ void dequant_role(const Params& p, const Sm sm, uint32_t tmem) {
-  uint32_t x = 0, c = 0, n8 = 0;
+  uint32_t x = 0, c = 0;
   for (uint32_t i = 0;; ++i) {
     if (!wait_unit(sm, i, p)) break;
     const Unit& u = sm.st->units[i % kUS];
     if (u.kind == kNone) break;
     switch (u.q) {
-      case 2: dequant_unit<2>(p, u, sm, tmem, x, c, i, n8); break;
-      case 3: dequant_unit<3>(p, u, sm, tmem, x, c, i, n8); break;
-      case 4: dequant_unit<4>(p, u, sm, tmem, x, c, i, n8); break;
-      case 5: dequant_unit<5>(p, u, sm, tmem, x, c, i, n8); break;
-      case 6: dequant_unit<6>(p, u, sm, tmem, x, c, i, n8); break;
-      case 7: dequant_unit<7>(p, u, sm, tmem, x, c, i, n8); break;
-      default: dequant_unit<8>(p, u, sm, tmem, x, c, i, n8++); break;
+      case 2: dequant_unit<2>(p, u, sm, tmem, x, c, i); break;
+      case 3: dequant_unit<3>(p, u, sm, tmem, x, c, i); break;
+      case 4: dequant_unit<4>(p, u, sm, tmem, x, c, i); break;
+      case 5: dequant_unit<5>(p, u, sm, tmem, x, c, i); break;
+      case 6: dequant_unit<6>(p, u, sm, tmem, x, c, i); break;
+      case 7: dequant_unit<7>(p, u, sm, tmem, x, c, i); break;
+      default: dequant_unit<8>(p, u, sm, tmem, x, c, i); break;
     }
     const int nt = u.nst / 2, ct = chunk_tiles(u.q);
     x += static_cast<uint32_t>(nt);
@@ -324,11 +299,11 @@ __device__ __forceinline__ void plane_loader_role(const Params& p, const Sm sm) 
     if (un.kind == kNone) break;
     const BlockDesc& d = *un.d;
     const int Q = un.q, ct = chunk_tiles(Q), nt = un.nst / 2;
-    if (lane < 2) {
-      // the unit's LUT rows (two runs of 64 rows) into L2 for the LUT writers
-      const long long rowb = static_cast<long long>(2) << Q;
-      const long long r0 = (lane == 0 ? 0ll : static_cast<long long>(d.rows / 2)) + un.strip * 64;
-      pw::prefetch_l2(reinterpret_cast<const char*>(d.lut) + r0 * rowb, static_cast<uint32_t>(64 * rowb));
+    if (lane == 0) {
+      // the unit's LUT (its strip's table, one contiguous run) into L2 ahead
+      // of the bulk copy into the region
+      const uint32_t bytes = 256u << Q;
+      pw::prefetch_l2(reinterpret_cast<const char*>(d.lut) + static_cast<long long>(un.strip) * bytes, bytes);
     }
     const uint32_t* plane = lane < Q ? st.planes[us][lane] : nullptr;
     for (int t0 = 0; t0 < nt; t0 += ct, ++c) {
@@ -478,13 +453,17 @@ __device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t 
 // ---------------------------------------------------------------------------
 // epilogue warps: LUT region one unit ahead, then the unit's epilogue
 // ---------------------------------------------------------------------------
-// Write unit i's LUT into region half i & 1 (q >= 5; q = 8 takes the whole
-// region) once every earlier user of those lines is finished, then signal the
-// half ready (also for q <= 4, which keeps the barrier phases one per unit).
-// Returns 1 when done, 0 when unit i is the end marker, and -1 without
-// waiting when `block` is false and unit i is not published yet.
-__device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i, bool& prev_q8, bool block) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+// Copy unit i's LUT into region half i & 1 (q = 8: the whole region) once
+// every earlier user of those lines is finished: one bulk copy of the strip's
+// table (LUT pages are stored in the region's order, 2^q lines of 256 bytes
+// per strip), issued by thread 0 of the epilogue warps; the half's barrier
+// completes when the bytes land.  Returns 1 when done, 0 when unit i is the
+// end marker, and -1 without waiting when `block` is false and unit i is not
+// published yet.  `last` (thread 0) records the last copy, drained at exit.
+__device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i, bool& prev_q8, bool block,
+                                        int& last) {
+  const int lane = threadIdx.x & 31;
+  const int etid = threadIdx.x - kEpiWarp0 * 32;
   if (!block) {
     int pub = 0;
     if (lane == 0) pub = pw::mbar_test(bar(sm, kBarUReady + static_cast<int>(i % kUS)), (i / kUS) & 1u);
@@ -493,43 +472,24 @@ __device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i
   if (!wait_unit(sm, i, p)) return 0;
   const Unit& u = sm.st->units[i % kUS];
   if (u.kind == kNone) return 0;
-  const int qd = warp & 3, pos = qd * 32 + lane;
-  const int h = static_cast<int>(i & 1u);
-  // units up to i - 2 (the half's previous user), or up to i - 1 when unit
-  // i or i - 1 takes the whole region, are finished by every dequant warp
-  const uint32_t need = static_cast<uint32_t>(kDeqWarpsAll) * ((u.q == 8 || prev_q8) ? i : (i >= 1 ? i - 1 : 0u));
-  const bool ok = wait_count(sm, &sm.st->deq_done, need, p);
-  if (ok && u.q <= 3) {
-    // q <= 3: the row's table (at most 16 bytes), row-major at the start of
-    // the half; the dequant threads load it into registers
-    const BlockDesc& d = *u.d;
-    const int row = strip_pos_row(u.strip, pos, d.rows / 2);
-    const uint4* src = reinterpret_cast<const uint4*>(d.lut + (static_cast<long long>(row) << u.q));
-    const uint32_t dst = sm.region + static_cast<uint32_t>(h) * 32768u + static_cast<uint32_t>(pos) * 32u;
-    if (u.q == 2) {
-      const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
-      asm volatile("st.shared.v2.u32 [%0], {%1, %2};" ::"r"(dst), "r"(v.x), "r"(v.y) : "memory");
+  if (etid == 0) {
+    const int h = static_cast<int>(i & 1u);
+    const uint32_t b = bar(sm, kBarRegReady + h);
+    // units up to i - 2 (the half's previous user), or up to i - 1 when unit
+    // i or i - 1 takes the whole region, are finished by every dequant warp
+    const uint32_t need = static_cast<uint32_t>(kDeqWarpsAll) * ((u.q == 8 || prev_q8) ? i : (i >= 1 ? i - 1 : 0u));
+    if (wait_count(sm, &sm.st->deq_done, need, p)) {
+      const uint32_t bytes = 256u << u.q;
+      const char* src = reinterpret_cast<const char*>(u.d->lut) + static_cast<long long>(u.strip) * bytes;
+      pw::fence_proxy_async_smem();   // the lines' earlier generic accesses before the async write
+      pw::mbar_arrive_expect_tx(b, bytes);
+      pw::bulk_g2s(sm.region + (u.q == 8 ? 0u : static_cast<uint32_t>(h) * 32768u), src, bytes, b);
+      last = static_cast<int>(i);
     } else {
-      const uint4 v = __ldg(src);
-      asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                   : "memory");
+      pw::mbar_arrive(b);   // giving up: complete the phase so that no waiter hangs on it
     }
-  } else if (ok && u.q < 8) {
-    const BlockDesc& d = *u.d;
-    const int row = strip_pos_row(u.strip, pos, d.rows / 2);
-    const uint16_t* lut = d.lut + (static_cast<long long>(row) << u.q);
-    const uint32_t tblw =
-        sm.region | (static_cast<uint32_t>((qd & 1) * 32 + lane) * 4u + static_cast<uint32_t>(qd >> 1) * 2u);
-    switch (u.q) {
-      case 4: pw::region_fill<4>(tblw, lut, h); break;
-      case 5: pw::region_fill<5>(tblw, lut, h); break;
-      case 6: pw::region_fill<6>(tblw, lut, h); break;
-      default: pw::region_fill<7>(tblw, lut, h); break;
-    }
+    prev_q8 = u.q == 8;
   }
-  prev_q8 = u.q == 8;
-  __syncwarp();
-  if (lane == 0) pw::mbar_arrive(bar(sm, kBarRegReady + h));
   return 1;
 }
 
@@ -613,25 +573,28 @@ __device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint
 // epilogue's gate_up completion).
 __device__ __forceinline__ void epilogue_role(const Params& p, const Sm sm, uint32_t tmem) {
   bool prev_q8 = false;
-  int more = lut_fill(p, sm, 0, prev_q8, true);
+  int last = -1;
+  int more = lut_fill(p, sm, 0, prev_q8, true, last);
   uint32_t x0 = 0;
   for (uint32_t i = 0; more == 1; ++i) {
     // fill the next unit's table as soon as it is published, but do not wait
     // for its publication past the moment this unit's accumulators are ready
-    int next = lut_fill(p, sm, i + 1, prev_q8, false);
+    int next = lut_fill(p, sm, i + 1, prev_q8, false, last);
     while (next < 0) {
       int done = 0;
       if ((threadIdx.x & 31) == 0) done = pw::mbar_test(bar(sm, kBarDone + static_cast<int>(i & 1u)), (i >> 1) & 1u);
       if (__shfl_sync(0xffffffffu, done, 0) || sm.st->abort) break;
       __nanosleep(128);
-      next = lut_fill(p, sm, i + 1, prev_q8, false);
+      next = lut_fill(p, sm, i + 1, prev_q8, false, last);
     }
     const uint32_t nt = static_cast<uint32_t>(sm.st->units[i % kUS].nst / 2);
     epilogue_unit(p, sm, tmem, i, x0);
     x0 += nt;
-    if (next < 0) next = lut_fill(p, sm, i + 1, prev_q8, true);
+    if (next < 0) next = lut_fill(p, sm, i + 1, prev_q8, true, last);
     more = next;
   }
+  // the last LUT copy lands before the CTA exits
+  if (last >= 0) drain_bar(sm, kBarRegReady + (last & 1), (static_cast<uint32_t>(last) >> 1) & 1u);
 }
 
 // ---------------------------------------------------------------------------
@@ -751,9 +714,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       pw::mbar_init(bar(sm, kBarDone + i), kIssuers);
       pw::mbar_init(bar(sm, kBarDFree + i), 4);
-      pw::mbar_init(bar(sm, kBarRegReady + i), 4);
+      pw::mbar_init(bar(sm, kBarRegReady + i), 1);
     }
-    pw::mbar_init(bar(sm, kBarQ8Fill), kDeqWarpsAll);
     pw::mbar_init(bar(sm, kBarEpiDone), 4);
     pw::mbar_init(bar(sm, kBarEpiGo), 1);
     for (int s = 0; s < kUS; ++s) {

@@ -88,9 +88,42 @@ __global__ void unpack_kernel(pw::BlockDesc d, int b, uint8_t* __restrict__ out)
   out[i] = static_cast<uint8_t>(v);
 }
 
+// One thread per (row, entry) of a LUT: the entry's tiled byte offset is
+// (strip*2^b + c)*256 + 4*((w%2)*32 + i) + 2*(w/2) for row position pos = 32w + i
+// of its strip, so a strip's table is one contiguous run in the order of the
+// kernels' shared LUT region (one bulk copy per unit).
+__global__ void pack_lut_kernel(const uint16_t* __restrict__ lut, int rows, int bits, uint16_t* __restrict__ out) {
+  const long long n = static_cast<long long>(rows) << bits;
+  for (long long t = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; t < n;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int row = static_cast<int>(t >> bits), c = static_cast<int>(t & ((1ll << bits) - 1));
+    const int half_rows = rows / 2;
+    const int half = row / half_rows, r = row % half_rows;
+    const int strip = r / 64, rr = r % 64, w = rr / 16, i = rr % 16 + 16 * half;
+    const long long byte = ((static_cast<long long>(strip) << bits) + c) * 256 + 4 * ((w % 2) * 32 + i) + 2 * (w / 2);
+    out[byte / 2] = lut[t];
+  }
+}
+
 }  // namespace
 
 extern "C" {
+
+int pw_pack_lut(const uint16_t* d_lut, int64_t rows, int bits, uint16_t* d_out, void* stream) {
+  if (rows <= 0 || rows % pw::kTileRows || rows > (1 << 30))
+    return pw::set_error(PW_ERR_UNSUPPORTED, "pack_lut: rows %lld must be a positive multiple of 128",
+                         static_cast<long long>(rows));
+  if (bits < 1 || bits > PW_MAX_BITS) return pw::set_error(PW_ERR_INVALID_ARG, "pack_lut: bits %d outside 1..8", bits);
+  if (!d_lut || !d_out || d_lut == d_out || (reinterpret_cast<uintptr_t>(d_out) & 15))
+    return pw::set_error(PW_ERR_INVALID_ARG, "pack_lut: NULL, aliased, or output not 16-byte aligned");
+  const long long n = rows << bits;
+  const int threads = 256;
+  const long long blocks = (n + threads - 1) / threads;
+  pack_lut_kernel<<<static_cast<unsigned>(blocks < 65535 ? blocks : 65535), threads, 0, pw::as_stream(stream)>>>(
+      d_lut, static_cast<int>(rows), bits, d_out);
+  PW_CUDA_TRY(cudaGetLastError());
+  return PW_OK;
+}
 
 size_t pw_plane_bytes(int64_t rows, int64_t cols, int layout) {
   if (layout != PW_LAYOUT_TILED || rows <= 0 || cols <= 0 || rows % pw::kTileRows || cols % pw::kTileCols)

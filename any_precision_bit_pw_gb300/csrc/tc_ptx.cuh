@@ -151,6 +151,13 @@ __device__ __forceinline__ uint32_t lds_u16(uint32_t addr) {
   asm("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr));
   return v;
 }
+// The same load, ordered after earlier volatile asm (barrier waits): for
+// addresses that do not depend on data read after the wait.
+__device__ __forceinline__ uint32_t lds_u16_ordered(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void sts_u16(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<uint16_t>(v)) : "memory");
 }

@@ -70,8 +70,9 @@ class APLMoEStack:
     def load_block(self, block: int, idx: torch.Tensor, luts: Dict[int, torch.Tensor], q: int,
                    keep_planes: Optional[int] = None, stream=None) -> None:
         """Pack parent indices (uint8 [rows][cols] on the device) into P planes,
-        keep the top ``keep_planes`` (default q) and the LUTs seed..keep, attach
-        them to the page table and commit q."""
+        keep the top ``keep_planes`` (default q) and the LUTs seed..keep
+        (row-major fp16, stored in the tiled LUT layout), attach them to the
+        page table and commit q."""
         rows, cols = self.block_shape(block % 2)
         assert tuple(idx.shape) == (rows, cols)
         keep = q if keep_planes is None else keep_planes
@@ -87,8 +88,10 @@ class APLMoEStack:
         for b in range(self.S, keep + 1):
             t = luts[b].to(self.device).contiguous()
             assert t.dtype == torch.float16 and tuple(t.shape) == (rows, 1 << b)
-            self.luts[block][b] = t
-            pw.pw_page_table_attach_lut(self.table, block, b, t.data_ptr())
+            tiled = torch.empty_like(t)
+            pw.pw_pack_lut(t, tiled, stream=stream)     # LUT pages are stored in the tiled LUT layout
+            self.luts[block][b] = tiled
+            pw.pw_page_table_attach_lut(self.table, block, b, tiled.data_ptr())
         self.commit(block, q)
 
     def commit(self, block: int, q: int) -> int:

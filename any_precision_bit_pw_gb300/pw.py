@@ -39,7 +39,7 @@ ERR_NAMES = {0: "PW_OK", -1: "PW_ERR_INVALID_ARG", -2: "PW_ERR_UNSUPPORTED", -3:
              -4: "PW_ERR_CUDA", -5: "PW_ERR_TIMEOUT", -6: "PW_ERR_WORKSPACE", -7: "PW_ERR_BUSY"}
 
 EXPORTS = (
-    "pw_last_error", "pw_plane_bytes", "pw_pack_bitplanes", "pw_desc_bytes", "pw_page_table_create",
+    "pw_last_error", "pw_plane_bytes", "pw_pack_bitplanes", "pw_pack_lut", "pw_desc_bytes", "pw_page_table_create",
     "pw_page_table_destroy", "pw_page_table_attach_plane", "pw_page_table_attach_lut",
     "pw_page_table_set_desired", "pw_page_table_set_bits", "pw_page_table_get", "pw_page_table_bytes",
     "pw_page_table_resident_bytes", "pw_page_table_sync", "pw_moe_route_topk", "pw_moe_route_topk_shared",
@@ -82,6 +82,7 @@ def lib() -> ctypes.CDLL:
             "pw_last_error": (ctypes.c_char_p, []),
             "pw_plane_bytes": (SZ, [I64, I64, I32]),
             "pw_pack_bitplanes": (I32, [P, I64, I64, I32, ctypes.POINTER(P), I32, P]),
+            "pw_pack_lut": (I32, [P, I64, I32, P, P]),
             "pw_desc_bytes": (SZ, [I32]),
             "pw_page_table_create": (I32, [ctypes.POINTER(P), I32, ctypes.POINTER(pw_block_info)]),
             "pw_page_table_destroy": (I32, [P]),
@@ -161,6 +162,16 @@ def pw_pack_bitplanes(idx: torch.Tensor, parent_bits: int, planes: Sequence[torc
     arr = (P * parent_bits)(*[p.data_ptr() for p in planes])
     _check(lib().pw_pack_bitplanes(_ptr(idx), idx.shape[0], idx.shape[1], parent_bits, arr, layout,
                                    _stream(stream)))
+
+
+def pw_pack_lut(lut: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """fp16 [rows][2^b] row-major LUT -> `out` (same size) in the tiled LUT layout."""
+    _dev(lut, torch.float16, "lut")
+    rows, C = lut.shape
+    bits = C.bit_length() - 1
+    if C != 1 << bits or not out.is_cuda or out.numel() * out.element_size() < rows * C * 2:
+        raise ValueError("pack_lut: need lut [rows][2^b] and an output of the same size")
+    _check(lib().pw_pack_lut(_ptr(lut), rows, bits, _ptr(out), _stream(stream)))
 
 
 def pw_desc_bytes(n_blocks: int) -> int:

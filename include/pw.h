@@ -77,6 +77,18 @@ size_t pw_plane_bytes(int64_t rows, int64_t cols, int layout);
 int pw_pack_bitplanes(const uint8_t* d_idx, int64_t rows, int64_t cols, int parent_bits,
                       uint32_t* const* h_planes, int layout, void* stream);
 
+/* Rearrange a LUT (fp16 [rows][2^bits] row-major, one row of centroids per
+ * output row, Figure 3 caption) into the tiled LUT layout that LUT pages are
+ * stored in (pw_page_table_attach_lut):
+ *   with half, strip, rr of row n as above, w = rr/16, i = rr%16 + 16*half,
+ *   entry c of row n is the fp16 at byte
+ *     (strip*2^bits + c)*256 + 4*((w%2)*32 + i) + 2*(w/2)
+ * so the table of a 128-row strip is one contiguous run of 2^bits*256 bytes
+ * (the order of the kernels' shared LUT region; a unit copies it in one
+ * piece).  d_out: rows*2^bits*2 bytes, 16-byte aligned, not d_lut.
+ * rows % 128 == 0, bits 1..8.  Asynchronous on `stream`. */
+int pw_pack_lut(const uint16_t* d_lut, int64_t rows, int bits, uint16_t* d_out, void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Weight page table (§3 and §3.1; Eq. 3)                                      */
 /* ------------------------------------------------------------------------ */
@@ -107,8 +119,9 @@ int pw_page_table_destroy(pw_page_table* t);
  * marks that plane GPU-resident.  The buffer must stay valid while attached. */
 int pw_page_table_attach_plane(pw_page_table* t, int block, int plane, const uint32_t* d_plane);
 
-/* Attach the LUT of bitwidth `bits` (seed..parent): fp16 [rows][2^bits],
- * 16-byte aligned, one row of centroids per output row (Figure 3 caption). */
+/* Attach the LUT of bitwidth `bits` (seed..parent): rows*2^bits fp16 in the
+ * tiled LUT layout (pw_pack_lut), 16-byte aligned, one row of centroids per
+ * output row (Figure 3 caption). */
 int pw_page_table_attach_lut(pw_page_table* t, int block, int bits, const uint16_t* d_lut);
 
 /* Record the planner's desired bitwidth d_i (bookkeeping; §3: q_i, not d_i,

@@ -53,6 +53,16 @@ def test_pack_bytes_match_oracle(N, K, P):
         assert np.array_equal(got, ref)
 
 
+@pytest.mark.parametrize("N,b", [(128, 2), (256, 3), (1024, 5), (4096, 8), (28672, 4)])
+def test_pack_lut_matches_oracle(N, b):
+    g = torch.Generator().manual_seed(N + b)
+    lut = (torch.randn((N, 1 << b), generator=g) * 0.02).to(torch.float16)
+    out = torch.empty((N, 1 << b), dtype=torch.float16, device=DEV)
+    pw.pw_pack_lut(lut.to(DEV).contiguous(), out)
+    torch.cuda.synchronize()
+    assert np.array_equal(out.view(torch.uint8).cpu().numpy().reshape(-1), apl.pack_lut_tiled(lut.numpy()))
+
+
 def _table_for(idx_dev, P, S, luts=None, q=None):
     N, K = idx_dev.shape
     t = pw.pw_page_table_create([pw.pw_block_info(N, K, P, S, pw.PW_LAYOUT_TILED, 0)])
@@ -63,8 +73,10 @@ def _table_for(idx_dev, P, S, luts=None, q=None):
     keep = [planes]
     if luts is not None:
         for b, l in luts.items():
-            pw.pw_page_table_attach_lut(t, 0, b, l.data_ptr())
-            keep.append(l)
+            lt = torch.empty_like(l)
+            pw.pw_pack_lut(l, lt)           # LUT pages are stored in the tiled LUT layout
+            pw.pw_page_table_attach_lut(t, 0, b, lt.data_ptr())
+            keep.append(lt)
         pw.pw_page_table_set_bits(t, 0, q)
     return t, keep
 

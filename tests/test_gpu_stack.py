@@ -90,8 +90,8 @@ def test_stack_offload_keeps_host_copies_and_parity():
     """The stack driver in offload mode (§3.3) on a three-layer tiny stack:
     lowering copies the released pages to pinned host memory first; once the
     copies finished, every page above its block's committed bitwidth is
-    CPU-resident only and its host bytes are the oracle's packed plane (or the
-    LUT); layer outputs follow the committed bitwidths; reloading every
+    CPU-resident only and its host bytes are the oracle's packed plane (or
+    tiled LUT); layer outputs follow the committed bitwidths; reloading every
     lowered block and raising it back restores the 4-bit outputs."""
     wl = synth.TINY_LAYER.with_(name="tiny_stack", tokens=24, bits_mode="fixed", fixed_bits=4,
                                 logits_mode="biased", layers=3)
@@ -121,7 +121,7 @@ def test_stack_offload_keeps_host_copies_and_parity():
                 assert np.array_equal(host, np.ascontiguousarray(ref_planes[page]).view(np.uint8).reshape(-1))
             else:
                 lut = synth.lut(wl, layer, e, u, page - pw.PW_MAX_BITS, DEV).cpu().numpy()
-                assert np.array_equal(host, lut.view(np.uint8).reshape(-1))
+                assert np.array_equal(host, apl.pack_lut_tiled(lut))
     assert lowered
     # outputs at the committed bitwidths
     for layer in range(run.L):
