@@ -64,7 +64,7 @@ struct Params {
   uint32_t* ctr;           // [0] ticket, [1] abort, [2, 2+E*nsplit) gate_up done, then strip arrivals
   uint32_t* gather_ctr;    // CTAs that finished their share of xp; [1]: CTAs done with all units;
                            // [2]: routing arrays written (routed call)
-  int grid_combine;        // 1: every CTA combines after the last unit (large batches)
+  int grid_combine;        // 1: every CTA combines after the last unit; 0: a strip's last down unit does
   // Routed call (routing in the same launch): CTA 0 computes ids, w, offsets,
   // perm and inv_perm from the logits and publishes them through
   // gather_ctr[2]; NULL logits: the routing arrays are inputs.  The kernels

@@ -34,6 +34,7 @@ PW_LAYOUT_TILED = 1
 PW_MAX_BITS = 8
 PW_PATH_AUTO, PW_PATH_DECODE, PW_PATH_PREFILL = 0, 1, 2
 PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL = 1
+PW_FFN_FLAG_STRIP_COMBINE = 2
 
 ERR_NAMES = {0: "PW_OK", -1: "PW_ERR_INVALID_ARG", -2: "PW_ERR_UNSUPPORTED", -3: "PW_ERR_NOT_RESIDENT",
              -4: "PW_ERR_CUDA", -5: "PW_ERR_TIMEOUT", -6: "PW_ERR_WORKSPACE", -7: "PW_ERR_BUSY"}

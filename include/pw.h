@@ -279,8 +279,8 @@ size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k);
  * Shapes: H % 128 == 0, I % 128 == 0, committed bitwidths 2..8.
  * The call picks the token-tile width from the average number of tokens per
  * expert (T*k/E): tiles of 16 tokens up to 16, of 32 below 48 (the decode
- * path), else of 64 (the prefill path, whose combine runs over the whole grid
- * after the last unit).  All run on the tcgen05 tensor cores;
+ * path), else of 64 (the prefill path).  The top-k weighted combine runs
+ * over the whole grid after the last unit.  All run on the tcgen05 tensor cores;
  * pw_moe_apl_ffn_ex can force either path. */
 int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
                    int E, int k, const int32_t* d_ids, const float* d_w,
@@ -321,6 +321,11 @@ int pw_moe_apl_ffn_noalloc(const void* d_desc, int layer, const uint16_t* d_x, i
 #define PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL 1u  /* test hook: one gate_up unit never
                                                  signals completion, so the waits
                                                  that depend on it run out */
+#define PW_FFN_FLAG_STRIP_COMBINE 2u          /* the CTA that finishes a 128-row
+                                                 strip's last down unit combines
+                                                 that strip, instead of the whole
+                                                 grid combining after the last
+                                                 unit (same result, bit for bit) */
 typedef struct pw_ffn_options {
   int32_t path;              /* PW_PATH_* */
   uint32_t flags;            /* PW_FFN_FLAG_* */

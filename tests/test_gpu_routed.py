@@ -164,3 +164,20 @@ def test_shared_expert_layers(name):
     y_ref = apl.moe_layer(li.x.cpu().numpy(), r["ids"], r["w"], sh.intermediate, blocks, tokens=toks)
     m = apl.compare(y_ref[toks], yf.float().cpu().numpy()[toks])
     assert m["rel_l2"] <= 2e-3 and m["max_abs_over_rms"] <= 1e-2, m
+
+
+@pytest.mark.parametrize("name,T", [("8x7b", 32), ("8x7b", 100), ("tiny", 40), ("8x7b", 256)])
+def test_strip_combine_equals_grid_combine(name, T):
+    """The two combine placements (whole grid after the last unit, or each
+    strip in the CTA of its last down unit) add the same terms in the same
+    order: y is identical bit for bit."""
+    li = _inputs(name, T)
+    st = _stack(li)
+    call = MoECall(st, T)
+    y_grid = call(0, li.x, li.logits).clone()
+    opts = pw.pw_ffn_options()
+    opts.flags = pw.PW_FFN_FLAG_STRIP_COMBINE
+    y_strip = call(0, li.x, li.logits, options=opts).clone()
+    torch.cuda.synchronize()
+    assert int(call.status.item()) == 0
+    assert torch.equal(y_grid, y_strip)
