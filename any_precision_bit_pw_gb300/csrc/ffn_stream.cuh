@@ -453,15 +453,34 @@ __device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t 
 // ---------------------------------------------------------------------------
 // epilogue warps: LUT region one unit ahead, then the unit's epilogue
 // ---------------------------------------------------------------------------
-// Copy unit i's LUT into region half i & 1 (q = 8: the whole region) once
-// every earlier user of those lines is finished: one bulk copy of the strip's
-// table (LUT pages are stored in the region's order, 2^q lines of 256 bytes
-// per strip), issued by thread 0 of the epilogue warps; the half's barrier
-// completes when the bytes land.  Returns 1 when done, 0 when unit i is the
-// end marker, and -1 without waiting when `block` is false and unit i is not
-// published yet.  `last` (thread 0) records the last copy, drained at exit.
+// Copies of the units' LUTs into the shared region go out in unit order, from
+// thread 0 of the epilogue warps; `next` is the first unit not copied yet and
+// `last` the last one copied (drained at exit).
+struct LutCopies {
+  uint32_t next = 0;
+  int last = -1;
+};
+
+// One bulk copy of unit i's table (its strip's run of 2^q lines) into region
+// half i & 1 (q = 8: the whole region), completing the half's barrier by its
+// bytes.  The caller has seen every earlier user of those lines finish.
+__device__ __forceinline__ void copy_lut(const Sm sm, uint32_t i, const Unit& u) {
+  const int h = static_cast<int>(i & 1u);
+  const uint32_t b = bar(sm, kBarRegReady + h);
+  const uint32_t bytes = 256u << u.q;
+  const char* src = reinterpret_cast<const char*>(u.d->lut) + static_cast<long long>(u.strip) * bytes;
+  pw::fence_proxy_async_smem();   // the lines' earlier generic accesses before the async write
+  pw::mbar_arrive_expect_tx(b, bytes);
+  pw::bulk_g2s(sm.region + (u.q == 8 ? 0u : static_cast<uint32_t>(h) * 32768u), src, bytes, b);
+}
+
+// Copy unit i's LUT unless it went out early (lut_early), once every earlier
+// user of its lines is finished: units up to i - 2 (the half's previous
+// user), or up to i - 1 when unit i or i - 1 takes the whole region.  Returns
+// 1 when done, 0 when unit i is the end marker, and -1 without waiting when
+// `block` is false and unit i is not published yet.
 __device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i, bool& prev_q8, bool block,
-                                        int& last) {
+                                        LutCopies& lc) {
   const int lane = threadIdx.x & 31;
   const int etid = threadIdx.x - kEpiWarp0 * 32;
   if (!block) {
@@ -473,27 +492,40 @@ __device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i
   const Unit& u = sm.st->units[i % kUS];
   if (u.kind == kNone) return 0;
   if (etid == 0) {
-    const int h = static_cast<int>(i & 1u);
-    const uint32_t b = bar(sm, kBarRegReady + h);
-    // units up to i - 2 (the half's previous user), or up to i - 1 when unit
-    // i or i - 1 takes the whole region, are finished by every dequant warp
-    const uint32_t need = static_cast<uint32_t>(kDeqWarpsAll) * ((u.q == 8 || prev_q8) ? i : (i >= 1 ? i - 1 : 0u));
-    if (wait_count(sm, &sm.st->deq_done, need, p)) {
-      const uint32_t bytes = 256u << u.q;
-      const char* src = reinterpret_cast<const char*>(u.d->lut) + static_cast<long long>(u.strip) * bytes;
-      pw::fence_proxy_async_smem();   // the lines' earlier generic accesses before the async write
-      pw::mbar_arrive_expect_tx(b, bytes);
-      pw::bulk_g2s(sm.region + (u.q == 8 ? 0u : static_cast<uint32_t>(h) * 32768u), src, bytes, b);
-      last = static_cast<int>(i);
-    } else {
-      pw::mbar_arrive(b);   // giving up: complete the phase so that no waiter hangs on it
+    if (lc.next <= i) {
+      const uint32_t need = static_cast<uint32_t>(kDeqWarpsAll) * ((u.q == 8 || prev_q8) ? i : (i >= 1 ? i - 1 : 0u));
+      if (wait_count(sm, &sm.st->deq_done, need, p)) {
+        copy_lut(sm, i, u);
+        lc.last = static_cast<int>(i);
+      } else {
+        pw::mbar_arrive(bar(sm, kBarRegReady + static_cast<int>(i & 1u)));   // giving up: complete the phase
+      }
+      lc.next = i + 1;
     }
     prev_q8 = u.q == 8;
   }
   return 1;
 }
 
-__device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint32_t tmem, uint32_t i, uint32_t x0) {
+// Thread 0 of the epilogue warps, once unit j - 2's MMAs are done: copy unit
+// j's table now if it is next in order, published, neither j nor j - 1 takes
+// the whole region, and every dequant warp has finished unit j - 2 (the
+// half's previous user).  Otherwise lut_fill copies it later.  Never waits.
+__device__ __forceinline__ void lut_early(const Sm sm, uint32_t j, LutCopies& lc) {
+  if (lc.next != j || j < 2) return;
+  if (!pw::mbar_test(bar(sm, kBarUReady + static_cast<int>(j % kUS)), (j / kUS) & 1u)) return;
+  const Unit& u = sm.st->units[j % kUS];
+  const Unit& prev = sm.st->units[(j - 1) % kUS];
+  if (u.kind == kNone || u.q == 8 || prev.q == 8) return;
+  if (*reinterpret_cast<volatile uint32_t*>(&sm.st->deq_done) < static_cast<uint32_t>(kDeqWarpsAll) * (j - 1)) return;
+  __threadfence_block();
+  copy_lut(sm, j, u);
+  lc.last = static_cast<int>(j);
+  lc.next = j + 1;
+}
+
+__device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint32_t tmem, uint32_t i, uint32_t x0,
+                                              LutCopies& lc) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int qd = warp & 3;
   const int pos = qd * 32 + lane;
@@ -502,6 +534,7 @@ __device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint
   const Unit& u = st.units[i % kUS];
   const uint32_t db = i & 1u;
   const bool ok = wait_bar(sm, kBarDone + static_cast<int>(db), (i >> 1) & 1u, p);
+  if (etid == 0 && ok) lut_early(sm, i + 2, lc);   // unit i's region half is free again
   const uint32_t nt = static_cast<uint32_t>(u.nst / 2);
   const BlockDesc& d = *u.d;
   const int row = strip_pos_row(u.strip, pos, d.rows / 2);
@@ -573,28 +606,28 @@ __device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint
 // epilogue's gate_up completion).
 __device__ __forceinline__ void epilogue_role(const Params& p, const Sm sm, uint32_t tmem) {
   bool prev_q8 = false;
-  int last = -1;
-  int more = lut_fill(p, sm, 0, prev_q8, true, last);
+  LutCopies lc;
+  int more = lut_fill(p, sm, 0, prev_q8, true, lc);
   uint32_t x0 = 0;
   for (uint32_t i = 0; more == 1; ++i) {
     // fill the next unit's table as soon as it is published, but do not wait
     // for its publication past the moment this unit's accumulators are ready
-    int next = lut_fill(p, sm, i + 1, prev_q8, false, last);
+    int next = lut_fill(p, sm, i + 1, prev_q8, false, lc);
     while (next < 0) {
       int done = 0;
       if ((threadIdx.x & 31) == 0) done = pw::mbar_test(bar(sm, kBarDone + static_cast<int>(i & 1u)), (i >> 1) & 1u);
       if (__shfl_sync(0xffffffffu, done, 0) || sm.st->abort) break;
       __nanosleep(128);
-      next = lut_fill(p, sm, i + 1, prev_q8, false, last);
+      next = lut_fill(p, sm, i + 1, prev_q8, false, lc);
     }
     const uint32_t nt = static_cast<uint32_t>(sm.st->units[i % kUS].nst / 2);
-    epilogue_unit(p, sm, tmem, i, x0);
+    epilogue_unit(p, sm, tmem, i, x0, lc);
     x0 += nt;
-    if (next < 0) next = lut_fill(p, sm, i + 1, prev_q8, true, last);
+    if (next < 0) next = lut_fill(p, sm, i + 1, prev_q8, true, lc);
     more = next;
   }
   // the last LUT copy lands before the CTA exits
-  if (last >= 0) drain_bar(sm, kBarRegReady + (last & 1), (static_cast<uint32_t>(last) >> 1) & 1u);
+  if (lc.last >= 0) drain_bar(sm, kBarRegReady + (lc.last & 1), (static_cast<uint32_t>(lc.last) >> 1) & 1u);
 }
 
 // ---------------------------------------------------------------------------
