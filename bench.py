@@ -90,12 +90,14 @@ def measured_traffic(kernel: str, workload: str, tokens: int):
     record or the kernel's code changed since it was taken."""
     try:
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
-            rec = json.load(f)[kernel]
-        if rec["workload"] != workload or int(rec["tokens"]) != tokens:
-            return None
-        paths = [os.path.join(ROOT, "any_precision_bit_pw_gb300", "csrc", n) for n in rec["source_files"]]
-        return float(rec["dram_bytes_per_launch"]) if source_digest(paths) == rec["source_sha256"] else None
-    except (OSError, KeyError, ValueError):
+            recs = json.load(f)[kernel]
+        for rec in recs:
+            if rec["workload"] != workload or int(rec["tokens"]) != tokens:
+                continue
+            paths = [os.path.join(ROOT, "any_precision_bit_pw_gb300", "csrc", n) for n in rec["source_files"]]
+            return float(rec["dram_bytes_per_launch"]) if source_digest(paths) == rec["source_sha256"] else None
+        return None
+    except (OSError, KeyError, ValueError, TypeError):
         return None
 
 
@@ -108,13 +110,15 @@ def get_workload(name: str, tokens=None):
 def ffn_kernel(tokens: int, top_k: int, experts: int) -> str:
     """The fused-layer kernel pw_moe_apl_ffn picks for this size (token-tile
     width from the average tokens per expert, as in the library)."""
-    A = tokens * top_k
-    if A >= 48 * experts:
-        return "apl_prefill_kernel"
-    return "apl_decode_kernel" if A <= 16 * experts else "apl_decode32_kernel"
+    return "apl_ffn_t16_kernel" if tokens * top_k < 12 * experts else "apl_ffn_t64_kernel"
 
 
-KERNEL_TILE = {"apl_decode_kernel": 16, "apl_decode32_kernel": 32, "apl_prefill_kernel": 64}
+def prefill_path(tokens: int, top_k: int, experts: int) -> bool:
+    """The library's path choice: routing is a launch of its own on the prefill path."""
+    return tokens * top_k >= 48 * experts
+
+
+KERNEL_TILE = {"apl_ffn_t16_kernel": 16, "apl_ffn_t64_kernel": 64}
 
 
 def kernel_label(name: str) -> str:
@@ -266,7 +270,7 @@ def gpu_arm(args, rank, world, local_rank):
     call = MoECall(stack, wl.tokens)
     stream = torch.cuda.current_stream()
     kname = ffn_kernel(wl.tokens, sh.top_k + sh.shared, sh.total_experts)
-    routed = kname != "apl_prefill_kernel"
+    routed = not prefill_path(wl.tokens, sh.top_k + sh.shared, sh.total_experts)
 
     # routing of each batch (for the algorithmic byte count)
     bytes_per_batch = []
@@ -398,7 +402,7 @@ def stack_arm(args, rank, world, local_rank):
     lgs = [[synth.router_logits(wl, l, s, dev) for l in range(L)] for s in range(n_in)]
     call, stack = run.call, run.stack
     stream = torch.cuda.current_stream()
-    routed = ffn_kernel(T, sh.top_k, E) != "apl_prefill_kernel"
+    routed = not prefill_path(T, sh.top_k, E)
 
     # warm-up: the layer calls without step boundaries (no commits, no mass)
     for i in range(args.warmup):

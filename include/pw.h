@@ -278,8 +278,9 @@ size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k);
  *  untouched on success, so the caller zeroes it beforehand).
  * Shapes: H % 128 == 0, I % 128 == 0, committed bitwidths 2..8.
  * The call picks the token-tile width from the average number of tokens per
- * expert (T*k/E): tiles of 16 tokens up to 16, of 32 below 48 (the decode
- * path), else of 64 (the prefill path).  The top-k weighted combine runs
+ * expert (T*k/E): tiles of 16 tokens below 12, else of 64; and the path:
+ * below 48 the decode path (down projection split over I in 2048-column
+ * parts), else the prefill path (no split).  The top-k weighted combine runs
  * over the whole grid after the last unit.  All run on the tcgen05 tensor cores;
  * pw_moe_apl_ffn_ex can force either path. */
 int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
@@ -316,8 +317,8 @@ int pw_moe_apl_ffn_noalloc(const void* d_desc, int layer, const uint16_t* d_x, i
 
 /* Options of pw_moe_apl_ffn_ex (zero-initialise, then set what you need). */
 #define PW_PATH_AUTO 0
-#define PW_PATH_DECODE 1   /* token tiles of 16 or 32 (decode batches) */
-#define PW_PATH_PREFILL 2  /* token tiles of 64 (prefill batches) */
+#define PW_PATH_DECODE 1   /* down split over I; routing inside the routed call's launch */
+#define PW_PATH_PREFILL 2  /* down over all of I; routing as its own launch in a routed call */
 #define PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL 1u  /* test hook: one gate_up unit never
                                                  signals completion, so the waits
                                                  that depend on it run out */
