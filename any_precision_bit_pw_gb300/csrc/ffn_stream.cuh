@@ -543,8 +543,11 @@ __device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint
   // x % kIssuers == k, i.e. the unit's tiles t with t = k - x0 mod kIssuers).
   // The partial sums are added in the order of that residue, not of the
   // issuer, so the result does not depend on which CTA took the unit.
+  // only the column chunks that hold the unit's tokens (a 64-token tile with
+  // a small token group reads one chunk, not four)
+  const int nc16 = min(kN / 16, (u.nrows + 15) / 16);
 #pragma unroll 1
-  for (int c16 = 0; c16 < kN / 16; ++c16) {
+  for (int c16 = 0; c16 < nc16; ++c16) {
     float acc[16];
 #pragma unroll
     for (int n = 0; n < 16; ++n) acc[n] = 0.f;
@@ -560,7 +563,7 @@ __device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint
         for (int n = 0; n < 16; ++n) acc[n] += __uint_as_float(v[n]);
       }
     }
-    if (c16 == kN / 16 - 1) {
+    if (c16 == nc16 - 1) {
       pw::tc_fence_before();
       __syncwarp();
       if (lane == 0) pw::mbar_arrive(bar(sm, kBarDFree + static_cast<int>(db)));   // all columns read
