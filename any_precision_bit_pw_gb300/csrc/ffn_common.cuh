@@ -40,7 +40,7 @@ constexpr int kAStages = 4;
 constexpr int kACols = pw::kStageK / 2;     // 32 TMEM columns (fp16 pairs) per stage
 constexpr int kDCol = kAStages * kACols;    // accumulator columns start here (per group)
 constexpr int kRingBytes = 32768;           // per group: plane staging ring [slot][plane][pos][16 B]
-constexpr int kDecodeSplitCols = 2048;      // down K-split of the decode path
+constexpr int kDecodeSplitCols = 3072;      // down K-split of the decode path (24 tiles; measured best of 2048, 3072, 4096)
 constexpr int kMaxE = 256;
 constexpr int kBarsPerGroup = 16;
 

@@ -279,7 +279,7 @@ size_t pw_moe_apl_ffn_workspace(int T, int H, int I, int E, int k);
  * Shapes: H % 128 == 0, I % 128 == 0, committed bitwidths 2..8.
  * The call picks the token-tile width from the average number of tokens per
  * expert (T*k/E): tiles of 16 tokens below 12, else of 64; and the path:
- * below 48 the decode path (down projection split over I in 2048-column
+ * below 48 the decode path (down projection split over I in 3072-column
  * parts), else the prefill path (no split).  The top-k weighted combine runs
  * over the whole grid after the last unit.  All run on the tcgen05 tensor cores;
  * pw_moe_apl_ffn_ex can force either path. */
@@ -298,7 +298,7 @@ int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, in
  * PW_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU that loads the library
  * holds until the process exits.  Calls whose workspace
  * (pw_moe_apl_ffn_workspace) exceeds it fail with PW_ERR_WORKSPACE before
- * anything is enqueued; for the Mixtral-8x7B shape that allows up to 110
+ * anything is enqueued; for the Mixtral-8x7B shape that allows up to 141
  * tokens per call at top-2.  This entry point allocates nothing itself (no
  * cudaMalloc/cudaFree, no allocating library routine).
  *  - The first call on a device looks up the array's device address (a one-off

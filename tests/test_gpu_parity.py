@@ -276,7 +276,9 @@ def test_ffn_is_deterministic():
     (256, 256, 1, 1, 5, (3, 5)),          # single expert, k = 1
     (256, 512, 2, 2, 80, (8, 2)),         # 80 tokens per expert: several token tiles on the decode path
     (512, 768, 4, 2, 1, (4, 7)),          # one token
-    (256, 2304, 3, 1, 9, (6, 3)),         # I not a multiple of the 2048-column down split
+    (256, 2304, 3, 1, 9, (6, 3)),         # I below the 3072-column down split
+    (256, 3200, 2, 1, 6, (5, 8)),         # I = 3072 + 128: a one-tile last down split
+    (128, 6272, 2, 2, 3, (3, 4)),         # I = 2 * 3072 + 128, H of one strip
     (384, 640, 2, 2, 300, (5, 4)),        # odd strip counts, 300 tokens per expert
 ])
 def test_ffn_edge_shapes(H, I, E, k, T, bits, path):
