@@ -554,7 +554,7 @@ def sweep(args, dev, out_path):
 # ---------------------------------------------------------------------------
 # the reference arm / CPU baseline: the oracle on the host cores
 # ---------------------------------------------------------------------------
-def oracle_sample(workload: str, experts_in_sample: int = 1, tokens=None) -> dict:
+def oracle_sample(workload: str, experts_in_sample: int = 3, tokens=None) -> dict:
     """Time the oracle on a bounded sample of the workload: the layer output
     contribution of the first ``experts_in_sample`` active experts (their
     gate_up and down blocks read from the packed bit-planes at the committed
@@ -592,6 +592,62 @@ def oracle_sample(workload: str, experts_in_sample: int = 1, tokens=None) -> dic
                       + (f" and by {wl.layers} layers" if wl.layers > 1 else "")}
 
 
+def oracle_steps(workload: str, steps: int, budget_s: float = 100.0, tokens=None) -> dict:
+    """The reference arm's steps.  Set-up (routing, packing the first active
+    expert's two blocks) runs once, and so does the oracle's own block path
+    (apl_linear over both whole blocks for that expert's routed tokens; the
+    down block's input is a stand-in of h's shape), timed.  Each step then
+    times the same unpack, dequantisation and matmul on one 128-row strip of
+    one block (the two in turn), scaled to that block's measured whole-block
+    time, the expert's two blocks and the number of active experts.  A step
+    costs tens of milliseconds, so a thousand steps end within minutes."""
+    from oracle import apl
+    wl = get_workload(workload, tokens)
+    sh = wl.shape
+    x = synth.activations(wl).numpy()
+    r = apl.route_topk_shared(synth.router_logits(wl).numpy(), sh.top_k, sh.shared)
+    active = [e for e in range(sh.total_experts) if r["offsets"][e + 1] > r["offsets"][e]]
+    e = active[0]
+    li = synth.layer_inputs(wl, experts=[e])
+    xe = x[np.nonzero((r["ids"] == e).any(axis=1))[0]].astype(np.float64)
+    blocks = []
+    for u in (0, 1):
+        idx = li.idx[(e, u)].numpy()
+        N, K = idx.shape
+        q = li.bits[2 * e + u]
+        inp = xe if u == 0 else np.ones((xe.shape[0], K))
+        blocks.append((apl.pack_bitplanes(idx, wl.parent_bits), li.luts[(e, u)][q].numpy(), q, N, K, inp))
+
+    def strip_time(b):
+        """Seconds block b would take, from one whole 128-row strip (the
+        oracle unpacks by strip) scaled by the strip count."""
+        planes, lut, q, N, K, inp = blocks[b]
+        t0 = time.perf_counter()
+        W = apl.dequant(apl.unpack_indices(planes, q, N, K, (0, 128)), lut, (0, 128))
+        _ = inp @ W.T
+        return (time.perf_counter() - t0) * N / 128
+
+    # the oracle's own path (apl_linear over each whole block, 2048-row
+    # chunks) once, timed: a strip stays in cache and costs less per weight,
+    # so each step's strip is scaled to its block's measured whole-block cost
+    t_block = []
+    for planes, lut, q, N, K, inp in blocks:
+        t0 = time.perf_counter()
+        apl.apl_linear(planes, lut, q, N, K, inp)
+        t_block.append(time.perf_counter() - t0)
+    t_full = sum(t_block)
+    ratio = [t_block[b] / max(np.mean([strip_time(b) for _ in range(3)]), 1e-9) for b in range(2)]
+    est = []
+    for i in range(max(1, steps)):
+        b = i % 2          # one strip of one block per step, the two blocks in turn
+        est.append(strip_time(b) * ratio[b] * t_full / t_block[b] * len(active) * wl.layers)
+    return {"est_layer_s": est, "sample": f"the oracle's apl_linear on both blocks of 1 of {len(active)} active experts "
+            f"timed once ({t_full:.2f} s); each step times its unpack + dequant + matmul on one 128-row strip of one "
+            f"block (in turn), scaled to that block's measured whole-block time, the expert's two blocks and "
+            f"{len(active)} active experts"
+            + (f" and {wl.layers} layers" if wl.layers > 1 else "")}
+
+
 def _child_cmd(workload: str, tokens=None) -> list:
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", workload]
     return cmd + ["--tokens", str(tokens)] if tokens else cmd
@@ -614,18 +670,11 @@ def reference_arm(args, rank, world):
     if rank != 0:
         return None
     wl = get_workload(args.workload, args.tokens)
-    times = []
-    sample = ""
-    for _ in range(args.warmup):
-        pass  # the oracle has no warm-up state
-    for _ in range(max(1, args.steps)):
-        d = json.loads(subprocess.run(
-            _child_cmd(args.workload, args.tokens),
-            env=dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-                     CUDA_VISIBLE_DEVICES=""), capture_output=True, text=True, timeout=600
-        ).stdout.strip().splitlines()[-1])
-        times.append(d["est_layer_s"])
-        sample = d["sample"]
+    cmd = _child_cmd(args.workload, args.tokens) + ["--steps", str(max(1, args.steps)), "--reference-child"]
+    d = json.loads(subprocess.run(cmd, env=dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
+                                                MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES=""),
+                                  capture_output=True, text=True, timeout=900).stdout.strip().splitlines()[-1])
+    times, sample = d["est_layer_s"], d["sample"]
     ms = 1e3 * float(np.mean(times))
     value = wl.tokens / (ms * 1e-3)
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": len(times),
@@ -649,10 +698,14 @@ def main():
     ap.add_argument("--sweep", default=None, help="also run the uniform-bitwidth sweep, JSON to this path")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--reference-child", action="store_true", help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "pw":
         args.warmup = 3
 
+    if args.cpu_baseline_child and args.reference_child:
+        print(json.dumps(oracle_steps(args.workload, args.steps, tokens=args.tokens)))
+        return
     if args.cpu_baseline_child:
         print(json.dumps(oracle_sample(args.workload, tokens=args.tokens)))
         return
