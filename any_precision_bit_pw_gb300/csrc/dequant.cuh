@@ -17,9 +17,11 @@
 //    into registers as a low-byte and a high-byte table, and one prmt looks
 //    up four 8-bit halves at once (q = 4 selects between two 8-entry halves
 //    with a byte mask built from the index MSB);
-//  * q >= 4 in the kernels: an 8x8 bit transpose of the plane words yields
-//    byte indices, one prmt forms each lookup address in the region, and
-//    lookups never conflict.
+//  * q >= 4 in the kernels: a bit transpose of the plane words yields byte
+//    indices (an 8x8 transpose for q >= 6; for q <= 5 a 4x4 transpose inside
+//    nibbles for the low four index bits, the rest merged per nibble, which
+//    takes 28 logic ops per 32 columns at q = 4 instead of 44), one prmt forms
+//    each lookup address in the region, and lookups never conflict.
 #pragma once
 
 #include "tc_ptx.cuh"
@@ -155,6 +157,24 @@ __device__ __forceinline__ void transpose8x8(uint32_t (&X)[8]) {
   }
 }
 
+// 4x4 bit-matrix transpose inside every nibble of four words (two rounds of
+// delta swaps): afterwards bit c of nibble n of L[i] holds what was bit i of
+// nibble n of L[c].
+__device__ __forceinline__ void transpose4x4(uint32_t (&L)[4]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t a = L[i], b = L[i + 2];
+    L[i] = (a & 0x33333333u) | (shl_mul(b, 2) & 0xCCCCCCCCu);
+    L[i + 2] = (shr_mul(a, 2) & 0x33333333u) | (b & 0xCCCCCCCCu);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; i += 2) {
+    const uint32_t a = L[i], b = L[i + 1];
+    L[i] = (a & 0x55555555u) | (shl_mul(b, 1) & 0xAAAAAAAAu);
+    L[i + 1] = (shr_mul(a, 1) & 0x55555555u) | (b & 0xAAAAAAAAu);
+  }
+}
+
 // The LUTs of a 128-row strip live in one shared region aligned to 64 KB:
 // entry c of every row is the 256-byte line c of the region; within a line,
 // rows of warps 0/1 of the group use the low half-words and rows of warps 2/3
@@ -179,11 +199,34 @@ struct RowDequant<Q, false> {
 
   // ww[p]: one 32-column word of plane p -> 16 fp16 pairs (columns in order).
   __device__ __forceinline__ void word(const uint32_t (&ww)[Q], uint32_t (&out)[16]) const {
-    // row i of the bit matrix = index bit i = plane Q-1-i; missing bits are 0
     uint32_t X[8];
+    if constexpr (Q <= 5) {
+      // index bits 0-3 (planes Q-1 .. Q-4): after a 4x4 transpose inside every
+      // nibble, nibble e of L[js] holds them for column 8*js + e
+      uint32_t L[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) X[i] = i < Q ? ww[Q - 1 - i] : (i == 7 ? hi7 : 0u);
-    transpose8x8(X);
+      for (int c = 0; c < 4; ++c) L[c] = c < Q ? ww[Q - 1 - c] : 0u;
+      transpose4x4(L);
+      // index bits 4-7 as a nibble per column: plane 0 in bit 0 (Q = 5) and
+      // the region half in bit 3; spread the two nibbles into index bytes
+      const uint32_t h = hi7 & (Q <= 4 ? 0x80808080u : 0x88888888u);
+#pragma unroll
+      for (int js = 0; js < 4; ++js) {
+        if constexpr (Q <= 4) {
+          X[js] = (L[js] & 0x0F0F0F0Fu) | h;
+          X[4 + js] = (shr_mul(L[js], 4) & 0x0F0F0F0Fu) | h;
+        } else {
+          const uint32_t H = (shr_mul(ww[0], js) & 0x11111111u) | h;
+          X[js] = (L[js] & 0x0F0F0F0Fu) | (shl_mul(H, 4) & 0xF0F0F0F0u);
+          X[4 + js] = (shr_mul(L[js], 4) & 0x0F0F0F0Fu) | (H & 0xF0F0F0F0u);
+        }
+      }
+    } else {
+      // row i of the bit matrix = index bit i = plane Q-1-i; missing bits are 0
+#pragma unroll
+      for (int i = 0; i < 8; ++i) X[i] = i < Q ? ww[Q - 1 - i] : (i == 7 ? hi7 : 0u);
+      transpose8x8(X);
+    }
     // column 8*js + e now has its full index in byte e/2 of X[4*(e%2) + js]
 #pragma unroll
     for (int js = 0; js < 4; ++js) {
