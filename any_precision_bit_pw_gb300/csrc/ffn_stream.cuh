@@ -143,14 +143,11 @@ __device__ __forceinline__ bool wait_bar(const Sm sm, int i, uint32_t parity, co
 }
 
 // Bounded wait that ignores the abort flag (copies and MMAs already issued
-// must land before the CTA exits); running out of time is reported.
-__device__ __forceinline__ void drain_bar(const Params& p, const Sm sm, int i, uint32_t parity) {
+// must land before the CTA exits).
+__device__ __forceinline__ void drain_bar(const Sm sm, int i, uint32_t parity) {
   const uint64_t t0 = pw::global_ns();
   while (!pw::mbar_try_wait_hint(bar(sm, i), parity, kHintNs))
-    if (pw::global_ns() - t0 > 100000000ull) {
-      report(p.status, PW_ERR_TIMEOUT);
-      return;
-    }
+    if (pw::global_ns() - t0 > 100000000ull) return;
 }
 
 // Bounded wait until a shared counter reaches `target`.
@@ -335,7 +332,7 @@ __device__ __forceinline__ void plane_loader_role(const Params& p, const Sm sm) 
   // the last copies land before the CTA exits
   if (lane == 0)
     for (uint32_t y = c > static_cast<uint32_t>(kPS) ? c - kPS : 0u; y < c; ++y)
-      drain_bar(p, sm, kBarPFull + static_cast<int>(y % kPS), (y / kPS) & 1u);
+      drain_bar(sm, kBarPFull + static_cast<int>(y % kPS), (y / kPS) & 1u);
   __syncwarp();
 }
 
@@ -386,7 +383,7 @@ __device__ __forceinline__ void b_loader_role(const Params& p, const Sm sm, cons
     pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(u % kUS)));
   }
   for (uint32_t y = x > static_cast<uint32_t>(kBS) ? x - kBS : 0u; y < x; ++y)
-    drain_bar(p, sm, kBarBFull + static_cast<int>(y % kBS), (y / kBS) & 1u);
+    drain_bar(sm, kBarBFull + static_cast<int>(y % kBS), (y / kBS) & 1u);
 }
 
 // ---------------------------------------------------------------------------
@@ -450,7 +447,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t 
     pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(mu % kUS)));
   }
   // the last MMAs complete before the CTA exits
-  if (issued) drain_bar(p, sm, kBarTFree + static_cast<int>(last % kF), (last / kF) & 1u);
+  if (issued) drain_bar(sm, kBarTFree + static_cast<int>(last % kF), (last / kF) & 1u);
 }
 
 // ---------------------------------------------------------------------------
@@ -458,11 +455,10 @@ __device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t 
 // ---------------------------------------------------------------------------
 // Copies of the units' LUTs into the shared region go out in unit order, from
 // thread 0 of the epilogue warps; `next` is the first unit not copied yet and
-// `last[h]` the last unit whose barrier phase in half h was completed (a
-// copy, or a give-up arrival), drained at exit.
+// `last` the last one copied (drained at exit).
 struct LutCopies {
   uint32_t next = 0;
-  int last[2] = {-1, -1};
+  int last = -1;
 };
 
 // One bulk copy of unit i's table (its strip's run of 2^q lines) into region
@@ -498,11 +494,12 @@ __device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i
   if (etid == 0) {
     if (lc.next <= i) {
       const uint32_t need = static_cast<uint32_t>(kDeqWarpsAll) * ((u.q == 8 || prev_q8) ? i : (i >= 1 ? i - 1 : 0u));
-      if (wait_count(sm, &sm.st->deq_done, need, p))
+      if (wait_count(sm, &sm.st->deq_done, need, p)) {
         copy_lut(sm, i, u);
-      else
+        lc.last = static_cast<int>(i);
+      } else {
         pw::mbar_arrive(bar(sm, kBarRegReady + static_cast<int>(i & 1u)));   // giving up: complete the phase
-      lc.last[i & 1u] = static_cast<int>(i);
+      }
       lc.next = i + 1;
     }
     prev_q8 = u.q == 8;
@@ -523,7 +520,7 @@ __device__ __forceinline__ void lut_early(const Sm sm, uint32_t j, LutCopies& lc
   if (*reinterpret_cast<volatile uint32_t*>(&sm.st->deq_done) < static_cast<uint32_t>(kDeqWarpsAll) * (j - 1)) return;
   __threadfence_block();
   copy_lut(sm, j, u);
-  lc.last[j & 1u] = static_cast<int>(j);
+  lc.last = static_cast<int>(j);
   lc.next = j + 1;
 }
 
@@ -632,10 +629,8 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sm sm, uint
     if (next < 0) next = lut_fill(p, sm, i + 1, prev_q8, true, lc);
     more = next;
   }
-  // the last LUT copy into each half lands before the CTA exits (every
-  // earlier phase of a half completed before its last one)
-  for (int h = 0; h < 2; ++h)
-    if (lc.last[h] >= 0) drain_bar(p, sm, kBarRegReady + h, (static_cast<uint32_t>(lc.last[h]) >> 1) & 1u);
+  // the last LUT copy lands before the CTA exits
+  if (lc.last >= 0) drain_bar(sm, kBarRegReady + (lc.last & 1), (static_cast<uint32_t>(lc.last) >> 1) & 1u);
 }
 
 // ---------------------------------------------------------------------------
