@@ -1,8 +1,8 @@
 // Per-row any-precision dequantisation for the tcgen05 path.
 //
 // "PagedWeight" arXiv text, §1 / Figure 3 caption: a b-bit weight is the entry
-// of its row's bitwidth-specific LUT selected by the index formed from the top
-// b bit-planes.  Here each thread of the four dequant warps owns one output
+// of its row's LUT for bitwidth b at the index formed from the top b
+// bit-planes.  Here each thread of the four dequant warps owns one output
 // row (one TMEM lane) of a 128-row strip and turns 64 consecutive columns per
 // pipeline stage into 32 fp16 pairs for tcgen05.st:
 //

@@ -3,8 +3,8 @@
 //
 // "PagedWeight" arXiv text, §3.3 (Fused Mixed-Precision MoE Kernel): one
 // kernel follows the committed bitwidth of every gate_up and down
-// linear-block and does the expert activation, the down projection and the
-// output accumulation in one launch.
+// linear-block and runs the experts' gate_up with SiLU·mul, their down
+// projection and the weighted sum of their outputs in one launch.
 //
 // Scheduling: a persistent launch (one CTA per SM) whose CTAs take work units
 // from an atomic ticket counter.  Tickets are issued in order: every gate_up

@@ -341,8 +341,8 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
                       void* d_ws, size_t ws_bytes, uint16_t* d_y, int32_t* d_status,
                       const pw_ffn_options* opts, void* stream);
 
-/* Routing and the fused expert layer in one launch (§3.3: the kernel takes
- * routing, the per-expert computation and the output accumulation together).
+/* Routing and the fused expert layer in one launch (§3.3: routing belongs to
+ * the fused kernel together with the experts' work and the weighted sum).
  * Computes what pw_moe_route_topk followed by pw_moe_apl_ffn computes, with
  * the same results bit for bit:
  *  d_logits fp32 [T][E] router logits (input, finite values);

@@ -10,8 +10,8 @@ LLM Serving with Dynamic Quality-Aware Weight Quantization" (arXiv text):
 overlaid bit-planes with per-bitwidth lookup tables (§1 and the Figure 3
 caption), per-expert linear-blocks gate_up and down (§3.1), top-K routing and
 routing mass (§2.1, Eq. 1), released-memory accounting (§3.1, Eq. 3) and the
-fused layer's routing, expert activation, down projection and output
-accumulation (§3.3).  See ``oracle/apl.py``.
+fused layer: routing, the experts' gate_up with SiLU·mul, their down
+projection and the weighted sum of their outputs, all in one step (§3.3).  See ``oracle/apl.py``.
 
 Parity status per function (what pins it, see tests/test_oracle_pins.py):
   pack / unpack ............ pinned: overlay invariant, round trip, hand-derived layout points

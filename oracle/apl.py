@@ -155,8 +155,8 @@ def unpack_indices(planes: Sequence[np.ndarray], b: int, N: int, K: int,
 # Dequantisation and the any-precision linear map
 # ----------------------------------------------------------------------------
 def dequant(idx_b: np.ndarray, lut_b: np.ndarray, rows: Optional[Tuple[int, int]] = None) -> np.ndarray:
-    """W[n][j] = LUT_b[n][idx_b[n][j]] in float64 (Figure 3 caption: the LUT holds
-    the bitwidth-specific centroid values; one LUT row per output row)."""
+    """W[n][j] = LUT_b[n][idx_b[n][j]] in float64 (Figure 3 caption: each bitwidth
+    has its own table of centroids; one LUT row per output row)."""
     lut = np.asarray(lut_b).astype(np.float64)
     r0, r1 = rows if rows is not None else (0, lut.shape[0])
     return np.take_along_axis(lut[r0:r1], idx_b, axis=1)
@@ -270,7 +270,7 @@ def route_topk_shared(logits: np.ndarray, k: int, S: int) -> Dict[str, np.ndarra
 
 
 # ----------------------------------------------------------------------------
-# The MoE layer (§3.3: routing, expert activation, down projection, output accumulation)
+# The MoE layer (§3.3: routing, the routed experts' two projections and the weighted sum)
 # ----------------------------------------------------------------------------
 def silu(z: np.ndarray) -> np.ndarray:
     return z / (1.0 + np.exp(-z))
