@@ -182,11 +182,16 @@ __device__ __forceinline__ bool wait_unit(const Sm sm, uint32_t i, const Params&
 // dequant warps
 // ---------------------------------------------------------------------------
 // Plane chunks: the loader copies a unit's tiles in chunks of consecutive
-// tiles (4 for q <= 4, 2 for q >= 5; at most 32 KB), one bulk copy per plane,
-// into kPS fixed slots.  Slot layout: [plane][tile of the chunk][row pos][16 B],
-// plane stride chunk_tiles * 2 KB.  Every dequant warp waits for each chunk
-// and signals it consumed, whether or not its set has a tile in it.
-__host__ __device__ constexpr int chunk_tiles(int q) { return q <= 4 ? 4 : 2; }
+// tiles (4 for q <= 4, 3 for q = 5 in the 16-token kernel, else 2; at most 32
+// KB and at most one tile per dequant set), one bulk copy per plane, into kPS
+// fixed slots.  Slot layout: [plane][tile of the chunk][row pos][16 B], plane
+// stride chunk_tiles * 2 KB.  Every dequant warp waits for each chunk and
+// signals it consumed, whether or not its set has a tile in it.  (Three-tile
+// chunks at q = 5 keep 30 instead of 20 KB of a slot in flight: 4 % faster at
+// b = 5 with four slots; with the 64-token kernel's three slots they measured
+// 2 % slower.)
+__host__ __device__ constexpr int chunk_tiles(int q) { return q <= 4 ? 4 : (q == 5 && kN <= 16 ? 3 : 2); }
+static_assert(3 * 5 * 2048 <= kPSlotBytes, "chunk sizes");
 
 template <int Q>
 __device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, const Sm sm, uint32_t tmem, uint32_t x0,
