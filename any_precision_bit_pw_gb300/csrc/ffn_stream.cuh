@@ -16,12 +16,13 @@
 //     own double-buffered TMEM columns), committed to the tile's "free"
 //     barrier, which releases its TMEM slot and its B slot.  Several issuing
 //     warps are needed: one thread issues an N <= 128 MMA only every ~45 ns;
-//   4 epilogue warps: write each unit's LUT into a shared region one unit
-//     ahead (two halves used alternately), sum the issuers' accumulators of a
-//     unit and write h = silu(gate)*up, down-projection partial sums or the
-//     linear output; then publish the unit and run the deterministic combine
-//     of a finished strip (or, for large batches, the whole grid combines
-//     after the last unit);
+//   4 epilogue warps: copy each unit's LUT into a shared region one or two
+//     units ahead (two halves used alternately), sum the issuers'
+//     accumulators of a unit and write h = silu(gate)*up, down-projection
+//     partial sums or the linear output; then publish the unit.  After the
+//     last unit the whole grid runs the deterministic top-k combine (with
+//     PW_FFN_FLAG_STRIP_COMBINE, a strip's last down unit combines it
+//     instead);
 //   plane loader warp: per chunk of a unit's consecutive tiles, one bulk copy
 //     per plane (a run of tiles of one plane is contiguous) into a slot;
 //   scheduler (one thread): takes tickets and publishes units into four slots
