@@ -592,7 +592,7 @@ def oracle_sample(workload: str, experts_in_sample: int = 3, tokens=None) -> dic
                       + (f" and by {wl.layers} layers" if wl.layers > 1 else "")}
 
 
-def oracle_steps(workload: str, steps: int, budget_s: float = 100.0, tokens=None) -> dict:
+def oracle_steps(workload: str, steps: int, tokens=None) -> dict:
     """The reference arm's steps.  Set-up (routing, packing the first active
     expert's two blocks) runs once, and so does the oracle's own block path
     (apl_linear over both whole blocks for that expert's routed tokens; the
@@ -671,9 +671,11 @@ def reference_arm(args, rank, world):
         return None
     wl = get_workload(args.workload, args.tokens)
     cmd = _child_cmd(args.workload, args.tokens) + ["--steps", str(max(1, args.steps)), "--reference-child"]
-    d = json.loads(subprocess.run(cmd, env=dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1",
-                                                MKL_NUM_THREADS="1", CUDA_VISIBLE_DEVICES=""),
-                                  capture_output=True, text=True, timeout=900).stdout.strip().splitlines()[-1])
+    r = subprocess.run(cmd, env=dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
+                                     CUDA_VISIBLE_DEVICES=""), capture_output=True, text=True, timeout=900)
+    if r.returncode != 0:
+        raise RuntimeError("oracle child failed: " + r.stderr[-500:])
+    d = json.loads(r.stdout.strip().splitlines()[-1])
     times, sample = d["est_layer_s"], d["sample"]
     ms = 1e3 * float(np.mean(times))
     value = wl.tokens / (ms * 1e-3)

@@ -1,0 +1,67 @@
+"""Host-side checks of bench.py's contract that need no GPU: the reference
+arm (the oracle timed on host cores) prints the JSON line the contract asks
+for, and a committed ncu DRAM-traffic record is reported only while the
+kernel sources it was taken on are unchanged."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+
+import bench  # noqa: E402
+
+
+def test_reference_arm_line_on_the_tiny_layer():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--workload", "tiny",
+                        "--steps", "3", "--warmup", "1"], cwd=ROOT, env=env, capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0, r.stderr[-500:]
+    d = json.loads(r.stdout.strip().splitlines()[-1])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "scaling",
+                "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference" and d["steps"] == 3 and d["n_gpus"] == 1
+    assert d["config"]["workload"] == "tiny" and d["config"]["tokens"] == 16
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["value"] == pytest.approx(16 / (d["ms_per_step"] * 1e-3))
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"] and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_reference_steps_scale_one_strip_per_step():
+    d = bench.oracle_steps("tiny", 4)
+    assert len(d["est_layer_s"]) == 4
+    assert all(t > 0 for t in d["est_layer_s"])
+    assert "active experts" in d["sample"]
+
+
+def test_traffic_record_follows_the_kernel_sources(monkeypatch):
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        records = json.load(f)
+    kernel, recs = next(iter(records.items()))
+    rec = recs[0]
+    csrc = os.path.join(ROOT, "any_precision_bit_pw_gb300", "csrc")
+    current = bench.source_digest([os.path.join(csrc, name) for name in rec["source_files"]])
+    got = bench.measured_traffic(kernel, rec["workload"], rec["tokens"])
+    if current == rec["source_sha256"]:
+        assert got == float(rec["dram_bytes_per_launch"])
+    else:
+        assert got is None
+    # a source change (here: a different digest) voids the record
+    monkeypatch.setattr(bench, "source_digest", lambda paths: "0" * 64)
+    assert bench.measured_traffic(kernel, rec["workload"], rec["tokens"]) is None
+
+
+def test_source_digest_ignores_comments(tmp_path):
+    a, b = tmp_path / "a.cuh", tmp_path / "b.cuh"
+    a.write_text("int f(int x) {\n  return x + 1;  // one\n}\n")
+    b.write_text("/* header */\nint f(int x) {\n\n  return x + 1;\n}\n")
+    assert bench.source_digest([str(a)]) == bench.source_digest([str(b)])
+    b.write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.source_digest([str(a)]) != bench.source_digest([str(b)])
