@@ -720,7 +720,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       pw_route::route_block(p.logits, p.T, p.E - p.route_shared, p.k - p.route_shared, p.route_shared, p.ids_out,
                             const_cast<float*>(p.w),
                             const_cast<int32_t*>(p.offsets), const_cast<int32_t*>(p.perm),
-                            const_cast<int32_t*>(p.inv_perm), p.mass_accum, smem_raw + (sm.region - pw::smem_u32(smem_raw)));
+                            const_cast<int32_t*>(p.inv_perm), p.mass_accum, smem_raw + (sm.region - pw::smem_u32(smem_raw)),
+                            pw::kLutRegionBytes);
       __syncthreads();
       if (threadIdx.x == 0) {
         __threadfence();

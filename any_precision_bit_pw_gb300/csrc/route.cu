@@ -17,13 +17,16 @@ constexpr int kThreads = 1024;
 constexpr int kWarps = kThreads / 32;
 using pw_route::kMaxE;
 using pw_route::kMaxK;
+constexpr size_t kScratch = 47 * 1024;
+static_assert(pw_route::scratch_bytes(kMaxE, kWarps) <= kScratch, "routing scratch");
 
 __global__ void __launch_bounds__(kThreads) route_kernel(const float* __restrict__ logits, int T, int E, int k, int S,
                                                          int32_t* __restrict__ ids, float* __restrict__ w,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                                                          int32_t* __restrict__ inv_perm, float* __restrict__ mass_accum) {
-  __shared__ __align__(16) uint8_t scratch[pw_route::scratch_bytes(kMaxE, kWarps)];
-  pw_route::route_block(logits, T, E, k, S, ids, w, offsets, perm, inv_perm, mass_accum, scratch);
+  // the required part plus room for the weights of up to ~2900 assignments
+  __shared__ __align__(16) uint8_t scratch[kScratch];
+  pw_route::route_block(logits, T, E, k, S, ids, w, offsets, perm, inv_perm, mass_accum, scratch, kScratch);
 }
 
 }  // namespace

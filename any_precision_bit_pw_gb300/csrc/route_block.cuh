@@ -16,13 +16,17 @@ namespace pw_route {
 constexpr int kMaxE = 256;   // routed + shared experts
 constexpr int kMaxK = 16;    // slots per token: routed top-k + shared experts
 
-// Shared-memory scratch of route_block: 3*E ints plus nwarps*E ints.
+// Shared-memory scratch route_block needs at least: 3*E ints, nwarps*E ints
+// and E + 1 offsets.  With 2*T*K more floats it also keeps the weights (by
+// slot, then in position order) for the routing mass; else it reads them back
+// from w.
 __host__ __device__ constexpr size_t scratch_bytes(int E, int nwarps) {
-  return static_cast<size_t>(3 + nwarps) * static_cast<size_t>(E) * 4u;
+  return (static_cast<size_t>(3 + nwarps) * static_cast<size_t>(E) + static_cast<size_t>(E) + 1u) * 4u;
 }
 
 // Every thread of the CTA calls this (it synchronises the CTA).  blockDim.x is
-// a multiple of 32; `scratch` is shared memory of scratch_bytes(E + S, warps).
+// a multiple of 32; `scratch` is `scratch_cap` bytes of shared memory, at least
+// scratch_bytes(E + S, warps).
 // logits are [T][E] (routed experts).  Each token gets K = k + S slots: its
 // top-k routed experts, then the S shared experts E .. E+S-1 with weight 1
 // (experts every token passes through, added to the routed output).  Writes
@@ -33,7 +37,7 @@ __host__ __device__ constexpr size_t scratch_bytes(int E, int nwarps) {
 // CTA, so they must not alias the logits.
 __device__ inline void route_block(const float* __restrict__ logits, int T, int E, int k, int S, int32_t* ids,
                                    float* w, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
-                                   float* mass_accum, uint8_t* scratch) {
+                                   float* mass_accum, uint8_t* scratch, size_t scratch_cap) {
   const int K = k + S, ET = E + S;
   const int nthreads = static_cast<int>(blockDim.x), nwarps = nthreads >> 5;
   const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, warp = tid >> 5;
@@ -41,6 +45,10 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
   int* s_base = s_cnt + ET;
   int* s_chunk = s_base + ET;
   int* s_wcnt = s_chunk + ET;   // [nwarps][E + S]
+  int* s_off = s_wcnt + nwarps * ET;   // [E + S + 1] the offsets, for step 4
+  float* s_wslot = reinterpret_cast<float*>(s_off + ET + 1);   // [T * K] weights by slot
+  float* s_wpos = s_wslot + static_cast<long long>(T) * K;     // [T * K] weights in position order
+  const bool wpos_smem = scratch_bytes(ET, nwarps) + static_cast<size_t>(T) * K * 8u <= scratch_cap;
   for (int e = tid; e < ET; e += nthreads) s_cnt[e] = 0;
   __syncthreads();
 
@@ -110,6 +118,7 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
       const float wj = routed ? expf(lsel[j] - lsel[0]) / den : 1.0f;
       ids[static_cast<long long>(t) * K + j] = e;
       w[static_cast<long long>(t) * K + j] = wj;
+      if (wpos_smem) s_wslot[static_cast<long long>(t) * K + j] = wj;
       atomicAdd(&s_cnt[e], 1);
       keep[j] = e;
     }
@@ -122,17 +131,21 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
     for (int e = 0; e < ET; ++e) {
       offsets[e] = run;
       s_base[e] = run;
+      s_off[e] = run;
       run += s_cnt[e];
     }
     offsets[ET] = run;
+    s_off[ET] = run;
   }
   __syncthreads();
 
   // 3) stable placement, one token per thread per chunk: the rank of token t
   //    inside expert e is the number of earlier tokens that also chose e.
+  //    Only the warps that hold tokens of the chunk take part.
   for (int c0 = 0; c0 < T; c0 += nthreads) {
     const int t = c0 + tid;
     const bool valid = t < T;
+    const int nwa = (min(T - c0, nthreads) + 31) >> 5;
     int my[kMaxK];
     int rank[kMaxK];
 #pragma unroll
@@ -141,19 +154,23 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
       rank[j] = 0;
     }
     const unsigned lt_mask = (1u << lane) - 1u;
-    for (int e = 0; e < ET; ++e) {
-      int jj = -1;
+    if (warp < nwa) {
+      for (int e = 0; e < ET; ++e) {
+        bool mine = false;
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j)
-        if (my[j] == e) jj = j;
-      const unsigned ball = __ballot_sync(0xffffffffu, jj >= 0);
-      if (jj >= 0) rank[jj] = __popc(ball & lt_mask);
-      if (lane == 0) s_wcnt[warp * ET + e] = __popc(ball);
+        for (int j = 0; j < kMaxK; ++j) mine |= my[j] == e;   // a token picks an expert at most once
+        const unsigned ball = __ballot_sync(0xffffffffu, mine);
+        const int r = __popc(ball & lt_mask);
+#pragma unroll
+        for (int j = 0; j < kMaxK; ++j)
+          if (my[j] == e) rank[j] = r;
+        if (lane == 0) s_wcnt[warp * ET + e] = __popc(ball);
+      }
     }
     __syncthreads();
     for (int e = tid; e < ET; e += nthreads) {
       int run = 0;
-      for (int wi = 0; wi < nwarps; ++wi) {
+      for (int wi = 0; wi < nwa; ++wi) {
         const int v = s_wcnt[wi * ET + e];
         s_wcnt[wi * ET + e] = run;
         run += v;
@@ -170,6 +187,7 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
         const int slot = t * K + j;
         perm[pos] = slot;
         inv_perm[slot] = pos;
+        if (wpos_smem) s_wpos[pos] = s_wslot[slot];
       }
     }
     __syncthreads();
@@ -183,7 +201,7 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
   if (mass_accum) {
     for (int e = warp; e < ET; e += nwarps) {
       float acc = 0.f;
-      for (int pos = offsets[e] + lane; pos < offsets[e + 1]; pos += 32) acc += w[perm[pos]];
+      for (int pos = s_off[e] + lane; pos < s_off[e + 1]; pos += 32) acc += wpos_smem ? s_wpos[pos] : w[perm[pos]];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (lane == 0) atomicAdd(&mass_accum[e], acc);
