@@ -722,6 +722,8 @@ def main():
             print(json.dumps(line), flush=True)
         return
 
+    if not torch.cuda.is_available():
+        sys.exit("bench.py: the pw arm runs the CUDA library and needs a GPU (--impl reference times the CPU oracle)")
     # the CPU baseline runs in a child process started before this process touches the GPU
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

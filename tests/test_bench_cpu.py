@@ -65,3 +65,12 @@ def test_source_digest_ignores_comments(tmp_path):
     assert bench.source_digest([str(a)]) == bench.source_digest([str(b)])
     b.write_text("int f(int x) {\n  return x + 2;\n}\n")
     assert bench.source_digest([str(a)]) != bench.source_digest([str(b)])
+
+
+def test_pw_arm_without_a_gpu_fails_at_once():
+    env = dict(os.environ, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "3", "--warmup", "3"], cwd=ROOT,
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0
+    assert "needs a GPU" in r.stderr
+    assert not r.stdout.strip()
