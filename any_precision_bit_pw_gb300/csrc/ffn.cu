@@ -240,7 +240,9 @@ int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,
 // Entry point for callers that cannot allocate device memory.  Its scratch is
 // this fixed array; host code must not hand the array's name to a kernel (on
 // the host it is only a stand-in symbol), so the device address is looked up
-// once per device with cudaGetSymbolAddress and cached.
+// once per device with cudaGetSymbolAddress and cached for the life of the
+// process (a cudaDeviceReset makes the cached address stale; the header says
+// so).
 // ---------------------------------------------------------------------------
 namespace {
 

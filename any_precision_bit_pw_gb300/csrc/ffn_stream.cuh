@@ -144,11 +144,15 @@ __device__ __forceinline__ bool wait_bar(const Sm sm, int i, uint32_t parity, co
 }
 
 // Bounded wait that ignores the abort flag (copies and MMAs already issued
-// must land before the CTA exits).
-__device__ __forceinline__ void drain_bar(const Sm sm, int i, uint32_t parity) {
+// must land before the CTA exits).  Giving up (after 100 ms) is reported as
+// PW_ERR_TIMEOUT.
+__device__ __forceinline__ void drain_bar(const Sm sm, int i, uint32_t parity, int32_t* status) {
   const uint64_t t0 = pw::global_ns();
   while (!pw::mbar_try_wait_hint(bar(sm, i), parity, kHintNs))
-    if (pw::global_ns() - t0 > 100000000ull) return;
+    if (pw::global_ns() - t0 > 100000000ull) {
+      report(status, PW_ERR_TIMEOUT);
+      return;
+    }
 }
 
 // Bounded wait until a shared counter reaches `target`.
@@ -194,8 +198,11 @@ __device__ __forceinline__ bool wait_unit(const Sm sm, uint32_t i, const Params&
 __host__ __device__ constexpr int chunk_tiles(int q) { return q <= 4 ? 4 : (q == 5 && kN <= 16 ? 3 : 2); }
 static_assert(3 * 5 * 2048 <= kPSlotBytes, "chunk sizes");
 
+// Returns false when a wait gave up (the CTA aborts); a chunk the warp did
+// not see land is then never released, so no copy can be issued over one
+// still in flight.
 template <int Q>
-__device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, const Sm sm, uint32_t tmem, uint32_t x0,
+__device__ __forceinline__ bool dequant_unit(const Params& p, const Unit& u, const Sm sm, uint32_t tmem, uint32_t x0,
                                              uint32_t c0, uint32_t ui) {
   constexpr int kCt = chunk_tiles(Q);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -226,7 +233,8 @@ __device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, con
     const int j = static_cast<int>((static_cast<uint32_t>(set) - xs) & 3u);   // this set's tile in the chunk
     const bool has = ok && j < n_in;
     if (ok) ok = wait_bar(sm, kBarPFull + ps, (c / kPS) & 1u, p);
-    if (has && ok) {
+    if (!ok) return false;
+    if (has) {
       const uint32_t x = xs + static_cast<uint32_t>(j);
       if (x >= kSA && !wait_bar(sm, kBarTFree + static_cast<int>((x - kSA) % kF), ((x - kSA) / kF) & 1u, p))
         ok = false;
@@ -258,6 +266,7 @@ __device__ __forceinline__ void dequant_unit(const Params& p, const Unit& u, con
     __syncwarp();
     if (lane == 0) pw::mbar_arrive(bar(sm, kBarPFree + ps));   // this warp is done with the chunk
   }
+  return ok;
 }
 
 __device__ __forceinline__ void dequant_role(const Params& p, const Sm sm, uint32_t tmem) {
@@ -266,15 +275,20 @@ __device__ __forceinline__ void dequant_role(const Params& p, const Sm sm, uint3
     if (!wait_unit(sm, i, p)) break;
     const Unit& u = sm.st->units[i % kUS];
     if (u.kind == kNone) break;
+    bool ok;
     switch (u.q) {
-      case 2: dequant_unit<2>(p, u, sm, tmem, x, c, i); break;
-      case 3: dequant_unit<3>(p, u, sm, tmem, x, c, i); break;
-      case 4: dequant_unit<4>(p, u, sm, tmem, x, c, i); break;
-      case 5: dequant_unit<5>(p, u, sm, tmem, x, c, i); break;
-      case 6: dequant_unit<6>(p, u, sm, tmem, x, c, i); break;
-      case 7: dequant_unit<7>(p, u, sm, tmem, x, c, i); break;
-      default: dequant_unit<8>(p, u, sm, tmem, x, c, i); break;
+      case 2: ok = dequant_unit<2>(p, u, sm, tmem, x, c, i); break;
+      case 3: ok = dequant_unit<3>(p, u, sm, tmem, x, c, i); break;
+      case 4: ok = dequant_unit<4>(p, u, sm, tmem, x, c, i); break;
+      case 5: ok = dequant_unit<5>(p, u, sm, tmem, x, c, i); break;
+      case 6: ok = dequant_unit<6>(p, u, sm, tmem, x, c, i); break;
+      case 7: ok = dequant_unit<7>(p, u, sm, tmem, x, c, i); break;
+      default: ok = dequant_unit<8>(p, u, sm, tmem, x, c, i); break;
     }
+    // after an abort the warp stops: an unfinished unit is not counted, so
+    // no LUT copy is issued into a region half whose copy may still be
+    // in flight
+    if (!ok) break;
     const int nt = u.nst / 2, ct = chunk_tiles(u.q);
     x += static_cast<uint32_t>(nt);
     c += static_cast<uint32_t>((nt + ct - 1) / ct);
@@ -338,7 +352,7 @@ __device__ __forceinline__ void plane_loader_role(const Params& p, const Sm sm) 
   // the last copies land before the CTA exits
   if (lane == 0)
     for (uint32_t y = c > static_cast<uint32_t>(kPS) ? c - kPS : 0u; y < c; ++y)
-      drain_bar(sm, kBarPFull + static_cast<int>(y % kPS), (y / kPS) & 1u);
+      drain_bar(sm, kBarPFull + static_cast<int>(y % kPS), (y / kPS) & 1u, p.status);
   __syncwarp();
 }
 
@@ -389,7 +403,7 @@ __device__ __forceinline__ void b_loader_role(const Params& p, const Sm sm, cons
     pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(u % kUS)));
   }
   for (uint32_t y = x > static_cast<uint32_t>(kBS) ? x - kBS : 0u; y < x; ++y)
-    drain_bar(sm, kBarBFull + static_cast<int>(y % kBS), (y / kBS) & 1u);
+    drain_bar(sm, kBarBFull + static_cast<int>(y % kBS), (y / kBS) & 1u, p.status);
 }
 
 // ---------------------------------------------------------------------------
@@ -453,7 +467,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t 
     pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(mu % kUS)));
   }
   // the last MMAs complete before the CTA exits
-  if (issued) drain_bar(sm, kBarTFree + static_cast<int>(last % kF), (last / kF) & 1u);
+  if (issued) drain_bar(sm, kBarTFree + static_cast<int>(last % kF), (last / kF) & 1u, p.status);
 }
 
 // ---------------------------------------------------------------------------
@@ -465,6 +479,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t 
 struct LutCopies {
   uint32_t next = 0;
   int last = -1;
+  int last_h[2] = {-1, -1};   // the last copy into each region half
 };
 
 // One bulk copy of unit i's table (its strip's run of 2^q lines) into region
@@ -500,11 +515,11 @@ __device__ __forceinline__ int lut_fill(const Params& p, const Sm sm, uint32_t i
   if (etid == 0) {
     if (lc.next <= i) {
       const uint32_t need = static_cast<uint32_t>(kDeqWarpsAll) * ((u.q == 8 || prev_q8) ? i : (i >= 1 ? i - 1 : 0u));
-      if (wait_count(sm, &sm.st->deq_done, need, p)) {
+      // giving up (abort) issues nothing: a region half's phases complete
+      // only by copies, which the exit drain relies on
+      if (wait_count(sm, &sm.st->deq_done, need, p) && !*reinterpret_cast<volatile int*>(&sm.st->abort)) {
         copy_lut(sm, i, u);
-        lc.last = static_cast<int>(i);
-      } else {
-        pw::mbar_arrive(bar(sm, kBarRegReady + static_cast<int>(i & 1u)));   // giving up: complete the phase
+        lc.last = lc.last_h[i & 1u] = static_cast<int>(i);
       }
       lc.next = i + 1;
     }
@@ -526,7 +541,7 @@ __device__ __forceinline__ void lut_early(const Sm sm, uint32_t j, LutCopies& lc
   if (*reinterpret_cast<volatile uint32_t*>(&sm.st->deq_done) < static_cast<uint32_t>(kDeqWarpsAll) * (j - 1)) return;
   __threadfence_block();
   copy_lut(sm, j, u);
-  lc.last = static_cast<int>(j);
+  lc.last = lc.last_h[j & 1u] = static_cast<int>(j);
   lc.next = j + 1;
 }
 
@@ -635,8 +650,17 @@ __device__ __forceinline__ void epilogue_role(const Params& p, const Sm sm, uint
     if (next < 0) next = lut_fill(p, sm, i + 1, prev_q8, true, lc);
     more = next;
   }
-  // the last LUT copy lands before the CTA exits
-  if (lc.last >= 0) drain_bar(sm, kBarRegReady + (lc.last & 1), (static_cast<uint32_t>(lc.last) >> 1) & 1u);
+  // Every LUT copy lands before the CTA exits.  On the normal path the
+  // dequant warps waited for each copy before reading the unit's table, so
+  // only the last one can still be in flight here.  After an abort they stop
+  // consuming units: the last copy into either half may be pending.
+  if (sm.st->abort) {
+    for (int h = 0; h < 2; ++h)
+      if (lc.last_h[h] >= 0)
+        drain_bar(sm, kBarRegReady + h, (static_cast<uint32_t>(lc.last_h[h]) >> 1) & 1u, p.status);
+  } else if (lc.last >= 0) {
+    drain_bar(sm, kBarRegReady + (lc.last & 1), (static_cast<uint32_t>(lc.last) >> 1) & 1u, p.status);
+  }
 }
 
 // ---------------------------------------------------------------------------

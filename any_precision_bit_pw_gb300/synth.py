@@ -8,7 +8,7 @@ depends on the other.
 Shapes follow the Mixtral models named in "PagedWeight: Efficient MoE LLM
 Serving with Dynamic Quality-Aware Weight Quantization" (arXiv text, §4,
 Table 1: Mixtral-8x7B has 8 experts and top-2 routing); the value
-distributions follow the synthetic-workload recipe stated in the design doc:
+distributions are these:
 
 * parent indices are i.i.d. uniform on [0, 2^P);
 * every lookup table row is 2^b fp16 centroids drawn from N(0, 0.02^2) in fp32,

@@ -363,11 +363,7 @@ def gpu_arm(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
         "ms_per_step": total_ms / K, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f16", "data": "synthetic (seeded; bit-plane indices uniform, LUTs sorted N(0,0.02), x N(0,1))",
-        "config": {"workload": wl.name, "hidden": H, "intermediate": sh.intermediate, "experts": E,
-                   "shared_experts": sh.shared, "top_k": sh.top_k, "tokens": T, "parent_bits": wl.parent_bits,
-                   "seed_bits": wl.seed_bits,
-                   "committed_bits": li.bits, "parallelism": f"replicas x{world}",
-                   "l2": "no flush: the planes read per step (%.0f MB) exceed the 129 MB L2" % (mean_planes / 1e6)},
+        "config": line_config(wl, li.bits, world),
         "roofline": roofline,
         "roofline_hbm": hbm_roof if prefill else None,
         "e2e": {"value": wl.tokens / (e2e_ms * 1e-3), "unit": UNIT,
@@ -554,98 +550,82 @@ def sweep(args, dev, out_path):
 # ---------------------------------------------------------------------------
 # the reference arm / CPU baseline: the oracle on the host cores
 # ---------------------------------------------------------------------------
-def oracle_sample(workload: str, experts_in_sample: int = 3, tokens=None) -> dict:
-    """Time the oracle on a bounded sample of the workload: the layer output
-    contribution of the first ``experts_in_sample`` active experts (their
-    gate_up and down blocks read from the packed bit-planes at the committed
-    bitwidths, for the tokens routed to them).  Scaled to the full layer by
-    the number of active experts (every expert's blocks have the same shape)."""
-    from oracle import apl
-    wl = get_workload(workload, tokens)
+REF_BUDGET_S = 210.0    # the reference arm's warm-up + timed steps end within about this
+
+
+def line_config(wl, bits, world: int) -> dict:
+    """The ``config`` object of a single-layer bench line (both arms)."""
     sh = wl.shape
-    x = synth.activations(wl).numpy()
-    logits = synth.router_logits(wl).numpy()
-    r = apl.route_topk_shared(logits, sh.top_k, sh.shared)
-    active = [e for e in range(sh.total_experts) if r["offsets"][e + 1] > r["offsets"][e]]
-    sample = active[:experts_in_sample]
-    li = synth.layer_inputs(wl, experts=sample)
-    blocks = {}
-    for e in sample:
-        for u in (0, 1):
-            idx = li.idx[(e, u)].numpy()
-            N, K = idx.shape
-            blocks[(e, u)] = apl.Block(apl.pack_bitplanes(idx, wl.parent_bits),
-                                       {b: t.numpy() for b, t in li.luts[(e, u)].items()},
-                                       li.bits[2 * e + u], N, K)
-    ids = r["ids"]
-    mask = np.isin(ids, sample)
-    toks = sorted(set(np.nonzero(mask)[0].tolist()))
-    t0 = time.perf_counter()
-    ids_s = np.where(mask, ids, -1)
-    apl.moe_layer(x, ids_s, r["w"], sh.intermediate, lambda e, u: blocks[(e, u)], tokens=toks)
-    dt = time.perf_counter() - t0
-    est_layer_s = dt * len(active) / len(sample) * wl.layers
-    return {"sample_s": dt, "est_layer_s": est_layer_s, "tokens_per_s": wl.tokens / est_layer_s,
-            "sample": f"oracle layer contribution of {len(sample)} of {len(active)} active experts "
-                      f"({sh.intermediate * 2}x{sh.hidden} gate_up + {sh.hidden}x{sh.intermediate} down each, "
-                      f"read from packed bit-planes), scaled by {len(active)}/{len(sample)}"
-                      + (f" and by {wl.layers} layers" if wl.layers > 1 else "")}
+    return {"workload": wl.name, "hidden": sh.hidden, "intermediate": sh.intermediate, "experts": sh.experts,
+            "shared_experts": sh.shared, "top_k": sh.top_k, "tokens": wl.tokens, "parent_bits": wl.parent_bits,
+            "seed_bits": wl.seed_bits, "committed_bits": list(bits), "parallelism": f"replicas x{world}",
+            "l2": "no flush: each step streams the committed planes of the active experts, "
+                  "hundreds of MB, above the 129 MB L2"}
 
 
-def oracle_steps(workload: str, steps: int, tokens=None) -> dict:
-    """The reference arm's steps.  Set-up (routing, packing the first active
-    expert's two blocks) runs once, and so does the oracle's own block path
-    (apl_linear over both whole blocks for that expert's routed tokens; the
-    down block's input is a stand-in of h's shape), timed.  Each step then
-    times the same unpack, dequantisation and matmul on one 128-row strip of
-    one block (the two in turn), scaled to that block's measured whole-block
-    time, the expert's two blocks and the number of active experts.  A step
-    costs tens of milliseconds, so a thousand steps end within minutes."""
-    from oracle import apl
+def oracle_workers(workload: str, tokens=None):
+    """The oracle's layer on the host cores: one process per active expert,
+    each holding its expert's gate_up and down blocks as packed bit-planes at
+    the committed bitwidths (seeded CPU draws of the workload's
+    distributions)."""
+    from oracle import apl, parallel
     wl = get_workload(workload, tokens)
     sh = wl.shape
     x = synth.activations(wl).numpy()
     r = apl.route_topk_shared(synth.router_logits(wl).numpy(), sh.top_k, sh.shared)
-    active = [e for e in range(sh.total_experts) if r["offsets"][e + 1] > r["offsets"][e]]
-    e = active[0]
-    li = synth.layer_inputs(wl, experts=[e])
-    xe = x[np.nonzero((r["ids"] == e).any(axis=1))[0]].astype(np.float64)
-    blocks = []
-    for u in (0, 1):
-        idx = li.idx[(e, u)].numpy()
-        N, K = idx.shape
-        q = li.bits[2 * e + u]
-        inp = xe if u == 0 else np.ones((xe.shape[0], K))
-        blocks.append((apl.pack_bitplanes(idx, wl.parent_bits), li.luts[(e, u)][q].numpy(), q, N, K, inp))
+    active = sorted({int(e) for e in r["ids"].ravel()})
+    files = parallel.ExpertFiles()
+    for e in active:
+        for u in (0, 1):
+            q = synth.committed_bits(wl)[2 * e + u]
+            files.add(e, u, synth.parent_indices(wl, 0, e, u).numpy(), synth.lut(wl, 0, e, u, q).numpy(), q)
+    ew = parallel.ExpertWorkers(files, x, r["ids"], r["w"], sh.intermediate, wl.parent_bits)
+    return wl, files, ew
 
-    def strip_time(b):
-        """Seconds block b would take, from one whole 128-row strip (the
-        oracle unpacks by strip) scaled by the strip count."""
-        planes, lut, q, N, K, inp = blocks[b]
-        t0 = time.perf_counter()
-        W = apl.dequant(apl.unpack_indices(planes, q, N, K, (0, 128)), lut, (0, 128))
-        _ = inp @ W.T
-        return (time.perf_counter() - t0) * N / 128
 
-    # the oracle's own path (apl_linear over each whole block, 2048-row
-    # chunks) once, timed: a strip stays in cache and costs less per weight,
-    # so each step's strip is scaled to its block's measured whole-block cost
-    t_block = []
-    for planes, lut, q, N, K, inp in blocks:
-        t0 = time.perf_counter()
-        apl.apl_linear(planes, lut, q, N, K, inp)
-        t_block.append(time.perf_counter() - t0)
-    t_full = sum(t_block)
-    ratio = [t_block[b] / max(np.mean([strip_time(b) for _ in range(3)]), 1e-9) for b in range(2)]
-    est = []
-    for i in range(max(1, steps)):
-        b = i % 2          # one strip of one block per step, the two blocks in turn
-        est.append(strip_time(b) * ratio[b] * t_full / t_block[b] * len(active) * wl.layers)
-    return {"est_layer_s": est, "sample": f"the oracle's apl_linear on both blocks of 1 of {len(active)} active experts "
-            f"timed once ({t_full:.2f} s); each step times its unpack + dequant + matmul on one 128-row strip of one "
-            f"block (in turn), scaled to that block's measured whole-block time, the expert's two blocks and "
-            f"{len(active)} active experts"
-            + (f" and {wl.layers} layers" if wl.layers > 1 else "")}
+def _sample_text(wl, ew, frac: float) -> str:
+    part = "the whole layer" if frac >= 1.0 else f"the first {frac:.4f} of every block's rows of the layer"
+    per = "; one layer of the {} per step".format(wl.layers) if wl.layers > 1 else ""
+    return (f"{part}: {len(ew.experts)} active experts' gate_up ({2 * wl.shape.intermediate}x{wl.shape.hidden}) "
+            f"and down ({wl.shape.hidden}x{wl.shape.intermediate}) read from packed bit-planes, one process per "
+            f"expert on {ew.cores} host cores ({ew.threads_per_worker} BLAS threads each){per}")
+
+
+def oracle_baseline(workload: str, tokens=None, passes: int = 1) -> dict:
+    """CPU baseline: wall time of whole-layer oracle passes (one by default:
+    a pass of the 8x7B layer is about 20 s of CPU work); tokens/s of the job
+    step (a stack step is its layers one after another, so its time is the
+    layer's times the layer count)."""
+    wl, files, ew = oracle_workers(workload, tokens)
+    try:
+        times = [ew.step(1.0) for _ in range(passes)]
+    finally:
+        ew.close()
+        files.close()
+    layer_s = float(np.median(times))
+    return {"value": wl.tokens / (layer_s * wl.layers), "layer_s": layer_s, "pass_s": times, "cores": ew.cores,
+            "sample": _sample_text(wl, ew, 1.0) + (f"; median of {passes} passes" if passes > 1 else "; one pass")}
+
+
+def oracle_reference_steps(workload: str, steps: int, warmup: int, tokens=None) -> dict:
+    """The reference arm's steps: each step is a timed oracle pass over the
+    layer (every active expert at once, as in oracle_baseline), or, when K + W
+    whole-layer passes would not end within REF_BUDGET_S, over the same first
+    fraction of every block's rows.  A step processes that fraction of the
+    job step (one layer of a stack step), so the line's tokens/s is
+    T * fraction / step time."""
+    wl, files, ew = oracle_workers(workload, tokens)
+    try:
+        t_full = ew.step(1.0)
+        n = max(1, steps) + max(0, warmup)
+        frac = 1.0 if n * t_full <= REF_BUDGET_S else max(REF_BUDGET_S / (n * t_full), 1e-4)
+        for _ in range(max(0, warmup)):
+            ew.step(frac)
+        times = [ew.step(frac) for _ in range(max(1, steps))]
+    finally:
+        ew.close()
+        files.close()
+    return {"step_s": times, "frac": frac / wl.layers, "cores": ew.cores, "sample": _sample_text(wl, ew, frac)}
 
 
 def _child_cmd(workload: str, tokens=None) -> list:
@@ -653,37 +633,45 @@ def _child_cmd(workload: str, tokens=None) -> list:
     return cmd + ["--tokens", str(tokens)] if tokens else cmd
 
 
+def _child_env() -> dict:
+    return dict(os.environ, CUDA_VISIBLE_DEVICES="")
+
+
 def cpu_baseline(workload: str, tokens=None) -> dict:
-    """Run the oracle sample in a fresh single-threaded child process."""
-    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-               CUDA_VISIBLE_DEVICES="")
-    cmd = _child_cmd(workload, tokens)
-    r = subprocess.run(cmd, env=env, capture_output=True, text=True, timeout=600)
+    """The oracle's whole layer on the host cores, in a child process started
+    before this process touches the GPU."""
+    r = subprocess.run(_child_cmd(workload, tokens), env=_child_env(), capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
-        return {"value": None, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
+        return {"value": None, "unit": UNIT, "cores": None, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    return {"value": d["tokens_per_s"], "unit": UNIT, "cores": 1, "kind": "oracle", "sample": d["sample"],
-            "sample_s": d["sample_s"]}
+    return {"value": d["value"], "unit": UNIT, "cores": d["cores"], "kind": "oracle", "sample": d["sample"],
+            "layer_s": d["layer_s"]}
 
 
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
     wl = get_workload(args.workload, args.tokens)
-    cmd = _child_cmd(args.workload, args.tokens) + ["--steps", str(max(1, args.steps)), "--reference-child"]
-    r = subprocess.run(cmd, env=dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1",
-                                     CUDA_VISIBLE_DEVICES=""), capture_output=True, text=True, timeout=900)
+    cmd = _child_cmd(args.workload, args.tokens) + ["--steps", str(max(1, args.steps)), "--warmup",
+                                                    str(max(0, args.warmup)), "--reference-child"]
+    r = subprocess.run(cmd, env=_child_env(), capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
         raise RuntimeError("oracle child failed: " + r.stderr[-500:])
     d = json.loads(r.stdout.strip().splitlines()[-1])
-    times, sample = d["est_layer_s"], d["sample"]
-    ms = 1e3 * float(np.mean(times))
-    value = wl.tokens / (ms * 1e-3)
+    times = d["step_s"]
+    step_s = float(np.mean(times))
+    value = wl.tokens * d["frac"] / step_s
+    cfg = line_config(wl, synth.committed_bits(wl), world) if wl.layers == 1 else \
+        {"workload": wl.name, "layers": wl.layers, "hidden": wl.shape.hidden,
+         "intermediate": wl.shape.intermediate, "experts": wl.shape.experts, "top_k": wl.shape.top_k,
+         "tokens": wl.tokens, "parent_bits": wl.parent_bits, "seed_bits": wl.seed_bits,
+         "parallelism": f"replicas x{world}"}
     return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": len(times),
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
-            "config": {"workload": wl.name, "tokens": wl.tokens},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "warmup": args.warmup, "ms_per_step": 1e3 * step_s, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded CPU draws of the same distributions)",
+            "impl": "reference", "config": cfg,
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": d["cores"], "kind": "oracle",
+                             "sample": d["sample"], "fraction_of_job_step": d["frac"]},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -706,10 +694,10 @@ def main():
         args.warmup = 3
 
     if args.cpu_baseline_child and args.reference_child:
-        print(json.dumps(oracle_steps(args.workload, args.steps, tokens=args.tokens)))
+        print(json.dumps(oracle_reference_steps(args.workload, args.steps, args.warmup, tokens=args.tokens)))
         return
     if args.cpu_baseline_child:
-        print(json.dumps(oracle_sample(args.workload, tokens=args.tokens)))
+        print(json.dumps(oracle_baseline(args.workload, tokens=args.tokens)))
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))

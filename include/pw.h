@@ -296,14 +296,21 @@ int pw_moe_apl_ffn(const void* d_desc, int layer, const uint16_t* d_x, int T, in
  *
  * The scratch space lives in a fixed array inside libpw of
  * PW_NOALLOC_SCRATCH_BYTES (32 MiB), which every GPU that loads the library
- * holds until the process exits.  Calls whose workspace
- * (pw_moe_apl_ffn_workspace) exceeds it fail with PW_ERR_WORKSPACE before
- * anything is enqueued; for the Mixtral-8x7B shape that allows up to 141
- * tokens per call at top-2.  This entry point allocates nothing itself (no
+ * holds until the process exits.  A call is accepted when the workspace of
+ * the path it takes fits the array, else it fails with PW_ERR_WORKSPACE
+ * before anything is enqueued.  The decode path (below 48 assignments per
+ * expert on average) needs more workspace per token than the prefill path,
+ * so the accepted token counts are not one interval: for the Mixtral-8x7B
+ * shape at top-2 they are T <= 141 (decode path) and 192 <= T <= 315
+ * (prefill path).  pw_moe_apl_ffn_workspace returns the larger of the two
+ * paths' sizes, so workspace(T) <= PW_NOALLOC_SCRATCH_BYTES is a sufficient
+ * (not a necessary) check.  This entry point allocates nothing itself (no
  * cudaMalloc/cudaFree, no allocating library routine).
  *  - The first call on a device looks up the array's device address (a one-off
  *    set-up, once per device, with that device current); make that first call
- *    before any stream capture.
+ *    before any stream capture.  The address is kept for the life of the
+ *    process: after cudaDeviceReset on a device it is stale, and this entry
+ *    point must not be called on that device again.
  *  - All calls share the one array and it keeps the last call's contents:
  *    calls that overlap on the GPU (different streams without ordering, or
  *    concurrent host threads) race and give wrong results.  Serialise them.
@@ -384,7 +391,9 @@ int pw_unpack_indices(const pw_page_table* t, int block, int b, uint8_t* d_idx_o
 
 /* out[m][n] = sum_j W[n][j] * x[m][j], W = LUT_q[n][idx_q[n][j]] of `block`
  * at its committed bitwidth q (2..8): d_x fp16 [M][cols], d_out fp32
- * [M][rows], fp32 accumulation.  M >= 0. */
+ * [M][rows], fp32 accumulation.  M >= 0.  Its work-ticket counter is one
+ * array inside the library, zeroed by each call: calls that overlap on the
+ * GPU (different streams without ordering) race.  Serialise them. */
 int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,
                   float* d_out, void* stream);
 

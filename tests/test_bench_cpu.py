@@ -30,15 +30,29 @@ def test_reference_arm_line_on_the_tiny_layer():
     assert d["value"] > 0 and d["ms_per_step"] > 0
     assert d["value"] == pytest.approx(16 / (d["ms_per_step"] * 1e-3))
     cb = d["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] == 1 and cb["value"] == d["value"] and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["cores"] == len(os.sched_getaffinity(0)) and cb["value"] == d["value"]
+    assert "whole layer" in cb["sample"] and cb["fraction_of_job_step"] == 1.0
+    bits = d["config"]["committed_bits"]
+    assert len(bits) == 8 and set(d["config"]) >= {"workload", "tokens", "hidden", "intermediate", "experts",
+                                                     "top_k", "parent_bits", "seed_bits", "parallelism"}
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
-def test_reference_steps_scale_one_strip_per_step():
-    d = bench.oracle_steps("tiny", 4)
-    assert len(d["est_layer_s"]) == 4
-    assert all(t > 0 for t in d["est_layer_s"])
-    assert "active experts" in d["sample"]
+def test_reference_steps_are_timed_passes(monkeypatch):
+    d = bench.oracle_reference_steps("tiny", 4, 1)
+    assert len(d["step_s"]) == 4 and all(t > 0 for t in d["step_s"])
+    assert d["frac"] == 1.0 and "whole layer" in d["sample"]
+    # when K + W whole passes would not fit the budget, each step covers a
+    # fraction of every block's rows and says so
+    monkeypatch.setattr(bench, "REF_BUDGET_S", 1e-6)
+    d = bench.oracle_reference_steps("tiny", 2, 0)
+    assert 0 < d["frac"] < 1 and "first" in d["sample"]
+
+
+def test_cpu_baseline_is_a_whole_layer_pass():
+    d = bench.oracle_baseline("tiny", passes=1)
+    assert d["value"] > 0 and d["cores"] == len(os.sched_getaffinity(0))
+    assert d["value"] == pytest.approx(16 / d["layer_s"])
 
 
 def test_traffic_record_follows_the_kernel_sources(monkeypatch):

@@ -13,6 +13,7 @@ pytestmark = pytest.mark.gpu
 pw = pytest.importorskip("any_precision_bit_pw_gb300.pw")
 from any_precision_bit_pw_gb300 import synth  # noqa: E402
 from any_precision_bit_pw_gb300.layer import APLMoEStack, MoECall, load_layer  # noqa: E402
+from oracle import parallel as oracle_parallel  # noqa: E402
 
 REL_L2 = 2e-3
 MAX_ABS_OVER_RMS = 1e-2
@@ -239,7 +240,7 @@ def test_ffn_tiny_workload():
 def test_ffn_back_to_back_calls(bits, T):
     """Thirty back-to-back calls of one 8x7B-shaped layer on the decode path:
     every call completes (no wait runs out) and returns the same bits (the
-    combine order is fixed), and a sampled token matches the oracle."""
+    combine order is fixed), and every token matches the oracle."""
     wl = synth.MIXTRAL_8X7B_SWEEP.with_(fixed_bits=bits, tokens=T)
     li = synth.layer_inputs(wl, device=DEV)
     sh = wl.shape
@@ -258,9 +259,7 @@ def test_ffn_back_to_back_calls(bits, T):
             first = y.clone()
         else:
             assert torch.equal(y, first)
-    toks = _sample_tokens(li, 1, seed=bits * 100 + T)
-    y_ref, _ = _oracle_y(li, tokens=toks)
-    _assert_close(y_ref, first.float().cpu().numpy(), rows=toks)
+    _check_rows(li, first.float().cpu().numpy(), list(range(T)))
 
 
 def test_ffn_is_deterministic():
@@ -354,49 +353,70 @@ def test_ffn_bounded_wait_reports_timeout():
 
 
 # ---------------------------------------------------------------------------
-# full-size workloads, sampled outputs
+# full-size workloads: every token, or a token set covering every (expert,
+# slot) pair; the oracle runs one expert per host core
 # ---------------------------------------------------------------------------
-def _sample_tokens(li, n, seed=0):
-    T = li.x.shape[0]
-    rng = np.random.default_rng(seed)
-    return sorted(rng.choice(T, size=min(n, T), replace=False).tolist())
+def _oracle_rows(li, tokens):
+    """Oracle rows y[tokens] of the layer at its committed bitwidths, and the
+    oracle's routing."""
+    sh, P = li.wl.shape, li.wl.parent_bits
+    lg = li.logits.cpu().numpy()
+    r = apl.route_topk_shared(lg, sh.top_k, sh.shared) if sh.shared else apl.route_topk(lg, sh.top_k)
+    experts = sorted({int(e) for e in r["ids"][tokens].ravel()})
+    with oracle_parallel.ExpertFiles() as f:
+        for e in experts:
+            for u in (0, 1):
+                q = li.bits[2 * e + u]
+                f.add(e, u, li.idx[(e, u)].cpu().numpy(), li.luts[(e, u)][q].cpu().numpy(), q)
+        y = oracle_parallel.layer_rows(f, li.x.cpu().numpy(), r["ids"], r["w"], sh.intermediate, P, tokens)
+    return y, r
+
+
+def _check_rows(li, y, tokens):
+    """The GPU output rows `tokens` against the oracle; every (expert, slot)
+    pair the batch routes to must be among them."""
+    y_ref, r = _oracle_rows(li, tokens)
+    ids = r["ids"]
+    pairs_all = {(int(ids[t, j]), j) for t in range(ids.shape[0]) for j in range(ids.shape[1])}
+    pairs = {(int(ids[t, j]), j) for t in tokens for j in range(ids.shape[1])}
+    assert pairs == pairs_all
+    assert np.all(np.isfinite(y[tokens]))
+    _assert_close(y_ref, y[tokens])
+    return r
 
 
 def test_ffn_mixtral_8x7b_decode_mixed_bits():
+    """The 8x7B decode layer with per-block bitwidths on 3..8: every one of
+    the 32 tokens against the oracle."""
     wl = synth.MIXTRAL_8X7B_DECODE
     li = synth.layer_inputs(wl, device=DEV)
     y, status, call, _ = _run_gpu(li)
     assert status == 0
-    toks = _sample_tokens(li, 2)
-    y_ref, r = _oracle_y(li, tokens=toks)
+    r = _check_rows(li, y, list(range(wl.tokens)))
     assert np.array_equal(call.route.ids.cpu().numpy(), r["ids"])
     assert np.array_equal(call.route.perm.cpu().numpy(), r["perm"])
-    _assert_close(y_ref, y, rows=toks)
-    assert np.all(np.isfinite(y))
 
 
-@pytest.mark.parametrize("b,T", [(3, 1), (8, 256), (5, 64)])
+@pytest.mark.parametrize("b,T", [(3, 1), (8, 256), (5, 64), (4, 64), (6, 64), (3, 8)])
 def test_ffn_mixtral_8x7b_uniform_sweep_points(b, T):
+    """Uniform-bitwidth sweep points of the 8x7B layer, every token."""
     wl = synth.MIXTRAL_8X7B_SWEEP.with_(fixed_bits=b, tokens=T)
     li = synth.layer_inputs(wl, device=DEV, lut_bits=range(wl.seed_bits, b + 1))
     y, status, _, _ = _run_gpu(li)
     assert status == 0
-    toks = _sample_tokens(li, 1, seed=b)
-    y_ref, _ = _oracle_y(li, tokens=toks)
-    _assert_close(y_ref, y, rows=toks)
+    _check_rows(li, y, list(range(T)))
 
 
 def test_ffn_mixtral_8x22b_prefill():
     """The 8x22B-shaped prefill layer: 4096 tokens, Zipf-skewed routing, hot
-    experts at 8 bits and the rest at 3-4 bits (64-token tiles)."""
+    experts at 8 bits and the rest at 3-4 bits (64-token tiles): tokens
+    covering every (expert, slot) pair plus 40 random ones."""
     wl = synth.MIXTRAL_8X22B_PREFILL
     li = synth.layer_inputs(wl, device=DEV)
     y, status, call, _ = _run_gpu(li)
     assert status == 0
     r_ids = call.route.ids.cpu().numpy()
-    toks = _sample_tokens(li, 2, seed=7)
-    y_ref, r = _oracle_y(li, tokens=toks)
+    toks = oracle_parallel.covering_tokens(r_ids, extra=40, seed=7)
+    r = _check_rows(li, y, toks)
     assert np.array_equal(r_ids, r["ids"])
     assert np.array_equal(call.route.perm.cpu().numpy(), r["perm"])
-    _assert_close(y_ref, y, rows=toks)
-    assert np.all(np.isfinite(y))

@@ -13,6 +13,7 @@ pytestmark = pytest.mark.gpu
 pw = pytest.importorskip("any_precision_bit_pw_gb300.pw")
 from any_precision_bit_pw_gb300 import synth  # noqa: E402
 from any_precision_bit_pw_gb300.layer import APLMoEStack, MoECall, load_layer  # noqa: E402
+from oracle import parallel as oracle_parallel  # noqa: E402
 
 DEV = "cuda"
 
@@ -36,6 +37,23 @@ def _stack(li):
     load_layer(st, 0, li)
     st.sync()
     return st
+
+
+def _oracle_rows(li, tokens):
+    """Oracle rows y[tokens] at the committed bitwidths (one expert per host
+    core) and the oracle's routing."""
+    sh = li.wl.shape
+    lg = li.logits.cpu().numpy()
+    r = apl.route_topk_shared(lg, sh.top_k, sh.shared) if sh.shared else apl.route_topk(lg, sh.top_k)
+    experts = sorted({int(e) for e in r["ids"][tokens].ravel()})
+    with oracle_parallel.ExpertFiles() as f:
+        for e in experts:
+            for u in (0, 1):
+                q = li.bits[2 * e + u]
+                f.add(e, u, li.idx[(e, u)].cpu().numpy(), li.luts[(e, u)][q].cpu().numpy(), q)
+        y = oracle_parallel.layer_rows(f, li.x.cpu().numpy(), r["ids"], r["w"], sh.intermediate,
+                                       li.wl.parent_bits, tokens)
+    return y, r
 
 
 def _routing(call):
@@ -84,16 +102,10 @@ def test_routed_call_matches_oracle_8x7b_decode():
     y = call(0, li.x, li.logits).float().cpu().numpy()
     torch.cuda.synchronize()
     assert int(call.status.item()) == 0
-    sh = li.wl.shape
-    toks = [0, 17]
-    r = apl.route_topk(li.logits.cpu().numpy(), sh.top_k)
-
-    def blocks(e, u):
-        idx = li.idx[(e, u)].cpu().numpy()
-        return apl.IndexBlock(idx, {b: t.cpu().numpy() for b, t in li.luts[(e, u)].items()}, li.bits[2 * e + u],
-                              li.wl.parent_bits)
-    y_ref = apl.moe_layer(li.x.cpu().numpy(), r["ids"], r["w"], sh.intermediate, blocks, tokens=toks)
-    m = apl.compare(y_ref[toks], y[toks])
+    toks = list(range(li.x.shape[0]))     # every token
+    y_ref, r = _oracle_rows(li, toks)
+    assert np.array_equal(call.route.ids.cpu().numpy(), r["ids"])
+    m = apl.compare(y_ref, y[toks])
     assert m["rel_l2"] <= 2e-3 and m["max_abs_over_rms"] <= 1e-2, m
 
 
@@ -140,7 +152,7 @@ def test_route_shared_matches_oracle(T, E, k, S):
 @pytest.mark.parametrize("name", ["qwen15moe_decode_mixed", "gemma4like_decode_mixed"])
 def test_shared_expert_layers(name):
     """The Qwen- and Gemma-shaped decode layers: routed call == two-launch call
-    bit for bit, and sampled tokens against the oracle."""
+    bit for bit, and every token against the oracle."""
     wl = synth.WORKLOADS[name]
     li = synth.layer_inputs(wl, device=DEV)
     st = _stack(li)
@@ -153,16 +165,10 @@ def test_shared_expert_layers(name):
     for a, b in zip(_routing(fused), _routing(split)):
         assert np.array_equal(a, b)
     assert torch.equal(yf, ys)
-    r = apl.route_topk_shared(li.logits.cpu().numpy(), sh.top_k, sh.shared)
+    toks = list(range(wl.tokens))          # every token, so every routed and shared expert
+    y_ref, r = _oracle_rows(li, toks)
     assert np.array_equal(_routing(fused)[0], r["ids"])
-    toks = [1, 22]
-
-    def blocks(e, u):
-        idx = li.idx[(e, u)].cpu().numpy()
-        return apl.IndexBlock(idx, {b: t.cpu().numpy() for b, t in li.luts[(e, u)].items()}, li.bits[2 * e + u],
-                              wl.parent_bits)
-    y_ref = apl.moe_layer(li.x.cpu().numpy(), r["ids"], r["w"], sh.intermediate, blocks, tokens=toks)
-    m = apl.compare(y_ref[toks], yf.float().cpu().numpy()[toks])
+    m = apl.compare(y_ref, yf.float().cpu().numpy()[toks])
     assert m["rel_l2"] <= 2e-3 and m["max_abs_over_rms"] <= 1e-2, m
 
 

@@ -147,8 +147,8 @@ def test_page_table_argument_errors(L):
 
 def test_workspace_and_host_validation(L):
     assert pw.pw_moe_apl_ffn_workspace(32, 4096, 14336, 8, 2) > 32 * 2 * 14336 * 2
-    assert pw.pw_moe_apl_ffn_workspace(32, 4000, 14336, 8, 2) == 0       # H % 256
-    assert pw.pw_moe_apl_ffn_workspace(32, 4096, 14336, 8, 9) == 0       # k > 8
+    assert pw.pw_moe_apl_ffn_workspace(32, 4000, 14336, 8, 2) == 0       # H not a multiple of 128
+    assert pw.pw_moe_apl_ffn_workspace(32, 4096, 14336, 8, 9) == 0       # k > E
     # argument errors are caught on the host before any CUDA call
     rc = L.pw_moe_route_topk(None, 4, 0, 1, None, None, None, None, None, None, None)
     assert rc == pw.PW_ERR_UNSUPPORTED
@@ -200,3 +200,19 @@ def test_page_movement_host_checks(L):
         assert pw.pw_page_table_take_released(t, 0) == 0
     finally:
         pw.pw_page_table_destroy(t)
+
+
+def test_noalloc_accepts_exactly_the_sizes_whose_path_fits(L):
+    """pw_moe_apl_ffn_noalloc takes a call when the workspace of the path the
+    call runs on fits its fixed array.  For the Mixtral-8x7B shape at top-2
+    the decode path (below 48 assignments per expert) fits up to 141 tokens,
+    the prefill path from 192 up to 315 tokens; the size check comes before
+    anything else that needs a GPU, so the rejections are seen here."""
+    def rc(T):
+        return L.pw_moe_apl_ffn_noalloc(None, 0, None, T, 4096, 14336, 8, 2, None, None, None, None, None,
+                                        None, None, None)
+    for T in (1, 32, 141, 192, 315):
+        assert rc(T) != pw.PW_ERR_WORKSPACE, T
+    for T in (142, 191, 316, 4096):
+        assert rc(T) == pw.PW_ERR_WORKSPACE, T
+        assert "scratch" in pw.pw_last_error()
