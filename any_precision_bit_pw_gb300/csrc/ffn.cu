@@ -87,9 +87,11 @@ namespace {
 // Shared by the fused entry points: checks, workspace layout, path choice and
 // launch.  `routed`: the routing arrays are outputs, computed from d_logits in
 // the same launch on the decode path and by a routing launch just before on
-// the prefill path.
-int ffn_launch(bool routed, const void* d_desc, int layer, const uint16_t* d_x, const float* d_logits, int T, int H,
-               int I, int E, int k, int32_t* d_ids, const float* d_w, const int32_t* d_offsets,
+// the prefill path.  `L` > 1 (routed only): L consecutive independent layers
+// starting at `layer`, each with T tokens and E routed experts, run as one
+// layer of L*T tokens and L*(E+S) experts whose routing never crosses layers.
+int ffn_launch(bool routed, const void* d_desc, int layer, int L, const uint16_t* d_x, const float* d_logits, int T,
+               int H, int I, int E, int k, int32_t* d_ids, const float* d_w, const int32_t* d_offsets,
                const int32_t* d_perm, const int32_t* d_inv_perm, float* d_mass_accum, void* d_ws, size_t ws_bytes,
                uint16_t* d_y, int32_t* d_status, const pw_ffn_options* opts, void* stream) {
   // routed call: E and k count routed experts; the options add S shared
@@ -97,19 +99,27 @@ int ffn_launch(bool routed, const void* d_desc, int layer, const uint16_t* d_x, 
   // runs over E + S experts and k + S slots per token
   const int S = (routed && opts) ? opts->shared_experts : 0;
   if (S < 0) return pw::set_error(PW_ERR_INVALID_ARG, "ffn: shared_experts %d", S);
+  if (L < 1 || L > kMaxE || (L > 1 && !routed)) return pw::set_error(PW_ERR_INVALID_ARG, "ffn: layers %d", L);
   const int ER = E, kR = k;
   E += S;
   k += S;
   if (int e = validate_shape(T, H, I, E, k)) return e;
+  if (static_cast<long long>(L) * E > kMaxE)
+    return pw::set_error(PW_ERR_UNSUPPORTED, "ffn: %d layers x %d experts exceed %d", L, E, kMaxE);
+  if (int e = validate_shape(L * T, H, I, L * E, k)) return e;
   if (layer < 0) return pw::set_error(PW_ERR_INVALID_ARG, "ffn: layer %d", layer);
   if (routed && T > 0 && !d_logits) return pw::set_error(PW_ERR_INVALID_ARG, "routed ffn: NULL logits");
   if (routed && (!d_ids || !d_offsets))
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: routed call needs ids and offsets");
   if (T == 0)
-    return routed ? pw_moe_route_topk_shared(d_logits, 0, ER, kR, S, d_ids, const_cast<float*>(d_w),
-                                             const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
-                                             const_cast<int32_t*>(d_inv_perm), d_mass_accum, stream)
+    return routed ? pw::route_layers(d_logits, L, 0, ER, kR, S, d_ids, const_cast<float*>(d_w),
+                                     const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
+                                     const_cast<int32_t*>(d_inv_perm), d_mass_accum, pw::as_stream(stream))
                   : PW_OK;
+  // the L layers as one: every count below is the total over the layers
+  const int E1 = E, T1 = T;
+  E *= L;
+  T *= L;
   if (!d_desc || !d_x || !d_w || !d_offsets || !d_perm || !d_inv_perm || !d_y || !d_status || !d_ws)
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: NULL argument");
   if ((reinterpret_cast<uintptr_t>(d_desc) & 15) || (reinterpret_cast<uintptr_t>(d_x) & 15) ||
@@ -118,14 +128,14 @@ int ffn_launch(bool routed, const void* d_desc, int layer, const uint16_t* d_x, 
   pw_ffn_options o{};
   if (opts) o = *opts;
   const int path = choose_path(T, E, k, o.path);
-  const WsLayout L = ws_layout(T, H, I, E, k, path);
-  if (ws_bytes < L.total || (reinterpret_cast<uintptr_t>(d_ws) & 255))
-    return pw::set_error(PW_ERR_WORKSPACE, "ffn: workspace needs %zu bytes, 256-byte aligned (got %zu)", L.total,
+  const WsLayout W = ws_layout(T, H, I, E, k, path);
+  if (ws_bytes < W.total || (reinterpret_cast<uintptr_t>(d_ws) & 255))
+    return pw::set_error(PW_ERR_WORKSPACE, "ffn: workspace needs %zu bytes, 256-byte aligned (got %zu)", W.total,
                          ws_bytes);
   cudaStream_t s = pw::as_stream(stream);
   char* ws = static_cast<char*>(d_ws);
   Params p{};
-  p.desc = static_cast<const BlockDesc*>(d_desc) + static_cast<long long>(layer) * E * 2;
+  p.desc = static_cast<const BlockDesc*>(d_desc) + static_cast<long long>(layer) * E1 * 2;
   p.x = d_x;
   p.y = d_y;
   p.w = d_w;
@@ -138,13 +148,13 @@ int ffn_launch(bool routed, const void* d_desc, int layer, const uint16_t* d_x, 
   p.E = E;
   p.k = k;
   p.A = T * k;
-  p.nsplit = L.nsplit;
-  p.split_cols = L.split_cols;
-  p.ctr = reinterpret_cast<uint32_t*>(ws + L.ctr);
-  p.h = reinterpret_cast<uint16_t*>(ws + L.h);
-  p.part = reinterpret_cast<float*>(ws + L.part);
-  p.xp = reinterpret_cast<uint16_t*>(ws + L.xp);
-  p.gather_ctr = reinterpret_cast<uint32_t*>(ws + L.gather);
+  p.nsplit = W.nsplit;
+  p.split_cols = W.split_cols;
+  p.ctr = reinterpret_cast<uint32_t*>(ws + W.ctr);
+  p.h = reinterpret_cast<uint16_t*>(ws + W.h);
+  p.part = reinterpret_cast<float*>(ws + W.part);
+  p.xp = reinterpret_cast<uint16_t*>(ws + W.xp);
+  p.gather_ctr = reinterpret_cast<uint32_t*>(ws + W.gather);
   // the whole grid combines after the last unit (measured faster than each
   // strip's last down unit combining it, by up to 8 % at 128 tokens)
   p.grid_combine = (o.flags & PW_FFN_FLAG_STRIP_COMBINE) ? 0 : 1;
@@ -155,17 +165,18 @@ int ffn_launch(bool routed, const void* d_desc, int layer, const uint16_t* d_x, 
   if (routed && path == PW_PATH_PREFILL) {
     // large batches: one CTA would route while the grid waits; a separate
     // routing launch comes first instead
-    if (int e = pw_moe_route_topk_shared(d_logits, T, ER, kR, S, d_ids, const_cast<float*>(d_w),
-                                         const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
-                                         const_cast<int32_t*>(d_inv_perm), d_mass_accum, stream))
+    if (int e = pw::route_layers(d_logits, L, T1, ER, kR, S, d_ids, const_cast<float*>(d_w),
+                                 const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
+                                 const_cast<int32_t*>(d_inv_perm), d_mass_accum, s))
       return e;
   } else if (routed) {
     p.logits = d_logits;
     p.route_shared = S;
+    p.route_layers = L;
     p.ids_out = d_ids;
     p.mass_accum = d_mass_accum;
   }
-  PW_CUDA_TRY(cudaMemsetAsync(p.ctr, 0, L.h - L.ctr, s));
+  PW_CUDA_TRY(cudaMemsetAsync(p.ctr, 0, W.h - W.ctr, s));
   return tile_width(T, E, k) == 16 ? pw_ffn::launch_ffn_t16(p, s) : pw_ffn::launch_ffn_t64(p, s);
 }
 
@@ -178,15 +189,24 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
                       const int32_t* d_inv_perm, void* d_ws, size_t ws_bytes, uint16_t* d_y, int32_t* d_status,
                       const pw_ffn_options* opts, void* stream) {
   (void)d_ids;
-  return ffn_launch(false, d_desc, layer, d_x, nullptr, T, H, I, E, k, nullptr, d_w, d_offsets, d_perm, d_inv_perm,
-                    nullptr, d_ws, ws_bytes, d_y, d_status, opts, stream);
+  return ffn_launch(false, d_desc, layer, 1, d_x, nullptr, T, H, I, E, k, nullptr, d_w, d_offsets, d_perm,
+                    d_inv_perm, nullptr, d_ws, ws_bytes, d_y, d_status, opts, stream);
 }
 
 int pw_moe_route_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, const float* d_logits, int T, int H,
                             int I, int E, int k, int32_t* d_ids, float* d_w, int32_t* d_offsets, int32_t* d_perm,
                             int32_t* d_inv_perm, float* d_mass_accum, void* d_ws, size_t ws_bytes, uint16_t* d_y,
                             int32_t* d_status, const pw_ffn_options* opts, void* stream) {
-  return ffn_launch(true, d_desc, layer, d_x, d_logits, T, H, I, E, k, d_ids, d_w, d_offsets, d_perm, d_inv_perm,
+  return ffn_launch(true, d_desc, layer, 1, d_x, d_logits, T, H, I, E, k, d_ids, d_w, d_offsets, d_perm, d_inv_perm,
+                    d_mass_accum, d_ws, ws_bytes, d_y, d_status, opts, stream);
+}
+
+int pw_moe_route_apl_ffn_layers(const void* d_desc, int layer0, int L, const uint16_t* d_x, const float* d_logits,
+                                int T, int H, int I, int E, int k, int32_t* d_ids, float* d_w, int32_t* d_offsets,
+                                int32_t* d_perm, int32_t* d_inv_perm, float* d_mass_accum, void* d_ws,
+                                size_t ws_bytes, uint16_t* d_y, int32_t* d_status, const pw_ffn_options* opts,
+                                void* stream) {
+  return ffn_launch(true, d_desc, layer0, L, d_x, d_logits, T, H, I, E, k, d_ids, d_w, d_offsets, d_perm, d_inv_perm,
                     d_mass_accum, d_ws, ws_bytes, d_y, d_status, opts, stream);
 }
 

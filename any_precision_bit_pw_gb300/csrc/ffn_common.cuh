@@ -73,7 +73,9 @@ struct Params {
   const float* logits;
   int32_t* ids_out;
   float* mass_accum;
-  int route_shared;        // shared experts: the last route_shared of E, the last of k slots
+  int route_shared;        // shared experts: the last route_shared of each layer's experts, the last of k slots
+  int route_layers;        // routed call over this many independent layers (T and E are the totals: each
+                           // layer has T / route_layers tokens and E / route_layers experts)
   int32_t* status;
   uint64_t wait_ns;
   uint32_t flags;

@@ -735,27 +735,34 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   DecState& st = *sm.st;
-  // routed call: CTA 0 routes the batch (the LUT region is its scratch: the
-  // pipeline has not started) and publishes the routing arrays; every CTA
-  // waits for them before it schedules or gathers (all CTAs are resident:
-  // one per SM)
+  // routed call: CTA l routes layer l of the route_layers layers (one layer:
+  // CTA 0 routes the batch; the LUT region is the scratch: the pipeline has
+  // not started), writing the routing arrays of all layers in one
+  // concatenated index space, and counts the layer as published; every CTA
+  // waits for all of them before it schedules or gathers (all CTAs are
+  // resident: one per SM)
   if (p.logits) {
-    if (blockIdx.x == 0) {
-      pw_route::route_block(p.logits, p.T, p.E - p.route_shared, p.k - p.route_shared, p.route_shared, p.ids_out,
-                            const_cast<float*>(p.w),
-                            const_cast<int32_t*>(p.offsets), const_cast<int32_t*>(p.perm),
-                            const_cast<int32_t*>(p.inv_perm), p.mass_accum, smem_raw + (sm.region - pw::smem_u32(smem_raw)),
-                            pw::kLutRegionBytes);
+    const int L = p.route_layers, S = p.route_shared;
+    const int Tl = p.T / L, ETl = p.E / L;
+    const long long Al = static_cast<long long>(Tl) * p.k;
+    for (int l = blockIdx.x; l < L; l += gridDim.x) {
+      pw_route::route_block(p.logits + static_cast<long long>(l) * Tl * (ETl - S), Tl, ETl - S, p.k - S, S,
+                            p.ids_out + l * Al, const_cast<float*>(p.w) + l * Al,
+                            const_cast<int32_t*>(p.offsets) + static_cast<long long>(l) * ETl,
+                            const_cast<int32_t*>(p.perm) + l * Al, const_cast<int32_t*>(p.inv_perm) + l * Al,
+                            p.mass_accum ? p.mass_accum + static_cast<long long>(l) * ETl : nullptr,
+                            smem_raw + (sm.region - pw::smem_u32(smem_raw)), pw::kLutRegionBytes,
+                            static_cast<int>(l * Al));
       __syncthreads();
       if (threadIdx.x == 0) {
         __threadfence();
-        pw::st_release_gpu(p.gather_ctr + 2, 1u);
+        atomicAdd(p.gather_ctr + 2, 1u);
       }
     }
     if (threadIdx.x == 0) {
       int ok = 1;
       const uint64_t t0 = pw::global_ns();
-      while (pw::ld_acquire_gpu(p.gather_ctr + 2) == 0u) {
+      while (pw::ld_acquire_gpu(p.gather_ctr + 2) < static_cast<uint32_t>(L)) {
         if (pw::global_ns() - t0 > p.wait_ns) {
           report(p.status, PW_ERR_TIMEOUT);
           ok = 0;

@@ -39,6 +39,13 @@ int cuda_error(cudaError_t e, const char* what);
 
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
+// Routing of L independent layers in one launch (route.cu): the arrays of
+// layer l start at l*T*E (logits), l*T*(k+S) (ids, w, perm, inv_perm),
+// l*(E+S) (offsets, mass); offsets, perm and inv_perm hold indices into the
+// concatenated assignments of all layers.  Arguments are not checked.
+int route_layers(const float* d_logits, int L, int T, int E, int k, int S, int32_t* d_ids, float* d_w,
+                 int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm, float* d_mass_accum, cudaStream_t s);
+
 // Host-side descriptor of `block` of a page table, at its committed bitwidth
 // (or at `bits_override` if > 0); fails unless the planes are attached.
 int table_block(const pw_page_table* t, int block, BlockDesc* out, int bits_override);

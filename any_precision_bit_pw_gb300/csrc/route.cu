@@ -20,16 +20,35 @@ using pw_route::kMaxK;
 constexpr size_t kScratch = 47 * 1024;
 static_assert(pw_route::scratch_bytes(kMaxE, kWarps) <= kScratch, "routing scratch");
 
+// CTA l routes layer l of a batch of independent layers whose arrays are
+// concatenated layer after layer (one layer: a grid of one CTA).
 __global__ void __launch_bounds__(kThreads) route_kernel(const float* __restrict__ logits, int T, int E, int k, int S,
                                                          int32_t* __restrict__ ids, float* __restrict__ w,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                                                          int32_t* __restrict__ inv_perm, float* __restrict__ mass_accum) {
   // the required part plus room for the weights of up to ~2900 assignments
   __shared__ __align__(16) uint8_t scratch[kScratch];
-  pw_route::route_block(logits, T, E, k, S, ids, w, offsets, perm, inv_perm, mass_accum, scratch, kScratch);
+  const long long l = blockIdx.x, A = static_cast<long long>(T) * (k + S);
+  pw_route::route_block(logits + l * T * E, T, E, k, S, ids + l * A, w + l * A, offsets + l * (E + S), perm + l * A,
+                        inv_perm + l * A, mass_accum ? mass_accum + l * (E + S) : nullptr, scratch, kScratch,
+                        static_cast<int>(l * A));
 }
 
 }  // namespace
+
+namespace pw {
+
+// Routing of L independent layers in one launch (CTA l: layer l), with the
+// offsets, permutation and inverse permutation in the concatenated index
+// space of the layers' assignments.
+int route_layers(const float* d_logits, int L, int T, int E, int k, int S, int32_t* d_ids, float* d_w,
+                 int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm, float* d_mass_accum, cudaStream_t s) {
+  route_kernel<<<L, kThreads, 0, s>>>(d_logits, T, E, k, S, d_ids, d_w, d_offsets, d_perm, d_inv_perm, d_mass_accum);
+  PW_CUDA_TRY(cudaGetLastError());
+  return PW_OK;
+}
+
+}  // namespace pw
 
 extern "C" int pw_moe_route_topk_shared(const float* d_logits, int T, int E, int k, int S, int32_t* d_ids,
                                         float* d_w, int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm,
@@ -41,10 +60,8 @@ extern "C" int pw_moe_route_topk_shared(const float* d_logits, int T, int E, int
   if (T < 0 || T > (1 << 20)) return pw::set_error(PW_ERR_UNSUPPORTED, "route: T=%d outside [0, 2^20]", T);
   if (!d_offsets || (T > 0 && (!d_logits || !d_ids || !d_w || !d_perm || !d_inv_perm)))
     return pw::set_error(PW_ERR_INVALID_ARG, "route: NULL argument");
-  route_kernel<<<1, kThreads, 0, pw::as_stream(stream)>>>(d_logits, T, E, k, S, d_ids, d_w, d_offsets, d_perm,
-                                                         d_inv_perm, d_mass_accum);
-  PW_CUDA_TRY(cudaGetLastError());
-  return PW_OK;
+  return pw::route_layers(d_logits, 1, T, E, k, S, d_ids, d_w, d_offsets, d_perm, d_inv_perm, d_mass_accum,
+                          pw::as_stream(stream));
 }
 
 extern "C" int pw_moe_route_topk(const float* d_logits, int T, int E, int k, int32_t* d_ids, float* d_w,

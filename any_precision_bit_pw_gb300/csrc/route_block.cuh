@@ -35,9 +35,13 @@ __host__ __device__ constexpr size_t scratch_bytes(int E, int nwarps) {
 // included) to mass_accum when it is not NULL, summed in a fixed order so that
 // every result is the same from run to run.  The arrays are read back by this
 // CTA, so they must not alias the logits.
+// `base` is added to every offset, permutation entry and inverse-permutation
+// entry written (not to ids): a batch routed as one layer of several whose
+// assignment arrays are concatenated, this layer's slots starting at `base`
+// (the caller offsets the array pointers to this layer's part).
 __device__ inline void route_block(const float* __restrict__ logits, int T, int E, int k, int S, int32_t* ids,
                                    float* w, int32_t* offsets, int32_t* perm, int32_t* inv_perm,
-                                   float* mass_accum, uint8_t* scratch, size_t scratch_cap) {
+                                   float* mass_accum, uint8_t* scratch, size_t scratch_cap, int base = 0) {
   const int K = k + S, ET = E + S;
   const int nthreads = static_cast<int>(blockDim.x), nwarps = nthreads >> 5;
   const int tid = static_cast<int>(threadIdx.x), lane = tid & 31, warp = tid >> 5;
@@ -129,12 +133,12 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
   if (tid == 0) {
     int run = 0;
     for (int e = 0; e < ET; ++e) {
-      offsets[e] = run;
+      offsets[e] = base + run;
       s_base[e] = run;
       s_off[e] = run;
       run += s_cnt[e];
     }
-    offsets[ET] = run;
+    offsets[ET] = base + run;
     s_off[ET] = run;
   }
   __syncthreads();
@@ -185,8 +189,8 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
         const int e = my[j];
         const int pos = s_base[e] + s_wcnt[warp * ET + e] + rank[j];
         const int slot = t * K + j;
-        perm[pos] = slot;
-        inv_perm[slot] = pos;
+        perm[pos] = base + slot;
+        inv_perm[slot] = base + pos;
         if (wpos_smem) s_wpos[pos] = s_wslot[slot];
       }
     }
@@ -201,7 +205,7 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
   if (mass_accum) {
     for (int e = warp; e < ET; e += nwarps) {
       float acc = 0.f;
-      for (int pos = s_off[e] + lane; pos < s_off[e + 1]; pos += 32) acc += wpos_smem ? s_wpos[pos] : w[perm[pos]];
+      for (int pos = s_off[e] + lane; pos < s_off[e + 1]; pos += 32) acc += wpos_smem ? s_wpos[pos] : w[perm[pos] - base];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
       if (lane == 0) atomicAdd(&mass_accum[e], acc);

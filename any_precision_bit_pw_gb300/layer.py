@@ -249,6 +249,43 @@ class MoECall:
         return self.y[: self.T]
 
 
+class MoELayersCall:
+    """Preallocated buffers for ``layers`` consecutive layers of a stack, each
+    with ``tokens`` tokens, run in one launch (pw_moe_route_apl_ffn_layers).
+    The routing arrays are in the layers' concatenated index space
+    (``offsets`` [L*E+1], ``perm``/``inv_perm`` [L*T*k]); ``ids`` and ``w`` are
+    [L][T][k] with each layer's own expert ids."""
+
+    def __init__(self, stack: APLMoEStack, tokens: int, layers: int, device=None):
+        dev = stack.device if device is None else torch.device(device)
+        L, T, E, k = layers, tokens, stack.E, stack.k + stack.shared
+        self.stack, self.T, self.L = stack, T, L
+        A = max(1, L * T * k)
+        self.ids = torch.empty((L, max(T, 1), k), dtype=torch.int32, device=dev)
+        self.w = torch.empty((L, max(T, 1), k), dtype=torch.float32, device=dev)
+        self.offsets = torch.empty((L * E + 1,), dtype=torch.int32, device=dev)
+        self.perm = torch.empty((A,), dtype=torch.int32, device=dev)
+        self.inv_perm = torch.empty((A,), dtype=torch.int32, device=dev)
+        ws = pw.pw_moe_apl_ffn_workspace(L * T, stack.H, stack.I, L * E, k)
+        self.ws = torch.empty((max(ws, 256),), dtype=torch.uint8, device=dev)
+        self.y = torch.empty((L, max(T, 1), stack.H), dtype=torch.float16, device=dev)
+        self.status = torch.zeros((1,), dtype=torch.int32, device=dev)
+
+    def __call__(self, layer0: int, x: torch.Tensor, logits: torch.Tensor, mass: Optional[torch.Tensor] = None,
+                 options=None, stream=None) -> torch.Tensor:
+        """x [L][T][H], logits [L][T][E_routed]; ``mass`` [L][E] (accumulated)
+        or None.  Returns y [L][T][H]."""
+        s = self.stack
+        opts = pw.pw_ffn_options()
+        if options is not None:
+            ctypes.memmove(ctypes.addressof(opts), ctypes.addressof(options), ctypes.sizeof(opts))
+        opts.shared_experts = s.shared
+        pw.pw_moe_route_apl_ffn_layers(s.desc, layer0, x, logits, s.I, s.routed, s.k, self.ids, self.w, self.offsets,
+                                       self.perm, self.inv_perm, mass, self.ws, self.y, self.status, options=opts,
+                                       stream=stream)
+        return self.y[:, : self.T]
+
+
 def load_layer(stack: APLMoEStack, layer: int, inputs, experts=None, stream=None) -> None:
     """Load one layer's blocks from a synth.LayerInputs-like object (fields
     ``idx[(e, u)]``, ``luts[(e, u)][b]``, ``bits[2e+u]``) at their committed

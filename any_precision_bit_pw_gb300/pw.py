@@ -47,7 +47,7 @@ EXPORTS = (
     "pw_page_bytes", "pw_page_offload", "pw_page_reload", "pw_page_table_poll", "pw_page_table_take_released",
     "pw_page_state",
     "pw_moe_apl_ffn_workspace", "pw_moe_apl_ffn", "pw_moe_apl_ffn_ex", "pw_moe_apl_ffn_noalloc",
-    "pw_moe_route_apl_ffn", "pw_moe_route_apl_ffn_ex",
+    "pw_moe_route_apl_ffn", "pw_moe_route_apl_ffn_ex", "pw_moe_route_apl_ffn_layers",
     "pw_unpack_indices",
     "pw_apl_linear",
 )
@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
                                            P]),
             "pw_moe_route_apl_ffn_ex": (I32, [P, I32, P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P, SZ, P,
                                               P, ctypes.POINTER(pw_ffn_options), P]),
+            "pw_moe_route_apl_ffn_layers": (I32, [P, I32, I32, P, P, I32, I32, I32, I32, I32, P, P, P, P, P, P, P,
+                                                  SZ, P, P, ctypes.POINTER(pw_ffn_options), P]),
             "pw_unpack_indices": (I32, [P, I32, I32, P, P]),
             "pw_apl_linear": (I32, [P, I32, P, I32, P, P]),
         }
@@ -323,6 +325,27 @@ def pw_moe_route_apl_ffn(d_desc: torch.Tensor, layer: int, x: torch.Tensor, logi
         _check(lib().pw_moe_route_apl_ffn(*args, _stream(stream)))
     else:
         _check(lib().pw_moe_route_apl_ffn_ex(*args, ctypes.byref(options), _stream(stream)))
+
+
+def pw_moe_route_apl_ffn_layers(d_desc: torch.Tensor, layer0: int, x: torch.Tensor, logits: torch.Tensor, I: int,
+                                E: int, k: int, ids: torch.Tensor, w: torch.Tensor, offsets: torch.Tensor,
+                                perm: torch.Tensor, inv_perm: torch.Tensor, mass_accum: Optional[torch.Tensor],
+                                ws: torch.Tensor, y: torch.Tensor, status: torch.Tensor,
+                                options: Optional[pw_ffn_options] = None, stream=None) -> None:
+    """Routing and the fused expert layer of L independent layers in one
+    launch: x [L][T][H], logits [L][T][E], y [L][T][H]; the routing arrays
+    are outputs in the layers' concatenated index space (see pw.h)."""
+    _dev(x, torch.float16, "x")
+    _dev(y, torch.float16, "y")
+    _dev(logits, torch.float32, "logits")
+    L, T, H = x.shape
+    if tuple(logits.shape) != (L, T, E) or tuple(y.shape[:2]) != (L, T) or y.shape[2] != H:
+        raise ValueError(f"layers call: x {tuple(x.shape)}, logits {tuple(logits.shape)}, y {tuple(y.shape)}")
+    opts = options if options is not None else pw_ffn_options()
+    _check(lib().pw_moe_route_apl_ffn_layers(_ptr(d_desc), layer0, L, _ptr(x), _ptr(logits), T, H, I, E, k, _ptr(ids),
+                                             _ptr(w), _ptr(offsets), _ptr(perm), _ptr(inv_perm), _ptr(mass_accum),
+                                             _ptr(ws), ws.numel() * ws.element_size(), _ptr(y), _ptr(status),
+                                             ctypes.byref(opts), _stream(stream)))
 
 
 PW_NOALLOC_SCRATCH_BYTES = 32 << 20

@@ -106,9 +106,9 @@ class StackRun:
     page the schedule can lower (allocated up front, outside any timing)."""
 
     def __init__(self, wl, device, layers=None, commit_every: int = 8, n_commits: int = 7,
-                 final_fraction: float = 0.4, offload: bool = False):
+                 final_fraction: float = 0.4, offload: bool = False, batched: bool = False):
         from . import synth
-        from .layer import APLMoEStack, MoECall, load_layer
+        from .layer import APLMoEStack, MoECall, MoELayersCall, load_layer
         import torch
         self.torch, self.synth = torch, synth
         self.wl = wl
@@ -122,6 +122,8 @@ class StackRun:
             del li
         self.stack.sync()
         self.call = MoECall(self.stack, wl.tokens)
+        # batched: every layer of a step in one launch (pw_moe_route_apl_ffn_layers)
+        self.layers_call = MoELayersCall(self.stack, wl.tokens, self.L) if batched else None
 
         def block_bytes(b, q):
             return self.stack.block_bytes_at(self.stack.block_id(*b), q)
@@ -143,18 +145,40 @@ class StackRun:
         return (self.synth.activations(self.wl, layer, step, dev),
                 self.synth.router_logits(self.wl, layer, step, dev))
 
+    def inputs_all(self, step: int):
+        """Every layer's inputs of a step, stacked: x [L][T][H], logits [L][T][E]."""
+        xs, lgs = zip(*(self.inputs(layer, step) for layer in range(self.L)))
+        return self.torch.stack(xs).contiguous(), self.torch.stack(lgs).contiguous()
+
     def step(self, xs=None, logits=None, on_layer=None):
-        """One step: every layer routes and runs its fused expert layer, then
+        """One step: every layer routes and runs its fused expert layer (one
+        launch per layer, or one launch for all layers when batched), then
         the step boundary commits any lowering due.  ``on_layer(layer, y)`` is
-        called after each layer's call is enqueued (``y`` is reused by the next
-        layer)."""
-        for layer in range(self.L):
-            x, lg = (xs[layer], logits[layer]) if xs is not None else self.inputs(layer, self.step_no)
-            y = self.call(layer, x, lg)
+        called after each layer's output is enqueued (per-layer calls reuse
+        ``y`` for the next layer).  Batched steps take ``xs`` / ``logits`` as
+        stacked [L][T][...] tensors."""
+        if self.layers_call is not None:
+            if xs is None:
+                xs, logits = self.inputs_all(self.step_no)
+            y = self.layers_call(0, xs, logits, mass=self.call.mass)
             if on_layer is not None:
-                on_layer(layer, y)
+                for layer in range(self.L):
+                    on_layer(layer, y[layer])
+        else:
+            for layer in range(self.L):
+                x, lg = (xs[layer], logits[layer]) if xs is not None else self.inputs(layer, self.step_no)
+                y = self.call(layer, x, lg)
+                if on_layer is not None:
+                    on_layer(layer, y)
         self.step_no += 1
         return self.boundary()
+
+    def status(self) -> int:
+        """The device status word of the calls (0 = fine)."""
+        st = int(self.call.status.item())
+        if st == 0 and self.layers_call is not None:
+            st = int(self.layers_call.status.item())
+        return st
 
     def _host_slice(self, nbytes: int):
         start = (self.arena_used + 255) & ~255

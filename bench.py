@@ -377,9 +377,11 @@ def gpu_arm(args, rank, world, local_rank):
 
 def stack_arm(args, rank, world, local_rank):
     """The 32-layer decode stack: every step runs routing + the fused layer
-    for each of the L layers on fresh seeded inputs; every 8 steps the step
-    boundary reads the accumulated routing mass, lowers blocks to the byte
-    target and releases their pages (all inside the timed region)."""
+    for each of the L layers on fresh seeded inputs -- all layers in one
+    launch (pw_moe_route_apl_ffn_layers), or with --per-layer one launch per
+    layer; every 8 steps the step boundary reads the accumulated routing
+    mass, lowers blocks to the byte target and releases their pages (all
+    inside the timed region)."""
     from any_precision_bit_pw_gb300 import pw
     from any_precision_bit_pw_gb300.stack import StackRun
 
@@ -389,25 +391,34 @@ def stack_arm(args, rank, world, local_rank):
     wl = get_workload(args.workload, args.tokens)
     sh = wl.shape
     T, H, E, L = wl.tokens, sh.hidden, sh.experts, wl.layers
+    batched = not args.per_layer
     run = StackRun(wl, dev, commit_every=synth.STACK_COMMIT_EVERY,
-                   n_commits=synth.STACK_STEPS // synth.STACK_COMMIT_EVERY - 1, offload=args.offload)
+                   n_commits=synth.STACK_STEPS // synth.STACK_COMMIT_EVERY - 1, offload=args.offload,
+                   batched=batched)
     f8 = run.schedule.f8
     K = args.steps
     n_in = min(K, 16)
     xs = [[synth.activations(wl, l, s, dev) for l in range(L)] for s in range(n_in)]
     lgs = [[synth.router_logits(wl, l, s, dev) for l in range(L)] for s in range(n_in)]
+    if batched:
+        xs_b = [torch.stack(xs[s]).contiguous() for s in range(n_in)]
+        lgs_b = [torch.stack(lgs[s]).contiguous() for s in range(n_in)]
     call, stack = run.call, run.stack
     stream = torch.cuda.current_stream()
     routed = not prefill_path(T, sh.top_k, E)
 
     # warm-up: the layer calls without step boundaries (no commits, no mass)
     for i in range(args.warmup):
-        for l in range(L):
-            call(l, xs[i % n_in][l], lgs[i % n_in][l], accumulate_mass=False)
+        if batched:
+            run.layers_call(0, xs_b[i % n_in], lgs_b[i % n_in])
+        else:
+            for l in range(L):
+                call(l, xs[i % n_in][l], lgs[i % n_in][l], accumulate_mass=False)
     torch.cuda.synchronize()
     call.mass.zero_()
 
-    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(L)]
+    n_ev = 1 if batched else L
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n_ev)]
           for _ in range(K)]
     bits_at = []            # committed bits of every block during each step
     resident = []
@@ -426,8 +437,13 @@ def stack_arm(args, rank, world, local_rank):
             bits_at.append([stack.committed_bits(b) for b in range(stack.n_blocks)])
             resident.append(stack.resident_bytes())
             s = i % n_in
-            for l in range(L):
-                layer_call(pw, stack, call, l, xs[s][l], lgs[s][l], call.mass[l], ev[i][l], stream, routed)
+            if batched:
+                ev[i][0][0].record(stream)
+                run.layers_call(0, xs_b[s], lgs_b[s], mass=call.mass)
+                ev[i][0][1].record(stream)
+            else:
+                for l in range(L):
+                    layer_call(pw, stack, call, l, xs[s][l], lgs[s][l], call.mass[l], ev[i][l], stream, routed)
             run.step_no += 1
             plan, released = run.boundary()
             released_total += released
@@ -439,8 +455,8 @@ def stack_arm(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     total_ms = start.elapsed_time(stop)
-    ffn_ms = np.array([[ev[i][l][0].elapsed_time(ev[i][l][1]) for l in range(L)] for i in range(K)])
-    status = int(call.status.item())
+    ffn_ms = np.array([[ev[i][l][0].elapsed_time(ev[i][l][1]) for l in range(n_ev)] for i in range(K)])
+    status = run.status()
 
     # algorithmic bytes of each launch: replay the routing (deterministic) untimed
     nbytes = np.zeros((K, L))
@@ -458,11 +474,20 @@ def stack_arm(args, rank, world, local_rank):
     hl = [[lgs[s][l].cpu().pin_memory() for l in range(L)] for s in range(min(n_in, 2))]
     hy = torch.empty((L, T, H), dtype=torch.float16).pin_memory()
     dx, dl = torch.empty_like(xs[0][0]), torch.empty_like(lgs[0][0])
+    if batched:
+        hx = [torch.stack(h).pin_memory() for h in hx]
+        hl = [torch.stack(h).pin_memory() for h in hl]
+        dx, dl = torch.empty_like(xs_b[0]), torch.empty_like(lgs_b[0])
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(stream)
     for i in range(K2):
         s = i % len(hx)
+        if batched:
+            dx.copy_(hx[s], non_blocking=True)
+            dl.copy_(hl[s], non_blocking=True)
+            hy.copy_(run.layers_call(0, dx, dl), non_blocking=True)
+            continue
         for l in range(L):
             dx.copy_(hx[s][l], non_blocking=True)
             dl.copy_(hl[s][l], non_blocking=True)
@@ -474,9 +499,12 @@ def stack_arm(args, rank, world, local_rank):
     total_ms = max_over_ranks(total_ms, world, dev)
     peak, peak_kind = _peaks()
     achieved = float(nbytes.sum() / (ffn_ms.sum() * 1e-3) / 1e9)
+    per_launch = nbytes.sum(axis=1) if batched else nbytes.reshape(-1)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": None, "kernel": kernel_label(ffn_kernel(T, sh.top_k, E)),
-                "algorithmic_bytes_per_launch": float(nbytes.mean()), "launch_ms": float(ffn_ms.mean()),
+                "launch": "all layers of a step in one launch" if batched else "one launch per layer",
+                "algorithmic_bytes_per_launch": float(per_launch.mean()), "launch_ms": float(ffn_ms.mean()),
+                "layer_ms": float(ffn_ms.sum() / (K * L)),
                 "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"}
     value = job_throughput(T, K, world, total_ms)
     return {
@@ -495,7 +523,7 @@ def stack_arm(args, rank, world, local_rank):
         "roofline": roofline,
         "e2e": {"value": T / (e2e_ms * 1e-3), "unit": UNIT,
                 "h2d_bytes_per_step": L * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": L * T * H * 2},
-        "gpu_launches": (1 if routed else 2) * L * K,
+        "gpu_launches": (1 if routed else 2) * (1 if batched else L) * K,
         "clocks": clk.summary(),
         "status": status,
     }
@@ -526,20 +554,29 @@ def sweep(args, dev, out_path):
             torch.cuda.synchronize()
             off = call.route.offsets.cpu().numpy()
             nbytes, planes, _ = algorithmic_bytes(wl.with_(tokens=T), li8.bits, off)
-            reps = 50
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record()
-            for _ in range(reps):
-                pw.pw_moe_apl_ffn(stack.desc, 0, x, sh.intermediate, sh.experts, sh.top_k, call.route.ids,
-                                  call.route.w, call.route.offsets, call.route.perm, call.route.inv_perm,
-                                  call.ws, call.y, call.status)
-            e1.record()
-            torch.cuda.synchronize()
-            ms = e0.elapsed_time(e1) / reps
+
+            def timed(reps):
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record()
+                for _ in range(reps):
+                    pw.pw_moe_apl_ffn(stack.desc, 0, x, sh.intermediate, sh.experts, sh.top_k, call.route.ids,
+                                      call.route.w, call.route.offsets, call.route.perm, call.route.inv_perm,
+                                      call.ws, call.y, call.status)
+                e1.record()
+                torch.cuda.synchronize()
+                return e0.elapsed_time(e1) / reps
+            # enough launches for about half a second, with the clocks sampled meanwhile
+            reps = max(50, int(500.0 / max(timed(10), 1e-3)))
+            with ClockSampler(args.smi_index) as clk:
+                ms = timed(reps)
             gbs = nbytes / (ms * 1e-3) / 1e9
-            results.append({"bits": b, "tokens": T, "ffn_ms": ms, "tokens_per_s": T / (ms * 1e-3),
+            results.append({"bits": b, "tokens": T, "kernel": ffn_kernel(T, sh.top_k, sh.experts),
+                            "path": "prefill" if prefill_path(T, sh.top_k, sh.experts) else "decode",
+                            "ffn_ms": ms, "launches": reps, "tokens_per_s": T / (ms * 1e-3),
+                            "algorithmic_bytes": nbytes, "plane_bytes": planes,
                             "algorithmic_GBps": gbs, "plane_GBps": planes / (ms * 1e-3) / 1e9,
-                            "frac_of_measured_hbm": gbs / peak, "status": int(call.status.item())})
+                            "frac_of_measured_hbm": gbs / peak, "clocks": clk.summary(),
+                            "status": int(call.status.item())})
             print(json.dumps(results[-1]), file=sys.stderr)
         del stack
         torch.cuda.empty_cache()
@@ -686,6 +723,8 @@ def main():
     ap.add_argument("--offload", action="store_true",
                     help="stack workload: lowering copies the released pages to pinned host memory first (§3.3)")
     ap.add_argument("--sweep", default=None, help="also run the uniform-bitwidth sweep, JSON to this path")
+    ap.add_argument("--per-layer", action="store_true",
+                    help="stack workload: one launch per layer instead of all layers of a step in one launch")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-baseline-child", action="store_true", help=argparse.SUPPRESS)
     ap.add_argument("--reference-child", action="store_true", help=argparse.SUPPRESS)
@@ -723,6 +762,8 @@ def main():
     if cpu is not None:
         line["cpu_baseline"] = cpu
     if args.sweep and rank == 0:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+        args.smi_index = vis.split(",")[local_rank] if vis and len(vis.split(",")) > local_rank else str(local_rank)
         sweep(args, torch.device(f"cuda:{local_rank}"), args.sweep)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -379,6 +379,32 @@ int pw_moe_route_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, 
                             float* d_mass_accum, void* d_ws, size_t ws_bytes, uint16_t* d_y,
                             int32_t* d_status, const pw_ffn_options* opts, void* stream);
 
+/* Several independent MoE layers in one launch: the routed call of
+ * pw_moe_route_apl_ffn_ex for layers layer0 .. layer0+L-1 of the descriptor
+ * array, each with its own T tokens (§3.3's fused kernel, applied to a stack
+ * of layers whose inputs are all known, e.g. a decode stack with independent
+ * per-layer batches).  The layers run as one layer of L*T tokens and
+ * L*(E+S) experts whose routing never crosses layers, so one persistent grid
+ * works through every layer's units and the per-launch start-up and tail are
+ * paid once.  Layouts, all arrays concatenated layer after layer:
+ *  d_x fp16 [L][T][H], d_logits fp32 [L][T][E], d_y fp16 [L][T][H];
+ *  d_ids int32 [L][T][k+S] (each layer's own expert ids, 0 .. E+S-1) and
+ *  d_w fp32 [L][T][k+S];
+ *  d_offsets int32 [L*(E+S)+1], d_perm and d_inv_perm int32 [L*T*(k+S)] in
+ *  the concatenated index space: layer l's expert e starts at
+ *  d_offsets[l*(E+S)+e], and its assignment slots are l*T*(k+S) + t*(k+S) + j;
+ *  d_mass_accum fp32 [L][E+S] or NULL.
+ * Workspace: pw_moe_apl_ffn_workspace(L*T, H, I, L*(E+S), k+S).  L*(E+S) must
+ * be at most 256.  Every result equals that of L pw_moe_route_apl_ffn_ex
+ * calls bit for bit (after the index shift above); every other argument,
+ * limit and error is that of pw_moe_route_apl_ffn_ex. */
+int pw_moe_route_apl_ffn_layers(const void* d_desc, int layer0, int L, const uint16_t* d_x,
+                                const float* d_logits, int T, int H, int I, int E, int k,
+                                int32_t* d_ids, float* d_w, int32_t* d_offsets, int32_t* d_perm,
+                                int32_t* d_inv_perm, float* d_mass_accum, void* d_ws, size_t ws_bytes,
+                                uint16_t* d_y, int32_t* d_status, const pw_ffn_options* opts,
+                                void* stream);
+
 /* ------------------------------------------------------------------------ */
 /* Test exports: they run the same device dequant code as the fused layer.     */
 /* ------------------------------------------------------------------------ */

@@ -161,11 +161,15 @@ def test_stack32_full_schedule_matches_oracle_every_phase(offload):
     (two per phase with page release, one with offload) are checked token by
     token against the oracle under the bitwidths committed at that step;
     every commit releases exactly the Eq. 3 bytes and the table's resident
-    bytes follow the schedule."""
+    bytes follow the schedule.  With page release every step runs the 32
+    layers in one launch; with offload, one launch per layer."""
     wl = synth.MIXTRAL_8X7B_STACK
     L, E = wl.layers, wl.shape.experts
+    # page release runs every step's 32 layers in one launch
+    # (pw_moe_route_apl_ffn_layers), offload one launch per layer
     run = StackRun(wl, DEV, commit_every=synth.STACK_COMMIT_EVERY,
-                   n_commits=synth.STACK_STEPS // synth.STACK_COMMIT_EVERY - 1, offload=offload)
+                   n_commits=synth.STACK_STEPS // synth.STACK_COMMIT_EVERY - 1, offload=offload,
+                   batched=not offload)
     st = run.stack
     f8 = run.schedule.f8
     assert st.resident_bytes() == f8
@@ -180,7 +184,7 @@ def test_stack32_full_schedule_matches_oracle_every_phase(offload):
         plan, released = run.step(on_layer=lambda l, y: outs.__setitem__(l, y.float().cpu().numpy())
                                   if l in layers else None)
         torch.cuda.synchronize()
-        assert int(run.call.status.item()) == 0, step
+        assert run.status() == 0, step
         for l in layers:
             seen_bits |= _check_layer(run, l, step, outs[l], bits[l])
             checks += 1

@@ -216,3 +216,14 @@ def test_noalloc_accepts_exactly_the_sizes_whose_path_fits(L):
     for T in (142, 191, 316, 4096):
         assert rc(T) == pw.PW_ERR_WORKSPACE, T
         assert "scratch" in pw.pw_last_error()
+
+
+def test_layers_call_checks_sizes_before_any_launch(L):
+    def rc(nl, E=8, T=128):
+        return L.pw_moe_route_apl_ffn_layers(None, 0, nl, None, None, T, 4096, 14336, E, 2, None, None, None, None,
+                                             None, None, None, 0, None, None, None, None)
+    assert rc(33) == pw.PW_ERR_UNSUPPORTED            # 33 layers x 8 experts > 256
+    assert "exceed" in pw.pw_last_error()
+    assert rc(0) == pw.PW_ERR_INVALID_ARG
+    assert rc(32) == pw.PW_ERR_INVALID_ARG           # sizes fine: the NULL arguments are next
+    assert rc(2, E=200) == pw.PW_ERR_UNSUPPORTED
