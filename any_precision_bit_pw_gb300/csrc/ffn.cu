@@ -44,11 +44,21 @@ WsLayout ws_layout(int T, int H, int I, int E, int k, int path) {
   return L;
 }
 
-// Token-tile width: 16 while experts average fewer than 12 tokens, else 64.
-// Measured on the 8x7B shape: at 8 tokens per expert and fewer the 64-token
-// kernel is 25-45 % slower; at 16 and more it is 10-13 % faster (it needs
-// fewer token groups, each of which reads and dequantises the weights again).
-int tile_width(int T, int E, int k) { return static_cast<long long>(T) * k < 12ll * E ? 16 : 64; }
+// Token-tile width: 16 while experts average fewer than 12 tokens, 64 below
+// 96, else 128.  Measured on the 8x7B shape: at 8 tokens per expert and fewer
+// the 64-token kernel is 25-45 % slower; at 16 and more it is 10-13 % faster
+// (it needs fewer token groups, each of which reads and dequantises the
+// weights again).  128-token tiles halve the dequantisation again for
+// prefill batches.
+int tile_width(int T, int E, int k) {
+  const long long A = static_cast<long long>(T) * k;
+  return A < 12ll * E ? 16 : (A < 96ll * E ? 64 : 128);
+}
+
+int launch_width(int width, const Params& p, cudaStream_t s) {
+  return width == 16 ? pw_ffn::launch_ffn_t16(p, s)
+                     : (width == 64 ? pw_ffn::launch_ffn_t64(p, s) : pw_ffn::launch_ffn_t128(p, s));
+}
 
 // Workspace of the path pw_moe_apl_ffn picks by itself for this size.
 WsLayout ws_layout(int T, int H, int I, int E, int k) {
@@ -177,7 +187,7 @@ int ffn_launch(bool routed, const void* d_desc, int layer, int L, const uint16_t
     p.mass_accum = d_mass_accum;
   }
   PW_CUDA_TRY(cudaMemsetAsync(p.ctr, 0, W.h - W.ctr, s));
-  return tile_width(T, E, k) == 16 ? pw_ffn::launch_ffn_t16(p, s) : pw_ffn::launch_ffn_t64(p, s);
+  return launch_width(tile_width(T, E, k), p, s);
 }
 
 }  // namespace
@@ -252,7 +262,7 @@ int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,
   p.linear = 1;
   p.nsplit = 1;
   p.split_cols = d.cols;
-  return M <= 16 ? pw_ffn::launch_ffn_t16(p, s) : pw_ffn::launch_ffn_t64(p, s);
+  return launch_width(M <= 16 ? 16 : (M <= 64 ? 64 : 128), p, s);
 }
 
 }  // extern "C"

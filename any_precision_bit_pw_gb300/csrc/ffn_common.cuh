@@ -359,8 +359,9 @@ __device__ inline void combine_all(const Params& p, long long tid, long long nth
 }
 
 // Kernel launchers (one translation unit each, ffn_stream.cuh instantiated
-// for 16- and 64-token tiles).
-int launch_ffn_t16(const Params& p, cudaStream_t s);   // 16-token tiles
-int launch_ffn_t64(const Params& p, cudaStream_t s);   // 64-token tiles
+// for 16-, 64- and 128-token tiles).
+int launch_ffn_t16(const Params& p, cudaStream_t s);    // 16-token tiles
+int launch_ffn_t64(const Params& p, cudaStream_t s);    // 64-token tiles
+int launch_ffn_t128(const Params& p, cudaStream_t s);   // 128-token tiles
 
 }  // namespace pw_ffn

@@ -1,5 +1,5 @@
 // Fused MoE layer kernel body, instantiated per token-tile width: a
-// translation unit defines PW_TILE_N (16, 32 or 64 tokens per tile),
+// translation unit defines PW_TILE_N (16, 32, 64 or 128 tokens per tile),
 // PW_KERNEL_NAME and PW_LAUNCHER_NAME, then includes this file.  See
 // ffn_common.cuh for the work units and their scheduling.
 //
@@ -10,7 +10,8 @@
 //     committed plane of its tile from a shared chunk, turns the row's 128
 //     columns into fp16 through its LUT (dequant.cuh) and stores them as
 //     operand A in one of the TMEM A slots (tcgen05.st);
-//   MMA issuers (one thread per warp; 4 for N <= 32, 2 for N = 64): issuer k
+//   MMA issuers (one thread per warp; 4 for N <= 32, 2 for N = 64, 1 for
+//     N = 128, whose two accumulator buffers take half of TMEM): issuer k
 //     takes the tiles x with x % issuers == k and issues each tile's eight
 //     tcgen05.mma (A from TMEM, B from shared memory, fp32 accumulator in its
 //     own double-buffered TMEM columns), committed to the tile's "free"
@@ -45,12 +46,12 @@ namespace pw_ffn {
 namespace {
 
 #ifndef PW_TILE_N
-#error "define PW_TILE_N (16, 32 or 64) before including ffn_stream.cuh"
+#error "define PW_TILE_N (16, 32, 64 or 128) before including ffn_stream.cuh"
 #endif
 constexpr int kN = PW_TILE_N;                     // tokens per tile
-static_assert(kN == 16 || kN == 32 || kN == 64, "tile widths");
+static_assert(kN == 16 || kN == 32 || kN == 64 || kN == 128, "tile widths");
 constexpr int kSets = 4;                          // dequant warp sets
-constexpr int kIssuers = kN <= 32 ? 4 : 2;        // MMA issuing warps
+constexpr int kIssuers = kN <= 32 ? 4 : (kN == 64 ? 2 : 1);   // MMA issuing warps
 constexpr int kDeqWarpsAll = kSets * 4;           // warps 0-15
 constexpr int kMmaWarp0 = kDeqWarpsAll;           // MMA issuers
 constexpr int kEpiWarp0 = kMmaWarp0 + kIssuers;   // 4 epilogue warps
@@ -65,10 +66,10 @@ constexpr int kDCol0 = kSA * kATileCols;          // accumulators: [buffer][issu
 constexpr int kTmemCols = 512;
 constexpr int kF = 16;                            // tile barrier slots (tile index mod 16)
 constexpr int kUS = 4;                            // unit slots
-constexpr int kBS = kN <= 32 ? 6 : 3;             // B ring slots
+constexpr int kBS = kN <= 32 ? 6 : (kN == 64 ? 3 : 2);        // B ring slots
 constexpr int kBAtom = kN * 128;                  // kN rows x 64 fp16, 128-byte swizzle
 constexpr int kBBytes = 2 * kBAtom;               // B of one tile
-constexpr int kPS = kN <= 16 ? 4 : 3;             // plane chunk slots
+constexpr int kPS = kN <= 16 ? 4 : (kN == 64 ? 3 : 2);        // plane chunk slots
 constexpr int kPSlotBytes = 32768;                // one chunk: up to 4 tiles x 4 planes or 2 tiles x 8 planes
 constexpr int kSmemBytes = 232448;
 constexpr uint32_t kHintNs = 20000;

@@ -110,7 +110,9 @@ def get_workload(name: str, tokens=None):
 def ffn_kernel(tokens: int, top_k: int, experts: int) -> str:
     """The fused-layer kernel pw_moe_apl_ffn picks for this size (token-tile
     width from the average tokens per expert, as in the library)."""
-    return "apl_ffn_t16_kernel" if tokens * top_k < 12 * experts else "apl_ffn_t64_kernel"
+    A = tokens * top_k
+    return "apl_ffn_t16_kernel" if A < 12 * experts else ("apl_ffn_t64_kernel" if A < 96 * experts
+                                                           else "apl_ffn_t128_kernel")
 
 
 def prefill_path(tokens: int, top_k: int, experts: int) -> bool:
@@ -118,7 +120,7 @@ def prefill_path(tokens: int, top_k: int, experts: int) -> bool:
     return tokens * top_k >= 48 * experts
 
 
-KERNEL_TILE = {"apl_ffn_t16_kernel": 16, "apl_ffn_t64_kernel": 64}
+KERNEL_TILE = {"apl_ffn_t16_kernel": 16, "apl_ffn_t64_kernel": 64, "apl_ffn_t128_kernel": 128}
 
 
 def kernel_label(name: str) -> str:

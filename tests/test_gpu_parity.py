@@ -278,7 +278,9 @@ def test_ffn_is_deterministic():
     (256, 2304, 3, 1, 9, (6, 3)),         # I below the 3072-column down split
     (256, 3200, 2, 1, 6, (5, 8)),         # I = 3072 + 128: a one-tile last down split
     (128, 6272, 2, 2, 3, (3, 4)),         # I = 2 * 3072 + 128, H of one strip
-    (384, 640, 2, 2, 300, (5, 4)),        # odd strip counts, 300 tokens per expert
+    (384, 640, 2, 2, 300, (5, 4)),        # odd strip counts, 300 tokens per expert (128-token tiles)
+    (256, 512, 2, 1, 192, (8, 3)),        # 96 tokens per expert: the smallest batch on 128-token tiles
+    (128, 384, 3, 3, 250, (7, 6)),        # every token to every expert: 250 per expert, a ragged last tile
 ])
 def test_ffn_edge_shapes(H, I, E, k, T, bits, path):
     wl = synth.Workload("edge", synth.MoEShape(H, I, E, k), tokens=T, parent_bits=8, seed_bits=2, seed=H + I + T,
