@@ -55,9 +55,14 @@ int tile_width(int T, int E, int k) {
   return A < 12ll * E ? 16 : (A < 96ll * E ? 64 : 128);
 }
 
+// Width 2: the CUDA-core instance.
 int launch_width(int width, const Params& p, cudaStream_t s) {
-  return width == 16 ? pw_ffn::launch_ffn_t16(p, s)
-                     : (width == 64 ? pw_ffn::launch_ffn_t64(p, s) : pw_ffn::launch_ffn_t128(p, s));
+  switch (width) {
+    case 2: return pw_ffn::launch_ffn_gemv(p, s);
+    case 16: return pw_ffn::launch_ffn_t16(p, s);
+    case 64: return pw_ffn::launch_ffn_t64(p, s);
+    default: return pw_ffn::launch_ffn_t128(p, s);
+  }
 }
 
 // Workspace of the path pw_moe_apl_ffn picks by itself for this size.
@@ -137,6 +142,8 @@ int ffn_launch(bool routed, const void* d_desc, int layer, int L, const uint16_t
     return pw::set_error(PW_ERR_INVALID_ARG, "ffn: descriptor/x must be 16-byte aligned, y 8-byte aligned");
   pw_ffn_options o{};
   if (opts) o = *opts;
+  if (o.kernel != PW_KERNEL_AUTO && o.kernel != PW_KERNEL_TENSOR && o.kernel != PW_KERNEL_CUDA_CORES)
+    return pw::set_error(PW_ERR_INVALID_ARG, "ffn: kernel %d", o.kernel);
   const int path = choose_path(T, E, k, o.path);
   const WsLayout W = ws_layout(T, H, I, E, k, path);
   if (ws_bytes < W.total || (reinterpret_cast<uintptr_t>(d_ws) & 255))
@@ -187,7 +194,7 @@ int ffn_launch(bool routed, const void* d_desc, int layer, int L, const uint16_t
     p.mass_accum = d_mass_accum;
   }
   PW_CUDA_TRY(cudaMemsetAsync(p.ctr, 0, W.h - W.ctr, s));
-  return launch_width(tile_width(T, E, k), p, s);
+  return launch_width(o.kernel == PW_KERNEL_CUDA_CORES ? 2 : tile_width(T, E, k), p, s);
 }
 
 }  // namespace
@@ -262,7 +269,7 @@ int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,
   p.linear = 1;
   p.nsplit = 1;
   p.split_cols = d.cols;
-  return launch_width(M <= 16 ? 16 : (M <= 64 ? 64 : 128), p, s);
+  return launch_width(M <= 2 ? 2 : (M <= 16 ? 16 : (M <= 64 ? 64 : 128)), p, s);
 }
 
 }  // extern "C"

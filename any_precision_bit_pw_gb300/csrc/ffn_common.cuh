@@ -140,6 +140,16 @@ __device__ void setup_schedule(const Params& p, Shared& sh) {
   }
   int n = 0, gu = 0, dn = 0, arr = 0;
   const int gu_strips = 2 * p.I / 128, dn_strips = p.H / 128;
+  // the offsets must run from 0 to A without decreasing, or no unit is run
+  // (a unit's rows are read and written at these offsets)
+  bool offsets_ok = p.offsets[0] == 0 && p.offsets[p.E] == p.A;
+  for (int e = 0; e < p.E && offsets_ok; ++e) offsets_ok = p.offsets[e + 1] >= p.offsets[e];
+  if (!offsets_ok) {
+    report(p.status, PW_ERR_INVALID_ARG);
+    sh.nact = 0;
+    sh.arrivals_per_strip = 0;
+    return;
+  }
   for (int e = 0; e < p.E; ++e) {
     const int ne = p.offsets[e + 1] - p.offsets[e];
     if (ne <= 0) continue;
@@ -316,6 +326,10 @@ __device__ __forceinline__ void combine_item(const Params& p, int t, int row) {
   for (int j = 0; j < p.k; ++j) {
     const int slot = t * p.k + j;
     const int ps = p.inv_perm[slot];
+    if (static_cast<unsigned>(ps) >= static_cast<unsigned>(p.A)) {   // not a permutation of the slots
+      report(p.status, PW_ERR_INVALID_ARG);
+      continue;
+    }
     const float wt = p.w[slot];
     const float4* base = reinterpret_cast<const float4*>(p.part + static_cast<long long>(ps) * p.H + row);
     const long long sstride = static_cast<long long>(p.A) * p.H / 4;   // float4 per split
@@ -363,5 +377,6 @@ __device__ inline void combine_all(const Params& p, long long tid, long long nth
 int launch_ffn_t16(const Params& p, cudaStream_t s);    // 16-token tiles
 int launch_ffn_t64(const Params& p, cudaStream_t s);    // 64-token tiles
 int launch_ffn_t128(const Params& p, cudaStream_t s);   // 128-token tiles
+int launch_ffn_gemv(const Params& p, cudaStream_t s);   // 2-token tiles on the CUDA cores
 
 }  // namespace pw_ffn

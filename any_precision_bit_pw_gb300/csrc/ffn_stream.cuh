@@ -48,10 +48,20 @@ namespace {
 #ifndef PW_TILE_N
 #error "define PW_TILE_N (16, 32, 64 or 128) before including ffn_stream.cuh"
 #endif
+#ifndef PW_GEMV
+#define PW_GEMV 0
+#endif
 constexpr int kN = PW_TILE_N;                     // tokens per tile
-static_assert(kN == 16 || kN == 32 || kN == 64 || kN == 128, "tile widths");
+// CUDA-core instance: the dequant warps multiply the dequantised weights with
+// the tile's (at most kN = 2) token rows themselves (fp32 FMA) instead of
+// handing them to the tensor core; no MMA issuers, no TMEM A slots
+constexpr bool kGemv = PW_GEMV != 0;
+static_assert(kGemv ? kN == 2 : (kN == 16 || kN == 32 || kN == 64 || kN == 128), "tile widths");
 constexpr int kSets = 4;                          // dequant warp sets
-constexpr int kIssuers = kN <= 32 ? 4 : (kN == 64 ? 2 : 1);   // MMA issuing warps
+constexpr int kIssuers = kGemv ? 0 : (kN <= 32 ? 4 : (kN == 64 ? 2 : 1));   // MMA issuing warps
+constexpr int kAccSlots = kGemv ? kSets : kIssuers;   // partial accumulators summed by the epilogue
+constexpr int kAccCols = kN < 16 ? 16 : kN;           // TMEM columns per partial accumulator
+constexpr int kIssuersOr1 = kIssuers > 0 ? kIssuers : 1;
 constexpr int kDeqWarpsAll = kSets * 4;           // warps 0-15
 constexpr int kMmaWarp0 = kDeqWarpsAll;           // MMA issuers
 constexpr int kEpiWarp0 = kMmaWarp0 + kIssuers;   // 4 epilogue warps
@@ -60,14 +70,15 @@ constexpr int kLoadWarp = kEpiWarp0 + 4;          // plane chunks
 constexpr int kSchedWarp = kLoadWarp + 1;
 constexpr int kBLoadWarp = kSchedWarp + 1;        // B operands
 constexpr int kThreads = (kBLoadWarp + 1) * 32;
-constexpr int kSA = kN <= 16 ? 6 : 4;             // TMEM A slots
+constexpr int kSA = kGemv ? 0 : (kN <= 16 ? 6 : 4);   // TMEM A slots
+constexpr int kSAOr1 = kSA > 0 ? kSA : 1;
 constexpr int kATileCols = 64;                    // TMEM columns per A tile (128 fp16 per row)
 constexpr int kDCol0 = kSA * kATileCols;          // accumulators: [buffer][issuer] x kN columns from here
 constexpr int kTmemCols = 512;
 constexpr int kF = 16;                            // tile barrier slots (tile index mod 16)
 constexpr int kUS = 4;                            // unit slots
-constexpr int kBS = kN <= 32 ? 6 : (kN == 64 ? 3 : 2);        // B ring slots
-constexpr int kBAtom = kN * 128;                  // kN rows x 64 fp16, 128-byte swizzle
+constexpr int kBS = kGemv ? 8 : (kN <= 32 ? 6 : (kN == 64 ? 3 : 2));   // B ring slots
+constexpr int kBAtom = kN * 128;                  // kN rows x 64 fp16 (128-byte swizzle; unswizzled for kGemv)
 constexpr int kBBytes = 2 * kBAtom;               // B of one tile
 constexpr int kPS = kN <= 16 ? 4 : (kN == 64 ? 3 : 2);        // plane chunk slots
 constexpr int kPSlotBytes = 32768;                // one chunk: up to 4 tiles x 4 planes or 2 tiles x 8 planes
@@ -77,10 +88,10 @@ constexpr uint32_t kHintNs = 20000;
 // faster with the smaller loop body (fewer instruction-fetch stalls), the
 // 64-token kernel with both halves unrolled (measured).
 constexpr int kHalfUnroll = kN <= 32 ? 1 : 2;
-static_assert(kDCol0 + 2 * kIssuers * kN <= kTmemCols, "TMEM columns");
+static_assert(kDCol0 + 2 * kAccSlots * kAccCols <= kTmemCols, "TMEM columns");
 static_assert(kSA <= kF && 2 * kBS <= kF, "barrier reuse distances");
 static_assert(4 * 4 * 2048 <= kPSlotBytes && 2 * 8 * 2048 <= kPSlotBytes, "chunk sizes");
-static_assert(kSets % kIssuers == 0, "issuers share sets evenly");
+static_assert(kGemv || kSets % kIssuersOr1 == 0, "issuers share sets evenly");
 static_assert(pw_route::scratch_bytes(pw_route::kMaxE, kThreads / 32) <= pw::kLutRegionBytes,
               "routing scratch fits the LUT region");
 
@@ -184,6 +195,12 @@ __device__ __forceinline__ bool wait_unit(const Sm sm, uint32_t i, const Params&
   return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// TMEM column of partial accumulator k (an MMA issuer's, or a set's on the
+// CUDA-core instance) in buffer db.
+__device__ __forceinline__ uint32_t acc_col(uint32_t db, int k) {
+  return kDCol0 + (db * kAccSlots + static_cast<uint32_t>(k)) * kAccCols;
+}
+
 // ---------------------------------------------------------------------------
 // dequant warps
 // ---------------------------------------------------------------------------
@@ -226,6 +243,9 @@ __device__ __forceinline__ bool dequant_unit(const Params& p, const Unit& u, con
   const int nt = u.nst / 2;
   const int nch = (nt + kCt - 1) / kCt;
   const uint32_t tl = tmem + (static_cast<uint32_t>(32 * qd) << 16);
+  float gacc[kGemv ? kN : 1];   // CUDA-core instance: this row's partial sums, one per token
+#pragma unroll
+  for (int r = 0; r < (kGemv ? kN : 1); ++r) gacc[r] = 0.f;
   for (int k = 0; k < nch; ++k) {
     const uint32_t c = c0 + static_cast<uint32_t>(k);
     const int ps = static_cast<int>(c % kPS);
@@ -235,13 +255,65 @@ __device__ __forceinline__ bool dequant_unit(const Params& p, const Unit& u, con
     const bool has = ok && j < n_in;
     if (ok) ok = wait_bar(sm, kBarPFull + ps, (c / kPS) & 1u, p);
     if (!ok) return false;
-    if (has) {
+    if constexpr (kGemv) if (has) {
+      // the tile's token rows (B slot x % kBS, row-major: atom of 64
+      // columns, 128 bytes per row); the slot's previous tile (x - kBS,
+      // another set's) must be consumed before its parity names tile x
+      const uint32_t x = xs + static_cast<uint32_t>(j);
+      if (x >= kBS && !wait_bar(sm, kBarTFree + static_cast<int>((x - kBS) % kF), ((x - kBS) / kF) & 1u, p))
+        ok = false;
+      if (ok && !wait_bar(sm, kBarBFull + static_cast<int>(x % kBS), (x / kBS) & 1u, p)) ok = false;
+      if (ok) {
+        const uint32_t src = sm.st->pslot[ps] + static_cast<uint32_t>(j) * pw::kTileBytes + pos * 16;
+        const uint32_t bsm = sm.st->bring + (x % kBS) * kBBytes;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t w2[Q][2];
+#pragma unroll
+          for (int q = 0; q < Q; ++q) pw::lds_v2(src + q * (kCt * pw::kTileBytes) + hh * 8, w2[q][0], w2[q][1]);
+#pragma unroll
+          for (int wd = 0; wd < 2; ++wd) {
+            uint32_t ww[Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) ww[q] = w2[q][wd];
+            uint32_t out[16];
+            dq.word(ww, out);
+            // columns 32 * (2 hh + wd) .. + 31 of the tile: atom hh, 64 bytes
+            // from byte 64 wd of each token row
+            const uint32_t xrow = bsm + hh * kBAtom + wd * 64;
+#pragma unroll
+            for (int r = 0; r < kN; ++r) {
+              if (r < u.nrows) {
+                uint32_t xv[16];
+#pragma unroll
+                for (int c4 = 0; c4 < 4; ++c4) {
+                  uint32_t v4[4];
+                  pw::lds_v4u(xrow + r * 128 + c4 * 16, v4);
+#pragma unroll
+                  for (int m = 0; m < 4; ++m) xv[4 * c4 + m] = v4[m];
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const float2 wf = __half22float2(*reinterpret_cast<const __half2*>(&out[i]));
+                  const float2 xf = __half22float2(*reinterpret_cast<const __half2*>(&xv[i]));
+                  gacc[r] = fmaf(wf.x, xf.x, gacc[r]);
+                  gacc[r] = fmaf(wf.y, xf.y, gacc[r]);
+                }
+              }
+            }
+          }
+        }
+        __syncwarp();
+        if (lane == 0) pw::mbar_arrive(bar(sm, kBarTFree + static_cast<int>(x % kF)));   // B slot consumed
+      }
+    }
+    if constexpr (!kGemv) if (has) {
       const uint32_t x = xs + static_cast<uint32_t>(j);
       if (x >= kSA && !wait_bar(sm, kBarTFree + static_cast<int>((x - kSA) % kF), ((x - kSA) / kF) & 1u, p))
         ok = false;
       if (ok) {
         pw::tc_fence_after();
-        const uint32_t acol = tl + (x % kSA) * kATileCols;
+        const uint32_t acol = tl + (x % kSAOr1) * kATileCols;
         const uint32_t src = sm.st->pslot[ps] + static_cast<uint32_t>(j) * pw::kTileBytes + pos * 16;
 #pragma unroll kHalfUnroll
         for (int hh = 0; hh < 2; ++hh) {
@@ -266,6 +338,20 @@ __device__ __forceinline__ bool dequant_unit(const Params& p, const Unit& u, con
     }
     __syncwarp();
     if (lane == 0) pw::mbar_arrive(bar(sm, kBarPFree + ps));   // this warp is done with the chunk
+  }
+  if constexpr (kGemv) {
+    // the set's partial sums (its tiles x = set mod 4) into its accumulator
+    // columns, once the epilogue has read unit ui - 2 from that buffer
+    if (!ok) return false;
+    const uint32_t db = ui & 1u;
+    if (ui >= 2 && !wait_bar(sm, kBarDFree + static_cast<int>(db), ((ui - 2) >> 1) & 1u, p)) return false;
+    const uint32_t v[2] = {__float_as_uint(gacc[0]), __float_as_uint(gacc[(kGemv && kN > 1) ? 1 : 0])};
+    pw::tc_fence_after();
+    pw::tmem_st_x2(tl + acc_col(db, set), v);
+    pw::tmem_st_wait();
+    pw::tc_fence_before();
+    __syncwarp();
+    if (lane == 0) pw::mbar_arrive(bar(sm, kBarDone + static_cast<int>(db)));
   }
   return ok;
 }
@@ -411,9 +497,6 @@ __device__ __forceinline__ void b_loader_role(const Params& p, const Sm sm, cons
 // MMA issuers: issuer k takes the tiles x with x % kIssuers == k and owns its
 // own accumulators
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t acc_col(uint32_t db, int k) {
-  return kDCol0 + (db * kIssuers + static_cast<uint32_t>(k)) * kN;
-}
 
 __device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t tmem, int k) {
   DecState& st = *sm.st;
@@ -431,7 +514,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t 
     if (mu >= 2 && !wait_bar(sm, kBarDFree + static_cast<int>(db), ((mu - 2) >> 1) & 1u, p)) break;
     const uint32_t dcol = tmem + acc_col(db, k);
     bool ok = true, any = false;
-    for (uint32_t x = x0 + ((static_cast<uint32_t>(k) - x0) % kIssuers); x < x0 + nt; x += kIssuers) {
+    for (uint32_t x = x0 + ((static_cast<uint32_t>(k) - x0) % kIssuersOr1); x < x0 + nt; x += kIssuersOr1) {
       const int fs = static_cast<int>(x % kF), b = static_cast<int>(x % kBS);
       // B slot b last held tile x - kBS, which another issuer owns (kIssuers
       // does not divide kBS).  A parity wait only tells the two latest phases
@@ -447,7 +530,7 @@ __device__ __forceinline__ void mma_role(const Params& p, const Sm sm, uint32_t 
         break;
       }
       pw::tc_fence_after();
-      const uint32_t a = tmem + (x % kSA) * kATileCols;
+      const uint32_t a = tmem + (x % kSAOr1) * kATileCols;
       const uint32_t bsm = sm.st->bring + static_cast<uint32_t>(b) * kBBytes;
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -567,7 +650,7 @@ __device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint
   // issuer, so the result does not depend on which CTA took the unit.
   // only the column chunks that hold the unit's tokens (a 64-token tile with
   // a small token group reads one chunk, not four)
-  const int nc16 = min(kN / 16, (u.nrows + 15) / 16);
+  const int nc16 = min(kAccCols / 16, (u.nrows + 15) / 16);
 #pragma unroll 1
   for (int c16 = 0; c16 < nc16; ++c16) {
     float acc[16];
@@ -575,9 +658,9 @@ __device__ __forceinline__ void epilogue_unit(const Params& p, const Sm sm, uint
     for (int n = 0; n < 16; ++n) acc[n] = 0.f;
     if (ok) {
       pw::tc_fence_after();
-      for (int r = 0; r < kIssuers; ++r) {
+      for (int r = 0; r < kAccSlots; ++r) {
         if (static_cast<uint32_t>(r) >= nt) continue;
-        const int k2 = static_cast<int>((static_cast<uint32_t>(r) + x0) % kIssuers);
+        const int k2 = static_cast<int>((static_cast<uint32_t>(r) + x0) % kAccSlots);
         uint32_t v[16];
         pw::tmem_ld_x16(tmem + acc_col(db, k2) + 16u * c16 + (static_cast<uint32_t>(32 * qd) << 16), v);
         pw::tmem_ld_wait();
@@ -746,14 +829,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = p.route_layers, S = p.route_shared;
     const int Tl = p.T / L, ETl = p.E / L;
     const long long Al = static_cast<long long>(Tl) * p.k;
+    uint8_t* scratch = smem_raw + (sm.region - pw::smem_u32(smem_raw));
     for (int l = blockIdx.x; l < L; l += gridDim.x) {
-      pw_route::route_block(p.logits + static_cast<long long>(l) * Tl * (ETl - S), Tl, ETl - S, p.k - S, S,
-                            p.ids_out + l * Al, const_cast<float*>(p.w) + l * Al,
-                            const_cast<int32_t*>(p.offsets) + static_cast<long long>(l) * ETl,
-                            const_cast<int32_t*>(p.perm) + l * Al, const_cast<int32_t*>(p.inv_perm) + l * Al,
-                            p.mass_accum ? p.mass_accum + static_cast<long long>(l) * ETl : nullptr,
-                            smem_raw + (sm.region - pw::smem_u32(smem_raw)), pw::kLutRegionBytes,
-                            static_cast<int>(l * Al));
+      const float* lg = p.logits + static_cast<long long>(l) * Tl * (ETl - S);
+      int32_t* ids = p.ids_out + l * Al;
+      float* w = const_cast<float*>(p.w) + l * Al;
+      int32_t* offsets = const_cast<int32_t*>(p.offsets) + static_cast<long long>(l) * ETl;
+      int32_t* perm = const_cast<int32_t*>(p.perm) + l * Al;
+      int32_t* inv_perm = const_cast<int32_t*>(p.inv_perm) + l * Al;
+      float* mass = p.mass_accum ? p.mass_accum + static_cast<long long>(l) * ETl : nullptr;
+      if (pw_route::warp_routes(Tl, ETl, p.k)) {   // small batch: one warp routes it (same results as the CTA)
+        if (warp == 0)
+          pw_route::route_warp(lg, Tl, ETl - S, p.k - S, S, ids, w, offsets, perm, inv_perm, mass,
+                               reinterpret_cast<float*>(scratch), static_cast<int>(l * Al));
+      } else {
+        pw_route::route_block(lg, Tl, ETl - S, p.k - S, S, ids, w, offsets, perm, inv_perm, mass, scratch,
+                              pw::kLutRegionBytes, static_cast<int>(l * Al));
+      }
       __syncthreads();
       if (threadIdx.x == 0) {
         __threadfence();
@@ -779,7 +871,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int i = 0; i < kF; ++i) {
       pw::mbar_init(bar(sm, kBarAFull + i), 4);
-      pw::mbar_init(bar(sm, kBarTFree + i), 1);
+      pw::mbar_init(bar(sm, kBarTFree + i), kGemv ? 4 : 1);   // a tile's MMAs' commit, or its set's 4 warps
     }
     for (int i = 0; i < kBS; ++i) pw::mbar_init(bar(sm, kBarBFull + i), 1);
     for (int i = 0; i < kPS; ++i) {
@@ -787,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       pw::mbar_init(bar(sm, kBarPFree + i), kDeqWarpsAll);
     }
     for (int i = 0; i < 2; ++i) {
-      pw::mbar_init(bar(sm, kBarDone + i), kIssuers);
+      pw::mbar_init(bar(sm, kBarDone + i), kGemv ? kDeqWarpsAll : kIssuers);
       pw::mbar_init(bar(sm, kBarDFree + i), 4);
       pw::mbar_init(bar(sm, kBarRegReady + i), 1);
     }
@@ -818,7 +910,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (long long v = static_cast<long long>(blockIdx.x) * kThreads + threadIdx.x; v < nvec;
          v += static_cast<long long>(gridDim.x) * kThreads) {
       const int a = static_cast<int>(v / vrow), c = static_cast<int>(v % vrow);
-      const int tok = p.perm[a] / p.k;
+      const int slot = p.perm[a];
+      if (static_cast<unsigned>(slot) >= static_cast<unsigned>(p.A)) {   // not a permutation of the slots
+        report(p.status, PW_ERR_INVALID_ARG);
+        continue;
+      }
+      const int tok = slot / p.k;
       const uint4 val = __ldg(reinterpret_cast<const uint4*>(p.x + static_cast<long long>(tok) * p.H) + c);
       reinterpret_cast<uint4*>(p.xp + static_cast<long long>(a) * p.H)[c] = val;
     }
@@ -836,7 +933,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp < kDeqWarpsAll) {
     dequant_role(p, sm, tmem);
   } else if (warp < kEpiWarp0) {
-    if (lane == 0) mma_role(p, sm, tmem, warp - kMmaWarp0);
+    if constexpr (!kGemv)
+      if (lane == 0) mma_role(p, sm, tmem, warp - kMmaWarp0);
   } else if (warp < kLoadWarp) {
     epilogue_role(p, sm, tmem);
   } else if (warp == kLoadWarp) {
@@ -891,7 +989,8 @@ int encode_rows(CUtensorMap* m, const void* base, long long cols, long long rows
   const cuuint32_t box[2] = {64, kN};
   const cuuint32_t es[2] = {1, 1};
   const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, kGemv ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) return pw::set_error(PW_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
   return PW_OK;

@@ -29,6 +29,13 @@ __global__ void __launch_bounds__(kThreads) route_kernel(const float* __restrict
   // the required part plus room for the weights of up to ~2900 assignments
   __shared__ __align__(16) uint8_t scratch[kScratch];
   const long long l = blockIdx.x, A = static_cast<long long>(T) * (k + S);
+  if (pw_route::warp_routes(T, E + S, k + S)) {   // small batch: one warp, no CTA barrier (same results)
+    if (threadIdx.x < 32)
+      pw_route::route_warp(logits + l * T * E, T, E, k, S, ids + l * A, w + l * A, offsets + l * (E + S),
+                           perm + l * A, inv_perm + l * A, mass_accum ? mass_accum + l * (E + S) : nullptr,
+                           reinterpret_cast<float*>(scratch), static_cast<int>(l * A));
+    return;
+  }
   pw_route::route_block(logits + l * T * E, T, E, k, S, ids + l * A, w + l * A, offsets + l * (E + S), perm + l * A,
                         inv_perm + l * A, mass_accum ? mass_accum + l * (E + S) : nullptr, scratch, kScratch,
                         static_cast<int>(l * A));

@@ -213,4 +213,124 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
   }
 }
 
+// The same routing by one warp, for batches of at most 32 tokens over at most
+// kWarpMaxE experts (routed + shared) with at most kWarpMaxK slots per token:
+// lane t routes token t, counts come from warp ballots, no CTA barrier.  Every result equals route_block's bit for bit:
+// the top-k and weights are the same per-token code, a token's position is
+// its expert's offset plus the number of earlier tokens that chose the
+// expert, and the routing mass is summed in the same order (by position,
+// lane-strided, then the same shuffle tree).  Called by all 32 lanes of one
+// warp; `s_wpos` is T*K floats of shared memory.
+constexpr int kWarpMaxE = 8;
+constexpr int kWarpMaxK = 4;
+__host__ __device__ constexpr bool warp_routes(int T, int ET, int K) {
+  return T <= 32 && ET <= kWarpMaxE && K <= kWarpMaxK;
+}
+__device__ inline void route_warp(const float* __restrict__ logits, int T, int E, int k, int S, int32_t* ids,
+                                  float* w, int32_t* offsets, int32_t* perm, int32_t* inv_perm, float* mass_accum,
+                                  float* s_wpos, int base = 0) {
+  const int K = k + S, ET = E + S;
+  const int t = static_cast<int>(threadIdx.x & 31);
+  const bool valid = t < T;
+  int sel[kWarpMaxK];
+  float wsel[kWarpMaxK];
+#pragma unroll
+  for (int j = 0; j < kWarpMaxK; ++j) {
+    sel[j] = -1;
+    wsel[j] = 0.f;
+  }
+  if (valid) {
+    const float* row = logits + static_cast<long long>(t) * E;
+    float v[kWarpMaxE];
+#pragma unroll
+    for (int e = 0; e < kWarpMaxE; ++e) v[e] = e < E ? __ldg(row + e) : 0.f;
+    float lsel[kWarpMaxK];
+    uint32_t taken = 0u;
+#pragma unroll
+    for (int j = 0; j < kWarpMaxK; ++j) {
+      if (j >= k) break;
+      int best = -1;
+      float lb = 0.f;
+#pragma unroll
+      for (int e = 0; e < kWarpMaxE; ++e) {
+        if (e < E && !((taken >> e) & 1u) && (best < 0 || v[e] > lb)) {
+          best = e;
+          lb = v[e];
+        }
+      }
+      taken |= 1u << best;
+      sel[j] = best;
+      lsel[j] = lb;
+    }
+    float den = 0.f;
+#pragma unroll
+    for (int j = 0; j < kWarpMaxK; ++j)
+      if (j < k) den += expf(lsel[j] - lsel[0]);
+#pragma unroll
+    for (int j = 0; j < kWarpMaxK; ++j) {
+      if (j >= K) break;
+      const bool routed = j < k;
+      sel[j] = routed ? sel[j] : E + (j - k);
+      wsel[j] = routed ? expf(lsel[j] - lsel[0]) / den : 1.0f;
+      ids[static_cast<long long>(t) * K + j] = sel[j];
+      w[static_cast<long long>(t) * K + j] = wsel[j];
+    }
+  }
+  // offsets: an exclusive scan of the per-expert counts (lane e holds expert
+  // e's count and, after the scan, its first position)
+  const unsigned lt_mask = (1u << t) - 1u;
+  int my_cnt = 0, my_off = 0, total = 0;
+  for (int e = 0; e < ET; ++e) {
+    bool mine = false;
+#pragma unroll
+    for (int j = 0; j < kWarpMaxK; ++j) mine |= sel[j] == e;
+    const int c = __popc(__ballot_sync(0xffffffffu, mine));
+    if (t == e) {
+      my_cnt = c;
+      my_off = total;
+    }
+    total += c;
+  }
+  if (t < ET) offsets[t] = base + my_off;
+  if (t == 0) offsets[ET] = base + total;
+  // placement: position = the expert's offset + the earlier tokens that chose
+  // it in any of their slots (a token picks an expert at most once)
+  for (int ee = 0; ee < ET; ++ee) {
+    bool mine = false;
+    int jm = 0;
+    float wm = 0.f;
+#pragma unroll
+    for (int j = 0; j < kWarpMaxK; ++j) {
+      if (j < K && sel[j] == ee) {
+        mine = true;
+        jm = j;
+        wm = wsel[j];
+      }
+    }
+    const unsigned ball = __ballot_sync(0xffffffffu, mine);
+    const int off_e = __shfl_sync(0xffffffffu, my_off, ee);
+    if (mine) {
+      const int pos = off_e + __popc(ball & lt_mask);
+      const int slot = t * K + jm;
+      perm[pos] = base + slot;
+      inv_perm[slot] = base + pos;
+      s_wpos[pos] = wm;
+    }
+  }
+  __syncwarp();
+  // Eq. 1 numerator: per expert, the weights in position order, lane-strided,
+  // then the shuffle tree (route_block's order)
+  if (mass_accum) {
+    for (int e = 0; e < ET; ++e) {
+      const int o0 = __shfl_sync(0xffffffffu, my_off, e), n = __shfl_sync(0xffffffffu, my_cnt, e);
+      float acc = 0.f;
+      for (int pos = o0 + t; pos < o0 + n; pos += 32) acc += s_wpos[pos];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+      if (t == 0) atomicAdd(&mass_accum[e], acc);
+    }
+  }
+  (void)my_cnt;
+}
+
 }  // namespace pw_route

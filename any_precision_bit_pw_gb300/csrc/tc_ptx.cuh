@@ -247,6 +247,10 @@ __device__ __forceinline__ void tmem_ld_x4(uint32_t taddr, uint32_t (&v)[4]) {
                : "r"(taddr)
                : "memory");
 }
+// 32 lanes x 2 consecutive columns.
+__device__ __forceinline__ void tmem_st_x2(uint32_t taddr, const uint32_t (&v)[2]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(v[0]), "r"(v[1]) : "memory");
+}
 // 32 lanes x 16 consecutive columns.
 __device__ __forceinline__ void tmem_st_x16(uint32_t taddr, const uint32_t (&v)[16]) {
   asm volatile(

@@ -33,6 +33,7 @@ def PW_PAGE_LUT(b: int) -> int:
 PW_LAYOUT_TILED = 1
 PW_MAX_BITS = 8
 PW_PATH_AUTO, PW_PATH_DECODE, PW_PATH_PREFILL = 0, 1, 2
+PW_KERNEL_AUTO, PW_KERNEL_TENSOR, PW_KERNEL_CUDA_CORES = 0, 1, 2
 PW_FFN_FLAG_TEST_DROP_ONE_ARRIVAL = 1
 PW_FFN_FLAG_STRIP_COMBINE = 2
 
@@ -66,7 +67,7 @@ class pw_block_info(ctypes.Structure):
 
 class pw_ffn_options(ctypes.Structure):
     _fields_ = [("path", ctypes.c_int32), ("flags", ctypes.c_uint32), ("wait_timeout_us", ctypes.c_uint32),
-                ("shared_experts", ctypes.c_int32), ("reserved", ctypes.c_int32 * 4)]
+                ("shared_experts", ctypes.c_int32), ("kernel", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
 
 
 _lib: Optional[ctypes.CDLL] = None

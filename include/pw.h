@@ -334,12 +334,26 @@ int pw_moe_apl_ffn_noalloc(const void* d_desc, int layer, const uint16_t* d_x, i
                                                  that strip, instead of the whole
                                                  grid combining after the last
                                                  unit (same result, bit for bit) */
+/* Which units multiply the dequantised weights with the tokens:
+ *  PW_KERNEL_AUTO         the library's choice (the tensor cores: measured
+ *                         faster at every batch size, see below);
+ *  PW_KERNEL_TENSOR       tcgen05 MMAs on 16-, 64- or 128-token tiles;
+ *  PW_KERNEL_CUDA_CORES   fp32 FMAs in the dequantising warps on 2-token
+ *                         tiles (a split-K GEMV: every unit sums its rows
+ *                         over its K range per set of warps; meant for one or
+ *                         two tokens per expert, correct for any batch).
+ * Results agree within the output tolerance, not bit for bit (the two sum
+ * the products in different orders). */
+#define PW_KERNEL_AUTO 0
+#define PW_KERNEL_TENSOR 1
+#define PW_KERNEL_CUDA_CORES 2
 typedef struct pw_ffn_options {
   int32_t path;              /* PW_PATH_* */
   uint32_t flags;            /* PW_FFN_FLAG_* */
   uint32_t wait_timeout_us;  /* bound of each in-kernel wait; 0 = 2 s */
   int32_t shared_experts;    /* routed call only: S shared experts (see pw_moe_route_topk_shared) */
-  int32_t reserved[4];
+  int32_t kernel;            /* PW_KERNEL_* */
+  int32_t reserved[3];
 } pw_ffn_options;
 
 int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T, int H, int I,
@@ -417,7 +431,8 @@ int pw_unpack_indices(const pw_page_table* t, int block, int b, uint8_t* d_idx_o
 
 /* out[m][n] = sum_j W[n][j] * x[m][j], W = LUT_q[n][idx_q[n][j]] of `block`
  * at its committed bitwidth q (2..8): d_x fp16 [M][cols], d_out fp32
- * [M][rows], fp32 accumulation.  M >= 0.  Its work-ticket counter is one
+ * [M][rows], fp32 accumulation.  M >= 0; M <= 2 runs on the CUDA-core
+ * instance of the fused kernel, larger M on its tensor-core instances.  Its work-ticket counter is one
  * array inside the library, zeroed by each call: calls that overlap on the
  * GPU (different streams without ordering) race.  Serialise them. */
 int pw_apl_linear(const pw_page_table* t, int block, const uint16_t* d_x, int M,

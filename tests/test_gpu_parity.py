@@ -120,7 +120,8 @@ def test_apl_linear_matches_oracle(q, N, K, M):
         pw.pw_page_table_destroy(t)
 
 
-@pytest.mark.parametrize("q,N,K,M", [(8, 128, 512, 5), (3, 256, 768, 40), (5, 128, 4096, 3), (2, 128, 128, 17)])
+@pytest.mark.parametrize("q,N,K,M", [(8, 128, 512, 5), (3, 256, 768, 40), (5, 128, 4096, 3), (2, 128, 128, 17),
+                                     (6, 256, 512, 2), (4, 128, 384, 1), (8, 384, 1024, 200)])
 def test_apl_linear_identity_lut_is_exact(q, N, K, M):
     """LUT_q[n][c] = c and integer x: the GPU result equals the integer matmul
     of the q-bit indices exactly (every partial sum is an integer < 2^24)."""
@@ -158,6 +159,8 @@ def _route_gpu(logits, k):
 
 
 @pytest.mark.parametrize("T,E,k,kind", [(16, 4, 2, "normal"), (32, 8, 2, "normal"), (1, 8, 2, "normal"),
+                                        (32, 8, 4, "normal"), (7, 3, 3, "normal"), (32, 4, 2, "ties"),
+                                        (31, 8, 2, "ties"), (33, 8, 2, "normal"),
                                         (4096, 8, 2, "zipf"), (2500, 8, 2, "ties"), (3000, 64, 4, "normal"),
                                         (256, 8, 2, "uniform"), (5, 256, 8, "normal")])
 def test_route_matches_oracle(T, E, k, kind):
@@ -178,6 +181,55 @@ def test_route_matches_oracle(T, E, k, kind):
     assert np.array_equal(got["inv_perm"], ref["inv_perm"])
     np.testing.assert_allclose(got["w"], ref["w"], atol=1e-6, rtol=0)
     np.testing.assert_allclose(got["mass"] / max(T, 1), ref["mass"], atol=1e-5, rtol=0)
+
+
+def test_route_small_batches_many_seeds():
+    """Batches of up to 32 tokens over up to 8 experts are routed by one warp
+    (ballots instead of a CTA-wide counting sort): every output against the
+    oracle over many seeds, tied logits included."""
+    for seed in range(40):
+        g = torch.Generator().manual_seed(1000 + seed)
+        T = 1 + seed % 32
+        E = 2 + seed % 7
+        k = 1 + seed % min(E, 4)
+        logits = torch.randn((T, E), generator=g)
+        if seed % 2:
+            logits = torch.round(logits * 2) / 2
+        got = _route_gpu(logits, k)
+        ref = apl.route_topk(logits.numpy(), k)
+        for key in ("ids", "offsets", "perm", "inv_perm"):
+            assert np.array_equal(got[key], ref[key]), (seed, key)
+        np.testing.assert_allclose(got["w"], ref["w"], atol=1e-6, rtol=0)
+
+
+def test_ffn_rejects_routing_arrays_that_are_not_a_permutation():
+    """The unrouted call takes the routing arrays from the caller: an entry
+    outside the assignment slots, or offsets that do not run from 0 to T*k,
+    set PW_ERR_INVALID_ARG (the kernel's own checks skip the bad entries) and
+    the context stays usable."""
+    li = synth.layer_inputs(synth.TINY_LAYER)
+    sh = li.wl.shape
+    y, status, call, stack = _run_gpu(li)
+    assert status == 0
+    r = call.route
+    A = li.wl.tokens * sh.top_k
+    for what in ("perm", "inv_perm", "offsets"):
+        perm, inv, off = r.perm.clone(), r.inv_perm.clone(), r.offsets.clone()
+        if what == "perm":
+            perm[3] = A + 7
+        elif what == "inv_perm":
+            inv[5] = -2
+        else:
+            off[-1] = A + 16
+        call.status.zero_()
+        pw.pw_moe_apl_ffn(stack.desc, 0, li.x.to(DEV), sh.intermediate, sh.experts, sh.top_k, r.ids, r.w, off, perm,
+                          inv, call.ws, call.y, call.status)
+        torch.cuda.synchronize()
+        assert int(call.status.item()) == pw.PW_ERR_INVALID_ARG, what
+    call.status.zero_()
+    y2 = call(0, li.x.to(DEV), li.logits.to(DEV)).float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(call.status.item()) == 0 and np.array_equal(y, y2)
 
 
 def test_route_zero_tokens():
@@ -422,3 +474,61 @@ def test_ffn_mixtral_8x22b_prefill():
     r = _check_rows(li, y, toks)
     assert np.array_equal(r_ids, r["ids"])
     assert np.array_equal(call.route.perm.cpu().numpy(), r["perm"])
+
+
+# ---------------------------------------------------------------------------
+# the CUDA-core instance (PW_KERNEL_CUDA_CORES): a split-K GEMV per unit
+# ---------------------------------------------------------------------------
+def _opts_cuda_cores(path=None):
+    o = pw.pw_ffn_options()
+    o.kernel = pw.PW_KERNEL_CUDA_CORES
+    if path is not None:
+        o.path = path
+    return o
+
+
+@pytest.mark.parametrize("path", [pw.PW_PATH_DECODE, pw.PW_PATH_PREFILL])
+def test_cuda_core_kernel_tiny(path):
+    li = synth.layer_inputs(synth.TINY_LAYER)
+    y, status, call, _ = _run_gpu(li, options=_opts_cuda_cores(path))
+    assert status == 0
+    y_ref, r = _oracle_y(li, from_planes=True)
+    assert np.array_equal(call.route.ids.cpu().numpy(), r["ids"])
+    _assert_close(y_ref, y)
+
+
+@pytest.mark.parametrize("b,T", [(3, 1), (8, 1), (5, 4), (3, 8)])
+def test_cuda_core_kernel_mixtral_sweep_points(b, T):
+    """Small decode batches of the 8x7B layer (one or two tokens per expert)
+    on the CUDA cores, every token against the oracle."""
+    wl = synth.MIXTRAL_8X7B_SWEEP.with_(fixed_bits=b, tokens=T)
+    li = synth.layer_inputs(wl, device=DEV, lut_bits=range(wl.seed_bits, b + 1))
+    y, status, _, _ = _run_gpu(li, options=_opts_cuda_cores())
+    assert status == 0
+    _check_rows(li, y, list(range(T)))
+
+
+def test_cuda_core_kernel_mixed_bits_skewed_groups():
+    """The decode layer with mixed bitwidths (up to ~14 tokens per expert, so
+    many 2-token units per expert) on the CUDA cores; repeated calls return
+    the same bits."""
+    wl = synth.MIXTRAL_8X7B_DECODE
+    li = synth.layer_inputs(wl, device=DEV)
+    y, status, call, _ = _run_gpu(li, options=_opts_cuda_cores())
+    assert status == 0
+    y2 = call(0, li.x, li.logits, options=_opts_cuda_cores()).float().cpu().numpy()
+    torch.cuda.synchronize()
+    assert int(call.status.item()) == 0 and np.array_equal(y, y2)
+    _check_rows(li, y, list(range(wl.tokens)))
+
+
+@pytest.mark.parametrize("H,I,E,k,T,bits", [(256, 2304, 3, 1, 9, (6, 3)), (128, 6272, 2, 2, 3, (3, 4)),
+                                           (384, 640, 2, 2, 7, (5, 4))])
+def test_cuda_core_kernel_edge_shapes(H, I, E, k, T, bits):
+    wl = synth.Workload("edge", synth.MoEShape(H, I, E, k), tokens=T, parent_bits=8, seed_bits=2, seed=H + I + T,
+                        bits_mode="uniform_choice", bits_choices=bits)
+    li = synth.layer_inputs(wl)
+    y, status, _, _ = _run_gpu(li, options=_opts_cuda_cores())
+    assert status == 0
+    y_ref, _ = _oracle_y(li)
+    _assert_close(y_ref, y)
