@@ -84,6 +84,24 @@ def test_noalloc_matches_workspace_entry_point_twice(wl):
             assert m["rel_l2"] <= REL_L2 and m["max_abs_over_rms"] <= MAX_ABS_OVER_RMS, (step, m)
 
 
+def test_noalloc_on_the_prefill_path_of_the_8x7b_layer():
+    """192 tokens of the 8x7B shape take the prefill path (48 assignments per
+    expert), whose workspace fits the array although the decode path's would
+    not: the call runs and equals the caller-workspace call bit for bit."""
+    wl = synth.MIXTRAL_8X7B_DECODE.with_(tokens=192)
+    sh = wl.shape
+    li = synth.layer_inputs(wl, device=DEV)
+    stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, wl.parent_bits, wl.seed_bits, DEV)
+    load_layer(stack, 0, li)
+    stack.sync()
+    call = MoECall(stack, wl.tokens)
+    y_ref = call(0, li.x, li.logits).float().cpu().numpy()
+    y, status = _noalloc(call, stack, li.x)
+    torch.cuda.synchronize()
+    assert int(call.status.item()) == 0 and int(status.item()) == 0
+    assert np.array_equal(y_ref, y[: wl.tokens].float().cpu().numpy())
+
+
 def test_noalloc_rejects_calls_beyond_its_scratch():
     # 8x7B shape at 512 tokens needs far more than the 32 MiB array
     assert pw.pw_moe_apl_ffn_workspace(512, 4096, 14336, 8, 2) > pw.PW_NOALLOC_SCRATCH_BYTES
