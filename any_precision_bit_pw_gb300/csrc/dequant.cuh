@@ -62,6 +62,24 @@ __device__ __forceinline__ uint32_t nibble_sel(const uint32_t* w, int js) {
   return s;
 }
 
+// 4x4 bit-matrix transpose inside every nibble of four words (two rounds of
+// delta swaps): afterwards bit c of nibble n of L[i] holds what was bit i of
+// nibble n of L[c].
+__device__ __forceinline__ void transpose4x4(uint32_t (&L)[4]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint32_t a = L[i], b = L[i + 2];
+    L[i] = (a & 0x33333333u) | (shl_mul(b, 2) & 0xCCCCCCCCu);
+    L[i + 2] = (shr_mul(a, 2) & 0x33333333u) | (b & 0xCCCCCCCCu);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; i += 2) {
+    const uint32_t a = L[i], b = L[i + 1];
+    L[i] = (a & 0x55555555u) | (shl_mul(b, 1) & 0xAAAAAAAAu);
+    L[i + 1] = (shr_mul(a, 1) & 0x55555555u) | (b & 0xAAAAAAAAu);
+  }
+}
+
 template <int Q, bool kInRegs = (Q <= 4)>
 struct RowDequant;
 
@@ -119,11 +137,24 @@ struct RowDequant<Q, true> {
 
   // ww[p]: one 32-column word of plane p -> 16 fp16 pairs (columns in order).
   __device__ __forceinline__ void word(const uint32_t (&ww)[Q], uint32_t (&out)[16]) const {
+    if constexpr (Q == 3) {
+      // the selectors of all four sub-blocks at once: after a 4x4 transpose
+      // inside nibbles, nibble e of L[js] is the index of column 8*js + e
+      // (bit 3 zero: prmt's plain byte mode)
+      uint32_t L[4] = {ww[2], ww[1], ww[0], 0u};
+      transpose4x4(L);
 #pragma unroll
-    for (int js = 0; js < 4; ++js) {
-      const uint32_t s = nibble_sel<0, Q>(ww, js);
-      quad(s, out[4 * js], out[4 * js + 1]);
-      quad(s >> 16, out[4 * js + 2], out[4 * js + 3]);
+      for (int js = 0; js < 4; ++js) {
+        quad(L[js], out[4 * js], out[4 * js + 1]);
+        quad(L[js] >> 16, out[4 * js + 2], out[4 * js + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int js = 0; js < 4; ++js) {
+        const uint32_t s = nibble_sel<0, Q>(ww, js);
+        quad(s, out[4 * js], out[4 * js + 1]);
+        quad(s >> 16, out[4 * js + 2], out[4 * js + 3]);
+      }
     }
   }
 };
@@ -154,24 +185,6 @@ __device__ __forceinline__ void transpose8x8(uint32_t (&X)[8]) {
     const uint32_t a = X[i], b = X[i + 1];
     X[i] = (a & 0x55555555u) | (shl_mul(b, 1) & 0xAAAAAAAAu);
     X[i + 1] = (shr_mul(a, 1) & 0x55555555u) | (b & 0xAAAAAAAAu);
-  }
-}
-
-// 4x4 bit-matrix transpose inside every nibble of four words (two rounds of
-// delta swaps): afterwards bit c of nibble n of L[i] holds what was bit i of
-// nibble n of L[c].
-__device__ __forceinline__ void transpose4x4(uint32_t (&L)[4]) {
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-    const uint32_t a = L[i], b = L[i + 2];
-    L[i] = (a & 0x33333333u) | (shl_mul(b, 2) & 0xCCCCCCCCu);
-    L[i + 2] = (shr_mul(a, 2) & 0x33333333u) | (b & 0xCCCCCCCCu);
-  }
-#pragma unroll
-  for (int i = 0; i < 4; i += 2) {
-    const uint32_t a = L[i], b = L[i + 1];
-    L[i] = (a & 0x55555555u) | (shl_mul(b, 1) & 0xAAAAAAAAu);
-    L[i + 1] = (shr_mul(a, 1) & 0x55555555u) | (b & 0xAAAAAAAAu);
   }
 }
 

@@ -167,6 +167,22 @@ __device__ void setup_schedule(const Params& p, Shared& sh) {
   sh.arrivals_per_strip = arr;
 }
 
+// Strip and token group of the r-th unit of a block of `strips` strips x
+// `groups` token groups: tickets run through blocks of kStripRun strips, token
+// group by token group, so a strip's planes and LUT are read again by its next
+// token group about kStripRun units later, while they are still in L2 (32
+// strips of 8-bit planes at K = 16384 are 64 MB), and not at the same time by
+// neighbouring CTAs.
+constexpr int kStripRun = 32;
+__device__ __forceinline__ void strip_group(int r, int strips, int groups, int& strip, int& tg) {
+  const int run = r / (kStripRun * groups);
+  const int first = run * kStripRun;
+  const int n = min(kStripRun, strips - first);
+  const int w = r - first * groups;
+  tg = w / n;
+  strip = first + w % n;
+}
+
 // Fetch and decode the next unit into sh.u (thread 0 only).
 template <int NMAX>
 __device__ void next_unit(const Params& p, Shared& sh) {
@@ -183,8 +199,7 @@ __device__ void next_unit(const Params& p, Shared& sh) {
     const int strips = d.rows / 128, groups = (p.M + NMAX - 1) / NMAX;
     if (t < static_cast<uint32_t>(strips * groups)) {
       u.kind = kLinear;
-      u.strip = static_cast<int>(t % strips);
-      u.tg = static_cast<int>(t / strips);
+      strip_group(static_cast<int>(t), strips, groups, u.strip, u.tg);
       u.off = 0;
       u.nrows = min(NMAX, p.M - u.tg * NMAX);
       u.npad = ((u.nrows + 15) / 16) * 16;
@@ -204,8 +219,7 @@ __device__ void next_unit(const Params& p, Shared& sh) {
     const int rem = static_cast<int>(t) - sh.cum_gu[ai];
     u.kind = kGateUp;
     u.e = sh.act[ai];
-    u.strip = rem % gu_strips;
-    u.tg = rem / gu_strips;
+    strip_group(rem, gu_strips, sh.ntg[ai], u.strip, u.tg);
     u.split = (u.strip * 64) / p.split_cols;
     u.d = p.desc + 2 * u.e;
     u.st0 = 0;
@@ -219,8 +233,7 @@ __device__ void next_unit(const Params& p, Shared& sh) {
     const int per_split = dn_strips * sh.ntg[ai];
     u.split = rem / per_split;
     const int r2 = rem % per_split;
-    u.strip = r2 % dn_strips;
-    u.tg = r2 / dn_strips;
+    strip_group(r2, dn_strips, sh.ntg[ai], u.strip, u.tg);
     u.d = p.desc + 2 * u.e + 1;
     const int c0 = u.split * p.split_cols;
     u.st0 = c0 / pw::kStageK;

@@ -524,7 +524,9 @@ def stack_arm(args, rank, world, local_rank):
                    "l2": "no flush: the planes read per step (%.1f GB) exceed the 129 MB L2" % (nbytes.sum() / K / 1e9)},
         "roofline": roofline,
         "e2e": {"value": T / (e2e_ms * 1e-3), "unit": UNIT,
-                "h2d_bytes_per_step": L * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": L * T * H * 2},
+                "h2d_bytes_per_step": L * (T * H * 2 + T * E * 4), "d2h_bytes_per_step": L * T * H * 2,
+                "steps": K2, "bits": "those of the schedule's last commit (after the timed steps), without "
+                                    "step boundaries: fewer plane bytes per step than the timed steps' mean"},
         "gpu_launches": (1 if routed else 2) * (1 if batched else L) * K,
         "clocks": clk.summary(),
         "status": status,
