@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "ffn_common.cuh"
+#include "route_block.cuh"
 
 namespace {
 
@@ -179,9 +180,10 @@ int ffn_launch(bool routed, const void* d_desc, int layer, int L, const uint16_t
   p.wait_ns = (o.wait_timeout_us ? o.wait_timeout_us : 2000000u) * 1000ull;
   p.flags = o.flags;
   p.linear = 0;
-  if (routed && path == PW_PATH_PREFILL) {
-    // large batches: one CTA would route while the grid waits; a separate
-    // routing launch comes first instead
+  if (routed && (path == PW_PATH_PREFILL || !pw_route::warp_routes(T1, E1, k))) {
+    // batches that one warp does not route (more than 32 tokens or 8 experts
+    // per layer): a routing launch comes first, so that the fused kernel
+    // holds no CTA-wide routing code and its grid does not wait on one CTA
     if (int e = pw::route_layers(d_logits, L, T1, ER, kR, S, d_ids, const_cast<float*>(d_w),
                                  const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
                                  const_cast<int32_t*>(d_inv_perm), d_mass_accum, s))

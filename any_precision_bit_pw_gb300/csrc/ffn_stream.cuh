@@ -819,32 +819,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   DecState& st = *sm.st;
-  // routed call: CTA l routes layer l of the route_layers layers (one layer:
-  // CTA 0 routes the batch; the LUT region is the scratch: the pipeline has
-  // not started), writing the routing arrays of all layers in one
-  // concatenated index space, and counts the layer as published; every CTA
-  // waits for all of them before it schedules or gathers (all CTAs are
-  // resident: one per SM)
+  // routed call (batches one warp routes: at most 32 tokens and 8 experts
+  // per layer; the host routes larger ones in a launch before this one):
+  // warp 0 of CTA l routes layer l of the route_layers layers, writing the
+  // routing arrays of all layers in one concatenated index space (the LUT
+  // region is its scratch: the pipeline has not started), and counts the
+  // layer as published; every CTA waits for all of them before it schedules
+  // or gathers (all CTAs are resident: one per SM)
   if (p.logits) {
     const int L = p.route_layers, S = p.route_shared;
     const int Tl = p.T / L, ETl = p.E / L;
     const long long Al = static_cast<long long>(Tl) * p.k;
-    uint8_t* scratch = smem_raw + (sm.region - pw::smem_u32(smem_raw));
+    float* scratch = reinterpret_cast<float*>(smem_raw + (sm.region - pw::smem_u32(smem_raw)));
     for (int l = blockIdx.x; l < L; l += gridDim.x) {
-      const float* lg = p.logits + static_cast<long long>(l) * Tl * (ETl - S);
-      int32_t* ids = p.ids_out + l * Al;
-      float* w = const_cast<float*>(p.w) + l * Al;
-      int32_t* offsets = const_cast<int32_t*>(p.offsets) + static_cast<long long>(l) * ETl;
-      int32_t* perm = const_cast<int32_t*>(p.perm) + l * Al;
-      int32_t* inv_perm = const_cast<int32_t*>(p.inv_perm) + l * Al;
-      float* mass = p.mass_accum ? p.mass_accum + static_cast<long long>(l) * ETl : nullptr;
-      if (pw_route::warp_routes(Tl, ETl, p.k)) {   // small batch: one warp routes it (same results as the CTA)
-        if (warp == 0)
-          pw_route::route_warp(lg, Tl, ETl - S, p.k - S, S, ids, w, offsets, perm, inv_perm, mass,
-                               reinterpret_cast<float*>(scratch), static_cast<int>(l * Al));
-      } else {
-        pw_route::route_block(lg, Tl, ETl - S, p.k - S, S, ids, w, offsets, perm, inv_perm, mass, scratch,
-                              pw::kLutRegionBytes, static_cast<int>(l * Al));
+      if (warp == 0) {
+        if (pw_route::warp_routes(Tl, ETl, p.k)) {
+          pw_route::route_warp(p.logits + static_cast<long long>(l) * Tl * (ETl - S), Tl, ETl - S, p.k - S, S,
+                               p.ids_out + l * Al, const_cast<float*>(p.w) + l * Al,
+                               const_cast<int32_t*>(p.offsets) + static_cast<long long>(l) * ETl,
+                               const_cast<int32_t*>(p.perm) + l * Al, const_cast<int32_t*>(p.inv_perm) + l * Al,
+                               p.mass_accum ? p.mass_accum + static_cast<long long>(l) * ETl : nullptr, scratch,
+                               static_cast<int>(l * Al));
+        } else if (lane == 0) {
+          report(p.status, PW_ERR_INVALID_ARG);   // the host routes such batches before the launch
+        }
       }
       __syncthreads();
       if (threadIdx.x == 0) {

@@ -13,7 +13,7 @@
 
 namespace {
 
-constexpr int kThreads = 1024;
+constexpr int kThreads = 512;   // 128 registers a thread: the routing code does not spill
 constexpr int kWarps = kThreads / 32;
 using pw_route::kMaxE;
 using pw_route::kMaxK;
@@ -26,7 +26,7 @@ __global__ void __launch_bounds__(kThreads) route_kernel(const float* __restrict
                                                          int32_t* __restrict__ ids, float* __restrict__ w,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
                                                          int32_t* __restrict__ inv_perm, float* __restrict__ mass_accum) {
-  // the required part plus room for the weights of up to ~2900 assignments
+  // the required part plus room for the weights of up to ~3400 assignments
   __shared__ __align__(16) uint8_t scratch[kScratch];
   const long long l = blockIdx.x, A = static_cast<long long>(T) * (k + S);
   if (pw_route::warp_routes(T, E + S, k + S)) {   // small batch: one warp, no CTA barrier (same results)

@@ -58,57 +58,33 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
 
   // 1) top-k per token: largest logit first, ties to the lower expert index;
   //    weights = softmax renormalised over the picks = exp(l_j - l_max) / sum.
-  //    Up to 32 experts the row is loaded into registers first (independent
-  //    loads, one memory latency per token instead of one per logit).  When
-  //    the batch fits one pass, each thread keeps its picks for step 3.
-  const bool one_pass = T <= nthreads;
-  int keep[kMaxK];
-#pragma unroll
-  for (int j = 0; j < kMaxK; ++j) keep[j] = -1;
-  for (int t = tid; t < T; t += nthreads) {
+  //    Up to 32 experts one thread takes a token and loads its row into
+  //    registers first (independent loads, one memory latency per token
+  //    instead of one per logit); above 32 experts one warp takes a token
+  //    (step 1b).  Step 3 reads the picks back from ids.
+  for (int t = tid; t < T && E <= 32; t += nthreads) {
     const float* row = logits + static_cast<long long>(t) * E;
     int sel[kMaxK];
     float lsel[kMaxK];
-    if (E <= 32) {
-      float v[32];
+    float v[32];
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = e < E ? __ldg(row + e) : 0.f;
-      uint32_t taken = 0u;
+    for (int e = 0; e < 32; ++e) v[e] = e < E ? __ldg(row + e) : 0.f;
+    uint32_t taken = 0u;
 #pragma unroll
-      for (int j = 0; j < kMaxK; ++j) {
-        if (j >= k) break;
-        int best = -1;
-        float lb = 0.f;
+    for (int j = 0; j < kMaxK; ++j) {
+      if (j >= k) break;
+      int best = -1;
+      float lb = 0.f;
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if (e < E && !((taken >> e) & 1u) && (best < 0 || v[e] > lb)) {
-            best = e;
-            lb = v[e];
-          }
+      for (int e = 0; e < 32; ++e) {
+        if (e < E && !((taken >> e) & 1u) && (best < 0 || v[e] > lb)) {
+          best = e;
+          lb = v[e];
         }
-        taken |= 1u << best;
-        sel[j] = best;
-        lsel[j] = lb;
       }
-    } else {
-      uint32_t taken[kMaxE / 32];
-#pragma unroll
-      for (int i = 0; i < kMaxE / 32; ++i) taken[i] = 0u;
-      for (int j = 0; j < k; ++j) {
-        int best = -1;
-        float lb = 0.f;
-        for (int e = 0; e < E; ++e) {
-          if ((taken[e >> 5] >> (e & 31)) & 1u) continue;
-          const float v = __ldg(row + e);
-          if (best < 0 || v > lb) {
-            best = e;
-            lb = v;
-          }
-        }
-        taken[best >> 5] |= 1u << (best & 31);
-        sel[j] = best;
-        lsel[j] = lb;
-      }
+      taken |= 1u << best;
+      sel[j] = best;
+      lsel[j] = lb;
     }
     float den = 0.f;
 #pragma unroll
@@ -124,7 +100,59 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
       w[static_cast<long long>(t) * K + j] = wj;
       if (wpos_smem) s_wslot[static_cast<long long>(t) * K + j] = wj;
       atomicAdd(&s_cnt[e], 1);
-      keep[j] = e;
+    }
+  }
+  // 1b) more than 32 experts: one warp per token, lane l holding logits
+  //     l, l + 32, ...; each pick is a warp arg-max under the order of the
+  //     scan above (larger logit, then the lower expert index), taken from
+  //     lane 0 so that every lane agrees.  Lane j keeps pick j and writes
+  //     slot j; the denominator is summed in pick order, as above.
+  for (int t = warp; t < T && E > 32; t += nwarps) {
+    const float* row = logits + static_cast<long long>(t) * E;
+    float v[kMaxE / 32];
+#pragma unroll
+    for (int i = 0; i < kMaxE / 32; ++i) v[i] = lane + 32 * i < E ? __ldg(row + lane + 32 * i) : 0.f;
+    uint32_t taken = 0u;   // bit i: expert lane + 32 i already picked
+    int my_e = -1;
+    float my_l = 0.f, l0 = 0.f, den = 0.f;
+    for (int j = 0; j < k; ++j) {
+      int best = -1;
+      float lb = 0.f;
+#pragma unroll
+      for (int i = 0; i < kMaxE / 32; ++i) {
+        if (lane + 32 * i < E && !((taken >> i) & 1u) && (best < 0 || v[i] > lb)) {
+          best = lane + 32 * i;
+          lb = v[i];
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const int ob = __shfl_xor_sync(0xffffffffu, best, o);
+        const float ol = __shfl_xor_sync(0xffffffffu, lb, o);
+        if (ob >= 0 && (best < 0 || ol > lb || (ol == lb && ob < best))) {
+          best = ob;
+          lb = ol;
+        }
+      }
+      best = __shfl_sync(0xffffffffu, best, 0);
+      lb = __shfl_sync(0xffffffffu, lb, 0);
+      if ((best & 31) == lane) taken |= 1u << (best >> 5);
+      if (j == 0) l0 = lb;
+      den += expf(lb - l0);
+      if (lane == j) {
+        my_e = best;
+        my_l = lb;
+      }
+    }
+    if (lane < K) {
+      const int j = lane;
+      const bool routed = j < k;
+      const int e = routed ? my_e : E + (j - k);
+      const float wj = routed ? expf(my_l - l0) / den : 1.0f;
+      ids[static_cast<long long>(t) * K + j] = e;
+      w[static_cast<long long>(t) * K + j] = wj;
+      if (wpos_smem) s_wslot[static_cast<long long>(t) * K + j] = wj;
+      atomicAdd(&s_cnt[e], 1);
     }
   }
   __syncthreads();
@@ -154,7 +182,7 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
     int rank[kMaxK];
 #pragma unroll
     for (int j = 0; j < kMaxK; ++j) {
-      my[j] = (valid && j < K) ? (one_pass ? keep[j] : ids[static_cast<long long>(t) * K + j]) : -1;
+      my[j] = (valid && j < K) ? ids[static_cast<long long>(t) * K + j] : -1;
       rank[j] = 0;
     }
     const unsigned lt_mask = (1u << lane) - 1u;

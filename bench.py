@@ -116,8 +116,15 @@ def ffn_kernel(tokens: int, top_k: int, experts: int) -> str:
 
 
 def prefill_path(tokens: int, top_k: int, experts: int) -> bool:
-    """The library's path choice: routing is a launch of its own on the prefill path."""
+    """The library's path choice between the decode and prefill layouts."""
     return tokens * top_k >= 48 * experts
+
+
+def kernel_routes(tokens: int, top_k: int, experts: int) -> bool:
+    """Whether a routed call routes inside the fused launch (one warp: at most
+    32 tokens, 8 experts and 4 slots per token, on the decode path); other
+    batches get a routing launch of their own first."""
+    return not prefill_path(tokens, top_k, experts) and tokens <= 32 and experts <= 8 and top_k <= 4
 
 
 KERNEL_TILE = {"apl_ffn_t16_kernel": 16, "apl_ffn_t64_kernel": 64, "apl_ffn_t128_kernel": 128}
@@ -272,7 +279,7 @@ def gpu_arm(args, rank, world, local_rank):
     call = MoECall(stack, wl.tokens)
     stream = torch.cuda.current_stream()
     kname = ffn_kernel(wl.tokens, sh.top_k + sh.shared, sh.total_experts)
-    routed = not prefill_path(wl.tokens, sh.top_k + sh.shared, sh.total_experts)
+    routed = kernel_routes(wl.tokens, sh.top_k + sh.shared, sh.total_experts)
 
     # routing of each batch (for the algorithmic byte count)
     bytes_per_batch = []
@@ -342,7 +349,7 @@ def gpu_arm(args, rank, world, local_rank):
     ffn_avg_ms = float(np.mean(ffn_ms))
     achieved = mean_bytes / (ffn_avg_ms * 1e-3) / 1e9
     peak, peak_kind = _peaks()
-    prefill = not routed
+    prefill = prefill_path(wl.tokens, sh.top_k + sh.shared, sh.total_experts)
     hbm_roof = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": measured_traffic(kname, wl.name, wl.tokens),
                 "traffic_unit": "bytes per launch (ncu dram__bytes_read.sum + dram__bytes_write.sum)",
@@ -407,7 +414,7 @@ def stack_arm(args, rank, world, local_rank):
         lgs_b = [torch.stack(lgs[s]).contiguous() for s in range(n_in)]
     call, stack = run.call, run.stack
     stream = torch.cuda.current_stream()
-    routed = not prefill_path(T, sh.top_k, E)
+    routed = kernel_routes(T, sh.top_k, E)
 
     # warm-up: the layer calls without step boundaries (no commits, no mass)
     for i in range(args.warmup):
@@ -504,7 +511,9 @@ def stack_arm(args, rank, world, local_rank):
     per_launch = nbytes.sum(axis=1) if batched else nbytes.reshape(-1)
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                 "traffic": None, "kernel": kernel_label(ffn_kernel(T, sh.top_k, E)),
-                "launch": "all layers of a step in one launch" if batched else "one launch per layer",
+                "launch": (("all layers of a step in one launch" if routed else
+                            "a routing launch, then all layers of a step in one launch") if batched
+                           else "one launch per layer"),
                 "algorithmic_bytes_per_launch": float(per_launch.mean()), "launch_ms": float(ffn_ms.mean()),
                 "layer_ms": float(ffn_ms.sum() / (K * L)),
                 "peak_kind": f"{peak_kind} HBM copy (MEASURED_PEAKS.json hbm_gbs)"}

@@ -371,10 +371,12 @@ int pw_moe_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, int T,
  *    here (layouts as in pw_moe_route_topk), none may be NULL when T > 0;
  *  d_mass_accum fp32 [E] or NULL: the routing mass is added as in
  *    pw_moe_route_topk.
- * On the decode path (T*k < 48*E) one CTA of the fused kernel routes the
- * batch at the start of the launch and the others wait for it (bounded; a
- * timeout sets d_status to PW_ERR_TIMEOUT).  On the prefill path, where one
- * CTA would route too slowly, a routing launch runs first on the same stream.
+ * Batches one warp routes (at most 32 tokens, 8 experts and 4 slots per
+ * token, shared experts included) on the decode path (T*k < 48*E) are routed
+ * by one warp of the fused kernel at the start of the launch while the other
+ * CTAs wait for it (bounded; a timeout sets d_status to PW_ERR_TIMEOUT).
+ * Other batches are routed by a routing launch that runs first on the same
+ * stream.
  * T = 0 writes the offsets (all zero) and nothing else (d_logits may then be
  * NULL).  E and k count the routed experts (the logits' width and top-k);
  * with options->shared_experts = S (the _ex form) routing is that of
@@ -393,7 +395,9 @@ int pw_moe_route_apl_ffn_ex(const void* d_desc, int layer, const uint16_t* d_x, 
                             float* d_mass_accum, void* d_ws, size_t ws_bytes, uint16_t* d_y,
                             int32_t* d_status, const pw_ffn_options* opts, void* stream);
 
-/* Several independent MoE layers in one launch: the routed call of
+/* Several independent MoE layers in one fused launch (plus one routing
+ * launch before it when the layers' batches are larger than one warp routes,
+ * as in pw_moe_route_apl_ffn): the routed call of
  * pw_moe_route_apl_ffn_ex for layers layer0 .. layer0+L-1 of the descriptor
  * array, each with its own T tokens (§3.3's fused kernel, applied to a stack
  * of layers whose inputs are all known, e.g. a decode stack with independent

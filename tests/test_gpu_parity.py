@@ -162,7 +162,9 @@ def _route_gpu(logits, k):
                                         (32, 8, 4, "normal"), (7, 3, 3, "normal"), (32, 4, 2, "ties"),
                                         (31, 8, 2, "ties"), (33, 8, 2, "normal"),
                                         (4096, 8, 2, "zipf"), (2500, 8, 2, "ties"), (3000, 64, 4, "normal"),
-                                        (256, 8, 2, "uniform"), (5, 256, 8, "normal")])
+                                        (256, 8, 2, "uniform"), (5, 256, 8, "normal"),
+                                        (100, 60, 4, "ties"), (40, 128, 8, "ties"), (33, 255, 16, "ties"),
+                                        (2000, 33, 3, "ties"), (64, 40, 1, "normal")])
 def test_route_matches_oracle(T, E, k, kind):
     g = torch.Generator().manual_seed(T + E + k)
     if kind == "zipf":
