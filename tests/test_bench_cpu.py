@@ -88,3 +88,17 @@ def test_pw_arm_without_a_gpu_fails_at_once():
     assert r.returncode != 0
     assert "needs a GPU" in r.stderr
     assert not r.stdout.strip()
+
+
+def test_kernel_routes_follows_the_library_rule():
+    """bench.py brackets the fused launch alone when the library routes in a
+    launch of its own: batches of at most 32 tokens over at most 8 experts
+    with at most 4 slots per token, on the decode path, route in-kernel."""
+    import bench
+    assert bench.kernel_routes(32, 2, 8)            # the 8x7B decode default
+    assert not bench.kernel_routes(33, 2, 8)        # more tokens than one warp routes
+    assert not bench.kernel_routes(128, 2, 8)
+    assert not bench.kernel_routes(32, 8, 64)       # 60 routed + 4 shared experts
+    assert not bench.kernel_routes(32, 9, 129)
+    assert not bench.kernel_routes(32, 5, 8)
+    assert not bench.kernel_routes(4096, 2, 8)      # prefill path
