@@ -157,23 +157,37 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
   }
   __syncthreads();
 
-  // 2) expert offsets (exclusive scan of the counts)
-  if (tid == 0) {
-    int run = 0;
-    for (int e = 0; e < ET; ++e) {
+  // 2) expert offsets (exclusive scan of the counts) by warp 0: lane l scans
+  //    experts [l*n, l*n + n), then a shuffle scan over the lanes' sums
+  if (warp == 0) {
+    const int n = (ET + 31) >> 5, e0 = lane * n;
+    int part = 0;
+    for (int e = e0; e < min(e0 + n, ET); ++e) part += s_cnt[e];
+    int incl = part;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    int run = incl - part;
+    for (int e = e0; e < min(e0 + n, ET); ++e) {
       offsets[e] = base + run;
       s_base[e] = run;
       s_off[e] = run;
       run += s_cnt[e];
     }
-    offsets[ET] = base + run;
-    s_off[ET] = run;
+    if (lane == 31) {
+      offsets[ET] = base + incl;
+      s_off[ET] = incl;
+    }
   }
   __syncthreads();
 
   // 3) stable placement, one token per thread per chunk: the rank of token t
-  //    inside expert e is the number of earlier tokens that also chose e.
-  //    Only the warps that hold tokens of the chunk take part.
+  //    inside expert e is the number of earlier tokens of its warp that also
+  //    chose e (the lanes' bits in the warp's mask for e), plus the counts of
+  //    the earlier warps.  Only the warps that hold tokens of the chunk take
+  //    part; a token picks an expert at most once.
   for (int c0 = 0; c0 < T; c0 += nthreads) {
     const int t = c0 + tid;
     const bool valid = t < T;
@@ -187,17 +201,18 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
     }
     const unsigned lt_mask = (1u << lane) - 1u;
     if (warp < nwa) {
-      for (int e = 0; e < ET; ++e) {
-        bool mine = false;
+      unsigned* wmask = reinterpret_cast<unsigned*>(s_wcnt + warp * ET);   // this warp's row: lane masks
+      for (int e = lane; e < ET; e += 32) wmask[e] = 0u;
+      __syncwarp();
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j) mine |= my[j] == e;   // a token picks an expert at most once
-        const unsigned ball = __ballot_sync(0xffffffffu, mine);
-        const int r = __popc(ball & lt_mask);
+      for (int j = 0; j < kMaxK; ++j)
+        if (my[j] >= 0) atomicOr(&wmask[my[j]], 1u << lane);
+      __syncwarp();
 #pragma unroll
-        for (int j = 0; j < kMaxK; ++j)
-          if (my[j] == e) rank[j] = r;
-        if (lane == 0) s_wcnt[warp * ET + e] = __popc(ball);
-      }
+      for (int j = 0; j < kMaxK; ++j)
+        if (my[j] >= 0) rank[j] = __popc(wmask[my[j]] & lt_mask);
+      __syncwarp();
+      for (int e = lane; e < ET; e += 32) s_wcnt[warp * ET + e] = __popc(wmask[e]);
     }
     __syncthreads();
     for (int e = tid; e < ET; e += nthreads) {
