@@ -57,12 +57,12 @@ int tile_width(int T, int E, int k) {
 }
 
 // Width 2: the CUDA-core instance.
-int launch_width(int width, const Params& p, cudaStream_t s) {
+int launch_width(int width, const Params& p, cudaStream_t s, bool after_route = false) {
   switch (width) {
-    case 2: return pw_ffn::launch_ffn_gemv(p, s);
-    case 16: return pw_ffn::launch_ffn_t16(p, s);
-    case 64: return pw_ffn::launch_ffn_t64(p, s);
-    default: return pw_ffn::launch_ffn_t128(p, s);
+    case 2: return pw_ffn::launch_ffn_gemv(p, s, after_route);
+    case 16: return pw_ffn::launch_ffn_t16(p, s, after_route);
+    case 64: return pw_ffn::launch_ffn_t64(p, s, after_route);
+    default: return pw_ffn::launch_ffn_t128(p, s, after_route);
   }
 }
 
@@ -180,14 +180,18 @@ int ffn_launch(bool routed, const void* d_desc, int layer, int L, const uint16_t
   p.wait_ns = (o.wait_timeout_us ? o.wait_timeout_us : 2000000u) * 1000ull;
   p.flags = o.flags;
   p.linear = 0;
+  const int width = o.kernel == PW_KERNEL_CUDA_CORES ? 2 : tile_width(T, E, k);
   if (routed && (path == PW_PATH_PREFILL || !pw_route::warp_routes(T1, E1, k))) {
     // batches that one warp does not route (more than 32 tokens or 8 experts
     // per layer): a routing launch comes first, so that the fused kernel
-    // holds no CTA-wide routing code and its grid does not wait on one CTA
+    // holds no CTA-wide routing code and its grid does not wait on one CTA;
+    // it also zeroes the fused launch's counters, and the fused kernel starts
+    // while it finishes
     if (int e = pw::route_layers(d_logits, L, T1, ER, kR, S, d_ids, const_cast<float*>(d_w),
                                  const_cast<int32_t*>(d_offsets), const_cast<int32_t*>(d_perm),
-                                 const_cast<int32_t*>(d_inv_perm), d_mass_accum, s))
+                                 const_cast<int32_t*>(d_inv_perm), d_mass_accum, s, p.ctr, W.h - W.ctr))
       return e;
+    return launch_width(width, p, s, true);
   } else if (routed) {
     p.logits = d_logits;
     p.route_shared = S;
@@ -196,7 +200,7 @@ int ffn_launch(bool routed, const void* d_desc, int layer, int L, const uint16_t
     p.mass_accum = d_mass_accum;
   }
   PW_CUDA_TRY(cudaMemsetAsync(p.ctr, 0, W.h - W.ctr, s));
-  return launch_width(o.kernel == PW_KERNEL_CUDA_CORES ? 2 : tile_width(T, E, k), p, s);
+  return launch_width(width, p, s);
 }
 
 }  // namespace

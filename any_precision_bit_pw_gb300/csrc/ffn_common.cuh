@@ -387,9 +387,9 @@ __device__ inline void combine_all(const Params& p, long long tid, long long nth
 
 // Kernel launchers (one translation unit each, ffn_stream.cuh instantiated
 // for 16-, 64- and 128-token tiles).
-int launch_ffn_t16(const Params& p, cudaStream_t s);    // 16-token tiles
-int launch_ffn_t64(const Params& p, cudaStream_t s);    // 64-token tiles
-int launch_ffn_t128(const Params& p, cudaStream_t s);   // 128-token tiles
-int launch_ffn_gemv(const Params& p, cudaStream_t s);   // 2-token tiles on the CUDA cores
+int launch_ffn_t16(const Params& p, cudaStream_t s, bool after_route = false);    // 16-token tiles
+int launch_ffn_t64(const Params& p, cudaStream_t s, bool after_route = false);    // 64-token tiles
+int launch_ffn_t128(const Params& p, cudaStream_t s, bool after_route = false);   // 128-token tiles
+int launch_ffn_gemv(const Params& p, cudaStream_t s, bool after_route = false);   // 2-token tiles on the CUDA cores
 
 }  // namespace pw_ffn

@@ -812,6 +812,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     PW_KERNEL_NAME(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap map_gu,
                       const __grid_constant__ CUtensorMap map_dn) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // launched early after a routing launch: wait for it (and its writes)
+  // before touching global memory; a no-op otherwise
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   Sm sm;
   if (!carve(sm, smem_raw)) {
     if (threadIdx.x == 0) report(p.status, PW_ERR_UNSUPPORTED);   // unexpected shared-window base
@@ -996,7 +999,7 @@ int encode_rows(CUtensorMap* m, const void* base, long long cols, long long rows
 
 }  // namespace
 
-int PW_LAUNCHER_NAME(const Params& p, cudaStream_t s) {
+int PW_LAUNCHER_NAME(const Params& p, cudaStream_t s, bool after_route) {
   static bool attr_done = false;
   if (!attr_done) {
     PW_CUDA_TRY(cudaFuncSetAttribute(PW_KERNEL_NAME, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
@@ -1012,9 +1015,20 @@ int PW_LAUNCHER_NAME(const Params& p, cudaStream_t s) {
     if (int e = encode_rows(&gu, p.xp, p.H, p.A)) return e;
     if (int e = encode_rows(&dn, p.h, p.I, p.A)) return e;
   }
-  // one CTA per SM: it owns all 512 TMEM columns
-  PW_KERNEL_NAME<<<sms, kThreads, kSmemBytes, s>>>(p, gu, dn);
-  PW_CUDA_TRY(cudaGetLastError());
+  // one CTA per SM: it owns all 512 TMEM columns.  After a routing launch
+  // the kernel may start while the routing grid finishes (programmatic
+  // dependent launch; it waits for that grid before it reads anything).
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(sms));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = after_route ? 1 : 0;
+  PW_CUDA_TRY(cudaLaunchKernelEx(&cfg, PW_KERNEL_NAME, p, gu, dn));
   return PW_OK;
 }
 

@@ -42,9 +42,14 @@ inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s
 // Routing of L independent layers in one launch (route.cu): the arrays of
 // layer l start at l*T*E (logits), l*T*(k+S) (ids, w, perm, inv_perm),
 // l*(E+S) (offsets, mass); offsets, perm and inv_perm hold indices into the
-// concatenated assignments of all layers.  Arguments are not checked.
+// concatenated assignments of all layers.  Arguments are not checked.  With
+// d_zero, the launch also zeroes zero_bytes there (16-byte aligned, a
+// multiple of 16: the next fused launch's counters), and it lets the next
+// kernel on the stream start early (programmatic dependent launch: that
+// kernel waits for this grid's completion before it reads anything).
 int route_layers(const float* d_logits, int L, int T, int E, int k, int S, int32_t* d_ids, float* d_w,
-                 int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm, float* d_mass_accum, cudaStream_t s);
+                 int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm, float* d_mass_accum, cudaStream_t s,
+                 void* d_zero = nullptr, size_t zero_bytes = 0);
 
 // Host-side descriptor of `block` of a page table, at its committed bitwidth
 // (or at `bits_override` if > 0); fails unless the planes are attached.

@@ -25,9 +25,15 @@ static_assert(pw_route::scratch_bytes(kMaxE, kWarps) <= kScratch, "routing scrat
 __global__ void __launch_bounds__(kThreads) route_kernel(const float* __restrict__ logits, int T, int E, int k, int S,
                                                          int32_t* __restrict__ ids, float* __restrict__ w,
                                                          int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
-                                                         int32_t* __restrict__ inv_perm, float* __restrict__ mass_accum) {
+                                                         int32_t* __restrict__ inv_perm, float* __restrict__ mass_accum,
+                                                         uint4* __restrict__ zero, int zero_n16) {
   // the required part plus room for the weights of up to ~3400 assignments
   __shared__ __align__(16) uint8_t scratch[kScratch];
+  // the next kernel may start launching (it waits for this grid to complete
+  // before it reads anything this one writes)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  if (blockIdx.x == 0)
+    for (int i = static_cast<int>(threadIdx.x); i < zero_n16; i += kThreads) zero[i] = make_uint4(0u, 0u, 0u, 0u);
   const long long l = blockIdx.x, A = static_cast<long long>(T) * (k + S);
   if (pw_route::warp_routes(T, E + S, k + S)) {   // small batch: one warp, no CTA barrier (same results)
     if (threadIdx.x < 32)
@@ -49,8 +55,10 @@ namespace pw {
 // offsets, permutation and inverse permutation in the concatenated index
 // space of the layers' assignments.
 int route_layers(const float* d_logits, int L, int T, int E, int k, int S, int32_t* d_ids, float* d_w,
-                 int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm, float* d_mass_accum, cudaStream_t s) {
-  route_kernel<<<L, kThreads, 0, s>>>(d_logits, T, E, k, S, d_ids, d_w, d_offsets, d_perm, d_inv_perm, d_mass_accum);
+                 int32_t* d_offsets, int32_t* d_perm, int32_t* d_inv_perm, float* d_mass_accum, cudaStream_t s,
+                 void* d_zero, size_t zero_bytes) {
+  route_kernel<<<L, kThreads, 0, s>>>(d_logits, T, E, k, S, d_ids, d_w, d_offsets, d_perm, d_inv_perm, d_mass_accum,
+                                      static_cast<uint4*>(d_zero), d_zero ? static_cast<int>(zero_bytes / 16) : 0);
   PW_CUDA_TRY(cudaGetLastError());
   return PW_OK;
 }
