@@ -129,8 +129,9 @@ __device__ __forceinline__ bool desc_ok(const BlockDesc& d, int rows, int cols) 
 // ---------------------------------------------------------------------------
 // Unit scheduling (thread 0)
 // ---------------------------------------------------------------------------
+// `offs`: the expert offsets (E + 1 values), staged in shared memory.
 template <int NMAX>
-__device__ void setup_schedule(const Params& p, Shared& sh) {
+__device__ void setup_schedule(const Params& p, const int* offs, Shared& sh) {
   sh.cum_gu[0] = 0;
   sh.cum_dn[0] = 0;
   if (p.linear) {
@@ -142,8 +143,8 @@ __device__ void setup_schedule(const Params& p, Shared& sh) {
   const int gu_strips = 2 * p.I / 128, dn_strips = p.H / 128;
   // the offsets must run from 0 to A without decreasing, or no unit is run
   // (a unit's rows are read and written at these offsets)
-  bool offsets_ok = p.offsets[0] == 0 && p.offsets[p.E] == p.A;
-  for (int e = 0; e < p.E && offsets_ok; ++e) offsets_ok = p.offsets[e + 1] >= p.offsets[e];
+  bool offsets_ok = offs[0] == 0 && offs[p.E] == p.A;
+  for (int e = 0; e < p.E && offsets_ok; ++e) offsets_ok = offs[e + 1] >= offs[e];
   if (!offsets_ok) {
     report(p.status, PW_ERR_INVALID_ARG);
     sh.nact = 0;
@@ -151,7 +152,7 @@ __device__ void setup_schedule(const Params& p, Shared& sh) {
     return;
   }
   for (int e = 0; e < p.E; ++e) {
-    const int ne = p.offsets[e + 1] - p.offsets[e];
+    const int ne = offs[e + 1] - offs[e];
     if (ne <= 0) continue;
     const int g = (ne + NMAX - 1) / NMAX;
     sh.act[n] = e;
@@ -165,6 +166,19 @@ __device__ void setup_schedule(const Params& p, Shared& sh) {
   }
   sh.nact = n;
   sh.arrivals_per_strip = arr;
+}
+
+// The active expert whose run of units holds unit v: the largest i < n with
+// cum[i] <= v, for non-decreasing cum[0..n] with cum[0] = 0 <= v < cum[n]
+// (binary search: up to 256 active experts).
+__device__ __forceinline__ int last_at_most(const int* cum, int n, int v) {
+  int lo = 0, hi = n - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cum[mid] <= v) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
 }
 
 // Strip and token group of the r-th unit of a block of `strips` strips x
@@ -215,7 +229,7 @@ __device__ void next_unit(const Params& p, Shared& sh) {
   const int gu_strips = 2 * p.I / 128, dn_strips = p.H / 128;
   int ai = 0;
   if (t < static_cast<uint32_t>(n_gu)) {
-    while (sh.cum_gu[ai + 1] <= static_cast<int>(t)) ++ai;
+    ai = last_at_most(sh.cum_gu, sh.nact, static_cast<int>(t));
     const int rem = static_cast<int>(t) - sh.cum_gu[ai];
     u.kind = kGateUp;
     u.e = sh.act[ai];
@@ -226,7 +240,7 @@ __device__ void next_unit(const Params& p, Shared& sh) {
     u.nst = p.H / pw::kStageK;
   } else if (t < static_cast<uint32_t>(n_gu + n_dn)) {
     const int v = static_cast<int>(t) - n_gu;
-    while (sh.cum_dn[ai + 1] <= v) ++ai;
+    ai = last_at_most(sh.cum_dn, sh.nact, v);
     const int rem = v - sh.cum_dn[ai];
     u.kind = kDown;
     u.e = sh.act[ai];

@@ -869,6 +869,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     if (*reinterpret_cast<volatile int*>(&st.abort)) return;   // nothing allocated or issued yet
   }
+  // the expert offsets into shared memory (the LUT region: the pipeline has
+  // not started), all threads at once, so that thread 0's schedule set-up
+  // does not wait a global-memory latency per expert
+  int* s_offs = reinterpret_cast<int*>(smem_raw + (sm.region - pw::smem_u32(smem_raw)));
+  if (!p.linear)
+    for (int e = static_cast<int>(threadIdx.x); e <= p.E; e += kThreads) s_offs[e] = p.offsets[e];
+  __syncthreads();
   if (threadIdx.x == 0) {
     for (int i = 0; i < kF; ++i) {
       pw::mbar_init(bar(sm, kBarAFull + i), 4);
@@ -894,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     st.abort = 0;
     st.deq_done = 0;
     st.sched.abort = 0;
-    setup_schedule<kN>(p, st.sched);
+    setup_schedule<kN>(p, s_offs, st.sched);
   }
   if (warp == 0) {
     pw::tmem_alloc(pw::smem_u32(&st.sched.tmem), kTmemCols);
