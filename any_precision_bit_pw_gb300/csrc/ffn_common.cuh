@@ -324,14 +324,18 @@ __device__ __forceinline__ int finish_unit(const Params& p, const Shared& sh, co
   return combine;
 }
 
+// The current device's SM count, looked up once per device (0 on failure).
 inline int sm_count_cached() {
-  static int count = 0;
-  if (count == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  constexpr int kDevs = 64;
+  static int count[kDevs] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 0;
+  int n = dev < kDevs ? count[dev] : 0;
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev < kDevs) count[dev] = n;
   }
-  return count;
+  return n;
 }
 
 // ---------------------------------------------------------------------------

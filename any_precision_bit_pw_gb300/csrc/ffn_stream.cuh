@@ -1007,10 +1007,14 @@ int encode_rows(CUtensorMap* m, const void* base, long long cols, long long rows
 }  // namespace
 
 int PW_LAUNCHER_NAME(const Params& p, cudaStream_t s, bool after_route) {
-  static bool attr_done = false;
-  if (!attr_done) {
+  // the shared-memory opt-in is a per-device attribute of the kernel
+  constexpr int kDevs = 64;
+  static bool attr_done[kDevs] = {};
+  int dev = 0;
+  PW_CUDA_TRY(cudaGetDevice(&dev));
+  if (dev >= kDevs || !attr_done[dev]) {
     PW_CUDA_TRY(cudaFuncSetAttribute(PW_KERNEL_NAME, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes));
-    attr_done = true;
+    if (dev < kDevs) attr_done[dev] = true;
   }
   const int sms = sm_count_cached();
   if (sms < 1) return pw::set_error(PW_ERR_CUDA, "could not query the SM count");
