@@ -29,8 +29,8 @@
 //   scheduler (one thread): takes tickets and publishes units into four slots
 //     ahead of the other roles;
 //   B loader (one thread): each tile's B operand (the N tokens' x or h
-//     columns: two 2-D tensor-map boxes in the 128-byte-swizzled layout the
-//     tensor core reads) into a ring.
+//     columns: one 3-D tensor-map box, both 64-column atoms, in the
+//     128-byte-swizzled layout the tensor core reads) into a ring.
 // Gate_up B rows are the routed tokens' x rows in expert order; every CTA
 // gathers a share of them into the workspace at the start and the B loader
 // waits for all shares before the first gate_up copy.
@@ -444,7 +444,7 @@ __device__ __forceinline__ void plane_loader_role(const Params& p, const Sm sm) 
 }
 
 // ---------------------------------------------------------------------------
-// B loader (one thread): each tile's 16 token rows, two tensor-map boxes
+// B loader (one thread): each tile's N token rows, one tensor-map box
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void b_loader_role(const Params& p, const Sm sm, const void* map_gu, const void* map_dn) {
   DecState& st = *sm.st;
@@ -483,8 +483,7 @@ __device__ __forceinline__ void b_loader_role(const Params& p, const Sm sm, cons
       pw::mbar_arrive_expect_tx(bb, kBBytes);
       const uint32_t dst = st.bring + static_cast<uint32_t>(b) * kBBytes;
       const int col = (tile0 + t) * pw::kTileCols;
-      pw::tma_load_2d(dst, map, col, brow, bb);
-      pw::tma_load_2d(dst + kBAtom, map, col + 64, brow, bb);
+      pw::tma_load_3d(dst, map, 0, brow, col / 64, bb);
     }
     if (!ok) break;
     pw::mbar_arrive(bar(sm, kBarUFree + static_cast<int>(u % kUS)));
@@ -992,11 +991,12 @@ int encode_rows(CUtensorMap* m, const void* base, long long cols, long long rows
       return pw::set_error(PW_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
     fn = reinterpret_cast<EncodeTiled>(f);
   }
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
-  const cuuint32_t box[2] = {64, kN};
-  const cuuint32_t es[2] = {1, 1};
-  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+  // (64 columns of an atom, row, atom): one box holds both atoms of a tile
+  const cuuint64_t dims[3] = {64, static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(cols / 64)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(cols) * 2, 128};
+  const cuuint32_t box[3] = {64, kN, 2};
+  const cuuint32_t es[3] = {1, 1, 1};
+  const CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, kGemv ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
