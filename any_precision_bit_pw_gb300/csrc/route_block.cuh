@@ -1,5 +1,7 @@
-// Top-k routing of one batch by the threads of one CTA: the device function
-// behind pw_moe_route_topk (route.cu) and the routing phase of the fused
+// Top-k routing of one batch: route_block (the threads of one CTA) is the
+// device function behind the routing launch (route.cu: pw_moe_route_topk and
+// the routed fused calls whose batches one warp does not route); route_warp
+// (one warp, small batches) is also the routing phase inside the fused
 // routed layer (ffn_stream.cuh).
 //
 // "PagedWeight" arXiv text, §2.1: the router gives weights to E experts and
@@ -258,8 +260,10 @@ __device__ inline void route_block(const float* __restrict__ logits, int T, int 
 
 // The same routing by one warp, for batches of at most 32 tokens over at most
 // kWarpMaxE experts (routed + shared) with at most kWarpMaxK slots per token:
-// lane t routes token t, counts come from warp ballots, no CTA barrier.  Every result equals route_block's bit for bit:
-// the top-k and weights are the same per-token code, a token's position is
+// lane t routes token t, counts come from warp ballots, no CTA barrier.
+// Every result equals route_block's bit for bit: the top-k and weights are
+// the same per-token code (route_block's one-thread-per-token path for up to
+// 32 experts), a token's position is
 // its expert's offset plus the number of earlier tokens that chose the
 // expert, and the routing mass is summed in the same order (by position,
 // lane-strided, then the same shuffle tree).  Called by all 32 lanes of one
