@@ -311,8 +311,9 @@ def pw_moe_route_apl_ffn(d_desc: torch.Tensor, layer: int, x: torch.Tensor, logi
                          inv_perm: torch.Tensor, mass_accum: Optional[torch.Tensor], ws: torch.Tensor,
                          y: torch.Tensor, status: torch.Tensor, options: Optional[pw_ffn_options] = None,
                          stream=None) -> None:
-    """Routing and the fused expert layer in one launch (the routing arrays
-    are outputs)."""
+    """Routing and the fused expert layer (the routing arrays are outputs):
+    one launch for batches one warp routes (at most 32 tokens, 8 experts and
+    4 slots per token), else a routing launch and the fused launch."""
     _dev(x, torch.float16, "x")
     _dev(y, torch.float16, "y")
     _dev(logits, torch.float32, "logits")
