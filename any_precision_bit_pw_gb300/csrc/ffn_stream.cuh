@@ -826,10 +826,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // warp 0 of CTA l routes layer l of the route_layers layers, writing the
   // routing arrays of all layers in one concatenated index space (the LUT
   // region is its scratch: the pipeline has not started), and counts the
-  // layer as published once its offsets and permutation are written (ids,
-  // weights and routing mass follow; only the combine after the end-of-units
-  // barrier reads the weights); every CTA waits for all layers before it
-  // schedules or gathers (all CTAs are resident: one per SM)
+  // layer as published; every CTA waits for all of them before it schedules
+  // or gathers (all CTAs are resident: one per SM)
   if (p.logits) {
     const int L = p.route_layers, S = p.route_shared;
     const int Tl = p.T / L, ETl = p.E / L;
@@ -843,12 +841,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                                const_cast<int32_t*>(p.offsets) + static_cast<long long>(l) * ETl,
                                const_cast<int32_t*>(p.perm) + l * Al, const_cast<int32_t*>(p.inv_perm) + l * Al,
                                p.mass_accum ? p.mass_accum + static_cast<long long>(l) * ETl : nullptr, scratch,
-                               static_cast<int>(l * Al), p.gather_ctr + 2);
-          __syncwarp();   // the next layer reuses the warp's scratch
+                               static_cast<int>(l * Al));
         } else if (lane == 0) {
           report(p.status, PW_ERR_INVALID_ARG);   // the host routes such batches before the launch
-          atomicAdd(p.gather_ctr + 2, 1u);        // nothing to wait for
         }
+      }
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(p.gather_ctr + 2, 1u);
       }
     }
     if (threadIdx.x == 0) {

@@ -273,12 +273,9 @@ constexpr int kWarpMaxK = 4;
 __host__ __device__ constexpr bool warp_routes(int T, int ET, int K) {
   return T <= 32 && ET <= kWarpMaxE && K <= kWarpMaxK;
 }
-// With `published`, lane 0 adds 1 there (after a GPU-scope fence) as soon as
-// the offsets, perm and inv_perm are written; ids, w and the routing mass are
-// written after it.
 __device__ inline void route_warp(const float* __restrict__ logits, int T, int E, int k, int S, int32_t* ids,
                                   float* w, int32_t* offsets, int32_t* perm, int32_t* inv_perm, float* mass_accum,
-                                  float* s_wpos, int base = 0, uint32_t* published = nullptr) {
+                                  float* s_wpos, int base = 0) {
   const int K = k + S, ET = E + S;
   const int t = static_cast<int>(threadIdx.x & 31);
   const bool valid = t < T;
@@ -322,6 +319,8 @@ __device__ inline void route_warp(const float* __restrict__ logits, int T, int E
       const bool routed = j < k;
       sel[j] = routed ? sel[j] : E + (j - k);
       wsel[j] = routed ? expf(lsel[j] - lsel[0]) / den : 1.0f;
+      ids[static_cast<long long>(t) * K + j] = sel[j];
+      w[static_cast<long long>(t) * K + j] = wsel[j];
     }
   }
   // offsets: an exclusive scan of the per-expert counts (lane e holds expert
@@ -366,18 +365,6 @@ __device__ inline void route_warp(const float* __restrict__ logits, int T, int E
     }
   }
   __syncwarp();
-  if (published && t == 0) {
-    __threadfence();
-    atomicAdd(published, 1u);
-  }
-  if (valid) {
-#pragma unroll
-    for (int j = 0; j < kWarpMaxK; ++j) {
-      if (j >= K) break;
-      ids[static_cast<long long>(t) * K + j] = sel[j];
-      w[static_cast<long long>(t) * K + j] = wsel[j];
-    }
-  }
   // Eq. 1 numerator: per expert, the weights in position order, lane-strided,
   // then the shuffle tree (route_block's order)
   if (mass_accum) {
