@@ -101,10 +101,15 @@ def measured_traffic(kernel: str, workload: str, tokens: int):
         return None
 
 
-def get_workload(name: str, tokens=None):
-    """A named workload, with its token count replaced when `tokens` is given."""
+def get_workload(name: str, tokens=None, bits=None):
+    """A named workload, with its token count replaced when `tokens` is given
+    and every block committed at `bits` when that is given."""
     wl = synth.WORKLOADS[name]
-    return wl.with_(tokens=tokens) if tokens else wl
+    if tokens:
+        wl = wl.with_(tokens=tokens)
+    if bits:
+        wl = wl.with_(bits_mode="fixed", fixed_bits=bits)
+    return wl
 
 
 def ffn_kernel(tokens: int, top_k: int, experts: int) -> str:
@@ -265,7 +270,7 @@ def gpu_arm(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     pw.lib()
-    wl = get_workload(args.workload, args.tokens)
+    wl = get_workload(args.workload, args.tokens, args.bits)
     sh = wl.shape
     li = synth.layer_inputs(wl, device=dev)
     stack = APLMoEStack(sh.hidden, sh.intermediate, sh.experts, sh.top_k, 1, wl.parent_bits, wl.seed_bits, dev,
@@ -397,7 +402,7 @@ def stack_arm(args, rank, world, local_rank):
     dev = torch.device(f"cuda:{local_rank}")
     torch.cuda.set_device(dev)
     pw.lib()
-    wl = get_workload(args.workload, args.tokens)
+    wl = get_workload(args.workload, args.tokens, args.bits)
     sh = wl.shape
     T, H, E, L = wl.tokens, sh.hidden, sh.experts, wl.layers
     batched = not args.per_layer
@@ -613,13 +618,13 @@ def line_config(wl, bits, world: int) -> dict:
                   "hundreds of MB, above the 129 MB L2"}
 
 
-def oracle_workers(workload: str, tokens=None):
+def oracle_workers(workload: str, tokens=None, bits=None):
     """The oracle's layer on the host cores: one process per active expert,
     each holding its expert's gate_up and down blocks as packed bit-planes at
     the committed bitwidths (seeded CPU draws of the workload's
     distributions)."""
     from oracle import apl, parallel
-    wl = get_workload(workload, tokens)
+    wl = get_workload(workload, tokens, bits)
     sh = wl.shape
     x = synth.activations(wl).numpy()
     r = apl.route_topk_shared(synth.router_logits(wl).numpy(), sh.top_k, sh.shared)
@@ -641,12 +646,12 @@ def _sample_text(wl, ew, frac: float) -> str:
             f"expert on {ew.cores} host cores ({ew.threads_per_worker} BLAS threads each){per}")
 
 
-def oracle_baseline(workload: str, tokens=None, passes: int = 1) -> dict:
+def oracle_baseline(workload: str, tokens=None, passes: int = 1, bits=None) -> dict:
     """CPU baseline: wall time of whole-layer oracle passes (one by default:
     a pass of the 8x7B layer is about 20 s of CPU work); tokens/s of the job
     step (a stack step is its layers one after another, so its time is the
     layer's times the layer count)."""
-    wl, files, ew = oracle_workers(workload, tokens)
+    wl, files, ew = oracle_workers(workload, tokens, bits)
     try:
         times = [ew.step(1.0) for _ in range(passes)]
     finally:
@@ -657,14 +662,14 @@ def oracle_baseline(workload: str, tokens=None, passes: int = 1) -> dict:
             "sample": _sample_text(wl, ew, 1.0) + (f"; median of {passes} passes" if passes > 1 else "; one pass")}
 
 
-def oracle_reference_steps(workload: str, steps: int, warmup: int, tokens=None) -> dict:
+def oracle_reference_steps(workload: str, steps: int, warmup: int, tokens=None, bits=None) -> dict:
     """The reference arm's steps: each step is a timed oracle pass over the
     layer (every active expert at once, as in oracle_baseline), or, when K + W
     whole-layer passes would not end within REF_BUDGET_S, over the same first
     fraction of every block's rows.  A step processes that fraction of the
     job step (one layer of a stack step), so the line's tokens/s is
     T * fraction / step time."""
-    wl, files, ew = oracle_workers(workload, tokens)
+    wl, files, ew = oracle_workers(workload, tokens, bits)
     try:
         t_full = ew.step(1.0)
         n = max(1, steps) + max(0, warmup)
@@ -678,19 +683,23 @@ def oracle_reference_steps(workload: str, steps: int, warmup: int, tokens=None) 
     return {"step_s": times, "frac": frac / wl.layers, "cores": ew.cores, "sample": _sample_text(wl, ew, frac)}
 
 
-def _child_cmd(workload: str, tokens=None) -> list:
+def _child_cmd(workload: str, tokens=None, bits=None) -> list:
     cmd = [sys.executable, os.path.abspath(__file__), "--cpu-baseline-child", "--workload", workload]
-    return cmd + ["--tokens", str(tokens)] if tokens else cmd
+    if tokens:
+        cmd += ["--tokens", str(tokens)]
+    if bits:
+        cmd += ["--bits", str(bits)]
+    return cmd
 
 
 def _child_env() -> dict:
     return dict(os.environ, CUDA_VISIBLE_DEVICES="")
 
 
-def cpu_baseline(workload: str, tokens=None) -> dict:
+def cpu_baseline(workload: str, tokens=None, bits=None) -> dict:
     """The oracle's whole layer on the host cores, in a child process started
     before this process touches the GPU."""
-    r = subprocess.run(_child_cmd(workload, tokens), env=_child_env(), capture_output=True, text=True, timeout=900)
+    r = subprocess.run(_child_cmd(workload, tokens, bits), env=_child_env(), capture_output=True, text=True, timeout=900)
     if r.returncode != 0:
         return {"value": None, "unit": UNIT, "cores": None, "kind": "oracle", "sample": "failed: " + r.stderr[-300:]}
     d = json.loads(r.stdout.strip().splitlines()[-1])
@@ -701,8 +710,8 @@ def cpu_baseline(workload: str, tokens=None) -> dict:
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
-    wl = get_workload(args.workload, args.tokens)
-    cmd = _child_cmd(args.workload, args.tokens) + ["--steps", str(max(1, args.steps)), "--warmup",
+    wl = get_workload(args.workload, args.tokens, args.bits)
+    cmd = _child_cmd(args.workload, args.tokens, args.bits) + ["--steps", str(max(1, args.steps)), "--warmup",
                                                     str(max(0, args.warmup)), "--reference-child"]
     r = subprocess.run(cmd, env=_child_env(), capture_output=True, text=True, timeout=1800)
     if r.returncode != 0:
@@ -733,6 +742,8 @@ def main():
     ap.add_argument("--impl", default="pw", choices=["pw", "reference"])
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--tokens", type=int, default=None, help="replace the workload's token count")
+    ap.add_argument("--bits", type=int, default=None,
+                    help="commit every block at this bitwidth (from the seed to the parent bitwidth)")
     ap.add_argument("--offload", action="store_true",
                     help="stack workload: lowering copies the released pages to pinned host memory first (§3.3)")
     ap.add_argument("--sweep", default=None, help="also run the uniform-bitwidth sweep, JSON to this path")
@@ -746,10 +757,11 @@ def main():
         args.warmup = 3
 
     if args.cpu_baseline_child and args.reference_child:
-        print(json.dumps(oracle_reference_steps(args.workload, args.steps, args.warmup, tokens=args.tokens)))
+        print(json.dumps(oracle_reference_steps(args.workload, args.steps, args.warmup, tokens=args.tokens,
+                                                bits=args.bits)))
         return
     if args.cpu_baseline_child:
-        print(json.dumps(oracle_baseline(args.workload, tokens=args.tokens)))
+        print(json.dumps(oracle_baseline(args.workload, tokens=args.tokens, bits=args.bits)))
         return
 
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -767,7 +779,7 @@ def main():
     # the CPU baseline runs in a child process started before this process touches the GPU
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.workload, args.tokens)
+        cpu = cpu_baseline(args.workload, args.tokens, args.bits)
     if world > 1:
         torch.distributed.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     arm = stack_arm if synth.WORKLOADS[args.workload].layers > 1 else gpu_arm

@@ -102,3 +102,12 @@ def test_kernel_routes_follows_the_library_rule():
     assert not bench.kernel_routes(32, 9, 129)
     assert not bench.kernel_routes(32, 5, 8)
     assert not bench.kernel_routes(4096, 2, 8)      # prefill path
+
+
+def test_bits_option_commits_every_block_at_that_bitwidth():
+    import bench
+    from any_precision_bit_pw_gb300 import synth
+    wl = bench.get_workload("mixtral8x7b_uniform_sweep", 8, 3)
+    assert wl.tokens == 8 and set(synth.committed_bits(wl)) == {3}
+    assert "--bits" in bench._child_cmd("mixtral8x7b_uniform_sweep", 8, 3)
+    assert bench.get_workload("mixtral8x7b_decode_mixed").tokens == 32
